@@ -1,0 +1,101 @@
+"""Seeded synthetic inputs for the gated delta rule.
+
+This module only draws random inputs; it holds none of the recurrence's
+arithmetic, so the CUDA path and the float64 oracle can both be fed from it.
+
+The workloads follow the shapes the "marcsun13/ggml-gated-delta-net" model
+card measures on (section "Measured": 32 value heads, head_dim 128, one
+token per step, 24 layers) plus batched decode and long prefill of the same
+head geometry.  Distributions:
+  q, k   ~ N(0, 1), then L2-normalised per (sequence, token, head) in fp32
+  v      ~ N(0, 1)
+  beta   = sigmoid(N(0, 1))
+  g      = -softplus(N(0, 1) + gate_shift)   (log-domain gate, always <= 0)
+  state  ~ N(0, state_std) fp32, [value][key]; state_std 0 means zeros
+q, k, v are cast to the workload dtype (bf16 or fp32) after normalisation;
+g, beta and the state stay fp32.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int                # n_seqs
+    T: int                # n_tokens
+    H: int                # n_heads (one key head per value head)
+    d: int                # head_dim
+    dtype: str            # "f32" or "bf16" for q, k, v
+    gate_shift: float     # g = -softplus(N(0,1) + gate_shift)
+    state_std: float      # 0 -> zero initial state
+    layers: int = 1       # independent layers (distinct states) per step
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+TINY = Workload("tiny_b1_t64_h4_d32_f32", 1, 64, 4, 32, "f32", 0.0, 0.0, seed=0)
+DECODE_24L = Workload("decode_b1_h32_d128_bf16_24layers", 1, 1, 32, 128, "bf16", 0.0, 0.02,
+                      layers=24, seed=1)
+DECODE_B64 = Workload("decode_b64_h32_d128_bf16", 64, 1, 32, 128, "bf16", 0.0, 0.02, seed=2)
+PREFILL_4K = Workload("prefill_b1_t4096_h32_d128_bf16", 1, 4096, 32, 128, "bf16", 2.0, 0.0, seed=3)
+PREFILL_16K = Workload("prefill_b8_t16384_h32_d128_bf16", 8, 16384, 32, 128, "bf16", 2.0, 0.02,
+                       seed=4)
+PREFILL_16K_D64 = PREFILL_16K.replace(name="prefill_b8_t16384_h64_d64_bf16", H=64, d=64, seed=5)
+PREFILL_16K_D256 = PREFILL_16K.replace(name="prefill_b8_t16384_h16_d256_bf16", H=16, d=256, seed=6)
+
+ALL = [TINY, DECODE_24L, DECODE_B64, PREFILL_4K, PREFILL_16K, PREFILL_16K_D64, PREFILL_16K_D256]
+BY_NAME = {w.name: w for w in ALL}
+
+
+def _gen(seed: int, device):
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return gen
+
+
+def make_inputs(w: Workload, device="cpu", layer: int = 0, B: int | None = None,
+                T: int | None = None, seed: int | None = None):
+    """Draw one layer's inputs for workload ``w`` on ``device``.
+
+    Returns a dict with q, k, v (B, T, H, d) in the workload dtype, g, beta
+    (B, T, H) fp32 and state (B, H, d, d) fp32 or None.  ``B``/``T`` override
+    the workload's sizes (same distributions), ``layer`` selects one of the
+    workload's independent layers."""
+    B = w.B if B is None else B
+    T = w.T if T is None else T
+    s = (w.seed if seed is None else seed) * 1000 + layer
+    gen = _gen(s, device)
+    H, d = w.H, w.d
+    shape = (B, T, H, d)
+    q = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    q = q / q.norm(dim=-1, keepdim=True)
+    k = k / k.norm(dim=-1, keepdim=True)
+    v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    beta = torch.sigmoid(torch.randn((B, T, H), generator=gen, device=device))
+    g = -torch.nn.functional.softplus(
+        torch.randn((B, T, H), generator=gen, device=device) + w.gate_shift)
+    state = None
+    if w.state_std > 0:
+        state = torch.randn((B, H, d, d), generator=gen, device=device) * w.state_std
+    dt = w.torch_dtype
+    return {"q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(), "v": v.to(dt).contiguous(),
+            "g": g.contiguous(), "beta": beta.contiguous(), "state": state}
+
+
+def to_numpy_f32(inputs):
+    """fp32 numpy copies (exact for bf16) of a ``make_inputs`` dict."""
+    out = {}
+    for key, val in inputs.items():
+        out[key] = None if val is None else val.detach().float().cpu().numpy()
+    return out

@@ -1,0 +1,160 @@
+/*
+ * Oracle for the gated delta rule: a plain, slow, float64 CPU recurrence.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; it exists so that tests, the smoke check and the CPU
+ * baseline in the benchmark can compare the CUDA library against an
+ * independent computation of the same definition.  It shares no code with
+ * the CUDA sources.
+ *
+ * What it computes (one independent problem per (sequence, head) pair):
+ *
+ *   S_0 = state_in[b,h]            (d x d, S[i][j]: i = value index, j = key index)
+ *   for t = 0 .. T-1:
+ *     alpha = exp(g[b,t,h])        (the gate arrives in the log domain and is
+ *                                   exponentiated here)
+ *     S <- alpha * S                                   -- gating (decay)
+ *     r <- S k_t                                        -- what the memory says for k_t
+ *     S <- S + beta_t (v_t - r) k_t^T                   -- delta rule: overwrite
+ *     o_t <- S q_t / sqrt(d)                            -- output from the updated state
+ *   state_out[b,h] = S
+ *
+ * which is S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and
+ * o_t = S_t q_t / sqrt(d) written step by step.
+ *
+ * Sources:
+ *   - "Gated Delta Net on AMD: why ROCm stumbles on hybrid-attention LLMs",
+ *     section "What Gated Delta Net is, in plain language": the delta rule
+ *     overwrites the part of the running summary that new information
+ *     contradicts; the gate scales how much of the old summary is kept.
+ *   - "marcsun13/ggml-gated-delta-net" model card, section "Ops": one call
+ *     covers a whole run of steps, (q, k, v, g, beta, state) -> (out,
+ *     final_state); shapes q,k,v (n_seqs, n_tokens, n_heads, head_dim),
+ *     g,beta (n_seqs, n_tokens, n_heads), state (n_seqs, n_heads, d, d);
+ *     state indexed [value][key], a fresh state is zeros; one key head per
+ *     value head; the output carries 1/sqrt(head_dim); g is a log-domain gate.
+ *
+ * Inputs are float32 (bf16 data is upcast exactly by the caller); every
+ * operation is done in double.  No blocking, no reordering beyond the
+ * definition above, no fast-math.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* One (sequence, head) problem.  Element strides are given so the caller can
+ * pass the (b, h) slice of a (B, T, H, d) array without copying:
+ *   q/k/v/out: token t, component i at [t * tok_stride + i]
+ *   g/beta:    token t at [t * gate_stride]
+ *   state:     S[i][j] at [i * d + j]                                      */
+static void oracle_one_head(const float *q, const float *k, const float *v,
+                            const float *g, const float *beta,
+                            long tok_stride, long gate_stride,
+                            const float *state_in, double *out,
+                            double *state_out, int T, int d, double *S,
+                            double *r)
+{
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    for (int i = 0; i < d; ++i)
+        for (int j = 0; j < d; ++j)
+            S[(size_t)i * d + j] = state_in ? (double)state_in[(size_t)i * d + j] : 0.0;
+
+    for (int t = 0; t < T; ++t) {
+        const float *qt = q + (size_t)t * tok_stride;
+        const float *kt = k + (size_t)t * tok_stride;
+        const float *vt = v + (size_t)t * tok_stride;
+        const double alpha = exp((double)g[(size_t)t * gate_stride]);
+        const double b = (double)beta[(size_t)t * gate_stride];
+
+        /* gating: S <- alpha S */
+        for (size_t e = 0; e < (size_t)d * d; ++e)
+            S[e] *= alpha;
+        /* r = S k */
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j)
+                acc += S[(size_t)i * d + j] * (double)kt[j];
+            r[i] = acc;
+        }
+        /* delta rule: S <- S + beta (v - r) k^T */
+        for (int i = 0; i < d; ++i) {
+            const double c = b * ((double)vt[i] - r[i]);
+            for (int j = 0; j < d; ++j)
+                S[(size_t)i * d + j] += c * (double)kt[j];
+        }
+        /* o = S q / sqrt(d) */
+        double *ot = out + (size_t)t * tok_stride;
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int j = 0; j < d; ++j)
+                acc += S[(size_t)i * d + j] * (double)qt[j];
+            ot[i] = acc * inv_sqrt_d;
+        }
+    }
+    memcpy(state_out, S, sizeof(double) * (size_t)d * d);
+}
+
+/* Full problem, all (b, h) pairs.  Layouts as on the model card:
+ *   q, k, v, out : (B, T, H, d) contiguous
+ *   g, beta      : (B, T, H) contiguous
+ *   state_in     : (B, H, d, d) contiguous, [value][key]; NULL means zeros
+ *   state_out    : (B, H, d, d) contiguous, [value][key]
+ * n_threads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad sizes or
+ * an allocation failure (outputs are then unspecified).                    */
+int gdn_oracle_forward(const float *q, const float *k, const float *v,
+                       const float *g, const float *beta,
+                       const float *state_in, double *out, double *state_out,
+                       int B, int T, int H, int d, int n_threads)
+{
+    if (B < 0 || T < 0 || H < 0 || d <= 0)
+        return -1;
+    const long tok_stride = (long)H * d;
+    const long gate_stride = H;
+    const long n_pairs = (long)B * H;
+    int failed = 0;
+#ifdef _OPENMP
+    if (n_threads > 0)
+        omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+#pragma omp parallel
+    {
+        double *S = (double *)malloc(sizeof(double) * (size_t)d * d);
+        double *r = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!S || !r) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (long p = 0; p < n_pairs; ++p) {
+            if (!S || !r)
+                continue;
+            const long b = p / H, h = p % H;
+            const size_t in_off = (size_t)b * T * H * d + (size_t)h * d;
+            const size_t gb_off = (size_t)b * T * H + (size_t)h;
+            const size_t st_off = (size_t)p * d * d;
+            oracle_one_head(q + in_off, k + in_off, v + in_off, g + gb_off,
+                            beta + gb_off, tok_stride, gate_stride,
+                            state_in ? state_in + st_off : NULL,
+                            out + in_off, state_out + st_off, T, d, S, r);
+        }
+        free(S);
+        free(r);
+    }
+    return failed ? -1 : 0;
+}
+
+/* Number of threads an OpenMP parallel region would use (for reporting). */
+int gdn_oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
