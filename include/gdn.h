@@ -1,0 +1,159 @@
+/*
+ * gdn.h -- C ABI of the GB300 (sm_103a) gated-delta-rule library, libgdn.so.
+ *
+ * The operation (one call = a whole run of steps for every sequence and head):
+ *
+ *   for each sequence b and head h, starting from S = state_in[b,h]:
+ *     for t = 0 .. n_tokens-1:
+ *       S   = exp(g[b,t,h]) * S * (I - beta[b,t,h] k k^T) + beta[b,t,h] v k^T
+ *       out[b,t,h,:] = S q / sqrt(head_dim)
+ *     state_out[b,h] = S
+ *   with q, k, v the vectors q[b,t,h,:], k[b,t,h,:], v[b,t,h,:].
+ *
+ * Sources:
+ *   - "marcsun13/ggml-gated-delta-net" model card, section "Ops": the op is
+ *     one dispatch for a whole run of gated-delta-rule steps with signature
+ *     (q, k, v, g, beta, state) -> (out, final_state); the shape table
+ *     (q, k, v: (n_seqs, n_tokens, n_heads, head_dim); g, beta: (n_seqs,
+ *     n_tokens, n_heads); state: (n_seqs, n_heads, head_dim, head_dim));
+ *     the contract notes under it: one key head per value head (identity
+ *     mapping), state indexed [value][key] and returned in the same layout,
+ *     a fresh state is zeros, the output carries 1/sqrt(head_dim), g is a
+ *     log-domain gate that the kernel exponentiates, and the head_dim
+ *     capability query.
+ *   - "marcsun13/ggml-gated-delta-net" model card, section "Where the kernels
+ *     come from": work is enqueued on the caller's queue, never as a
+ *     separate submission.  Here: every call only enqueues on `stream`.
+ *   - "Gated Delta Net on AMD: why ROCm stumbles on hybrid-attention LLMs",
+ *     section "What Gated Delta Net is, in plain language": delta rule
+ *     (overwrite what new information contradicts) plus a gate (how much
+ *     of the old state is kept).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *     row-major in the torch order above.  q, k, v, out, state_in and
+ *     state_out must be 16-byte aligned; g and beta 4-byte aligned.
+ *   - g and beta are float32.  state_in / state_out are float32 [value][key].
+ *     out is float32 (n_seqs, n_tokens, n_heads, head_dim), already scaled.
+ *   - state_in may be NULL: the initial state is then zeros.
+ *   - state_out == state_in (the same pointer) updates the state in place.
+ *     Any other overlap between an output (out, state_out) and any other
+ *     buffer is rejected with GDN_ERR_ALIAS.
+ *   - q and k are used as given: the op does not L2-normalise them.
+ *   - Sizes: n_seqs, n_heads >= 0, n_tokens >= 0.  A call with n_seqs == 0 or
+ *     n_heads == 0 does nothing.  n_tokens == 0 copies state_in (or zeros)
+ *     into state_out and writes no output.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and never synchronise the host.
+ *   - Return value: GDN_OK (0), or a negative GDN_ERR_* code.  Argument
+ *     errors are detected on the host before anything is enqueued: nothing
+ *     is launched and nothing is written.  GDN_ERR_CUDA reports a failed
+ *     launch or enqueue (the CUDA error is then available from
+ *     cudaGetLastError-like queries by the caller).  Faults that happen
+ *     later on the device are reported by gdn_get_device_status().
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t. */
+typedef struct CUstream_st *gdn_stream_t;
+
+enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_ARG = -1,       /* NULL pointer for a non-empty tensor, negative size, size overflow */
+    GDN_ERR_HEADDIM = -2,   /* head_dim not supported on the requested path (see gdn_supports) */
+    GDN_ERR_ALIGN = -3,     /* pointer misaligned (16 B for tensors, 4 B for g/beta) */
+    GDN_ERR_ALIAS = -4,     /* an output overlaps an input or the other output */
+    GDN_ERR_CUDA = -5,      /* a CUDA launch / enqueue / allocation call failed */
+    GDN_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (gdn_get_device_status) */
+    GDN_ERR_WORKSPACE = -7, /* caller workspace NULL, too small or misaligned */
+    GDN_ERR_NOMEM = -8      /* stream-ordered workspace allocation failed */
+};
+
+/* dtype of q, k, v */
+enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 };
+
+/* execution path; AUTO picks by n_tokens and head_dim */
+enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 };
+
+/*
+ * gdn_forward -- the op with float32 q, k, v.
+ * q, k, v: (n_seqs, n_tokens, n_heads, head_dim) float32.  Other arguments as
+ * described above.  Uses the AUTO path; if that path needs a workspace it is
+ * taken from cudaMallocAsync on `stream` and released on `stream` (stream
+ * ordered, no host synchronisation).
+ */
+int gdn_forward(const float *q, const float *k, const float *v,
+                const float *g, const float *beta, const float *state_in,
+                float *out, float *state_out,
+                int n_seqs, int n_tokens, int n_heads, int head_dim,
+                gdn_stream_t stream);
+
+/* gdn_forward_bf16 -- as gdn_forward with bfloat16 q, k, v (raw 16-bit
+ * words, __nv_bfloat16 layout).  Computation is float32 with exact upcast. */
+int gdn_forward_bf16(const void *q, const void *k, const void *v,
+                     const float *g, const float *beta, const float *state_in,
+                     float *out, float *state_out,
+                     int n_seqs, int n_tokens, int n_heads, int head_dim,
+                     gdn_stream_t stream);
+
+/*
+ * gdn_forward_ex -- explicit dtype, path and workspace.
+ * dtype: GDN_DTYPE_*; path: GDN_PATH_*.
+ * workspace: caller-owned device buffer of at least
+ *   gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype, path)
+ *   bytes, 256-byte aligned; or NULL, in which case the call allocates and
+ *   frees it stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ * The workspace contents on entry are ignored; on return they are garbage.
+ * Two calls in flight at once must not share a workspace.
+ */
+int gdn_forward_ex(const void *q, const void *k, const void *v,
+                   const float *g, const float *beta, const float *state_in,
+                   float *out, float *state_out,
+                   int n_seqs, int n_tokens, int n_heads, int head_dim,
+                   int dtype, int path, void *workspace, size_t workspace_bytes,
+                   gdn_stream_t stream);
+
+/* Bytes of device workspace gdn_forward_ex needs for these sizes, dtype and
+ * path (0 when the selected path needs none).  Returns 0 on invalid sizes. */
+size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
+                           int dtype, int path);
+
+/* Which path AUTO selects for these sizes (GDN_PATH_RECURRENT or
+ * GDN_PATH_CHUNKED), or a negative GDN_ERR_* for unsupported sizes. */
+int gdn_select_path(int n_tokens, int head_dim);
+
+/*
+ * gdn_supports -- capability query, the counterpart of the model card's
+ * supports_gated_delta_net(head_dim) ("Ops" table and the note that the
+ * head dim must be asked, not assumed).  Returns a bit mask: bit 0 (1) =
+ * the recurrent path supports head_dim, bit 1 (2) = the chunked path does.
+ * 0 means unsupported.  Supported: 32 (recurrent), 64, 128, 256 (both).
+ */
+int gdn_supports(int head_dim);
+
+/*
+ * gdn_get_device_status -- synchronises `stream`, then returns and clears
+ * the library's device status word on the current device: GDN_OK, or
+ * GDN_ERR_TIMEOUT if a kernel's bounded wait gave up since the last query.
+ * Returns GDN_ERR_CUDA if the synchronisation itself failed.
+ */
+int gdn_get_device_status(gdn_stream_t stream);
+
+/* Static English text for a status code (never NULL). */
+const char *gdn_status_string(int status);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+int gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

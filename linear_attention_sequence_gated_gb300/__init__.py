@@ -1,0 +1,164 @@
+"""GB300 (sm_103a) gated delta rule: Python binding of libgdn.so.
+
+This module only marshals arguments: it checks torch tensors, takes their
+device pointers and the current CUDA stream, and calls the C ABI declared in
+``include/gdn.h``.  Every step of the computation runs in the library's CUDA
+kernels; there is no CPU or PyTorch fallback.  If ``libgdn.so`` has not been
+built (``python -m linear_attention_sequence_gated_gb300._build``) every
+call raises.
+
+    out, final_state = forward(q, k, v, g, beta, state)
+
+q, k, v: (n_seqs, n_tokens, n_heads, head_dim) bf16 or fp32 CUDA tensors,
+g, beta: (n_seqs, n_tokens, n_heads) fp32, state: (n_seqs, n_heads, head_dim,
+head_dim) fp32 [value][key] or None (zeros).  out is fp32 and already carries
+1/sqrt(head_dim).  ("marcsun13/ggml-gated-delta-net" model card, section
+"Ops" and its shape table.)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdn.so")
+
+OK = 0
+ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NOMEM = \
+    -1, -2, -3, -4, -5, -6, -7, -8
+DTYPE_F32, DTYPE_BF16 = 0, 1
+PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
+
+# Every symbol include/gdn.h declares.
+EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
+           "gdn_select_path", "gdn_supports", "gdn_get_device_status", "gdn_status_string",
+           "gdn_version"]
+
+_lib = None
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str = "gdn"):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)} ({status})")
+
+
+def lib():
+    """The loaded libgdn.so (ctypes), raising if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libgdn.so not found at {LIB_PATH}; build it with "
+                "`python -m linear_attention_sequence_gated_gb300._build` (no fallback exists)")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, fp, i, sz = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        fwd = [vp, vp, vp, fp, fp, fp, fp, fp, i, i, i, i]
+        L.gdn_forward.argtypes = fwd + [vp]
+        L.gdn_forward_bf16.argtypes = fwd + [vp]
+        L.gdn_forward_ex.argtypes = fwd + [i, i, vp, sz, vp]
+        for f in (L.gdn_forward, L.gdn_forward_bf16, L.gdn_forward_ex):
+            f.restype = i
+        L.gdn_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        L.gdn_workspace_bytes.restype = sz
+        L.gdn_select_path.argtypes = [i, i]
+        L.gdn_select_path.restype = i
+        L.gdn_supports.argtypes = [i]
+        L.gdn_supports.restype = i
+        L.gdn_get_device_status.argtypes = [vp]
+        L.gdn_get_device_status.restype = i
+        L.gdn_status_string.argtypes = [i]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_version.restype = i
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def supports(head_dim: int) -> int:
+    """Bit mask: 1 = recurrent path, 2 = chunked path, 0 = unsupported."""
+    return int(lib().gdn_supports(int(head_dim)))
+
+
+def select_path(n_tokens: int, head_dim: int) -> str:
+    r = int(lib().gdn_select_path(int(n_tokens), int(head_dim)))
+    if r < 0:
+        raise GdnError(r, "gdn_select_path")
+    return {v: k for k, v in PATHS.items()}[r]
+
+
+def workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype="bf16", path="auto") -> int:
+    dt = DTYPE_BF16 if dtype in ("bf16", "bfloat16") else DTYPE_F32
+    return int(lib().gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dt, PATHS[path]))
+
+
+def device_status(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device status word."""
+    return int(lib().gdn_get_device_status(_stream_handle(stream)))
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str = "auto",
+            workspace=None, stream=None):
+    """Run the gated delta rule over every token of every sequence.
+
+    Returns (out, final_state).  ``state_out`` may be ``state`` itself for
+    an in-place update.  ``workspace`` is an optional uint8 CUDA tensor of at
+    least ``workspace_bytes(...)`` bytes; without it the library allocates
+    stream-ordered scratch when the chosen path needs any."""
+    import torch
+    L = lib()
+    if q.dtype == torch.bfloat16:
+        dt = DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dt = DTYPE_F32
+    else:
+        raise TypeError(f"q/k/v must be bf16 or fp32, got {q.dtype}")
+    if q.dim() != 4:
+        raise ValueError("q must be (n_seqs, n_tokens, n_heads, head_dim)")
+    B, T, H, d = q.shape
+    for name, t, shape, dtype in (("k", k, (B, T, H, d), q.dtype), ("v", v, (B, T, H, d), q.dtype),
+                                  ("g", g, (B, T, H), torch.float32),
+                                  ("beta", beta, (B, T, H), torch.float32)):
+        if tuple(t.shape) != shape or t.dtype != dtype:
+            raise ValueError(f"{name}: expected {shape} {dtype}, got {tuple(t.shape)} {t.dtype}")
+    tensors = [q, k, v, g, beta]
+    if state is not None:
+        if tuple(state.shape) != (B, H, d, d) or state.dtype != torch.float32:
+            raise ValueError("state must be (n_seqs, n_heads, head_dim, head_dim) fp32")
+        tensors.append(state)
+    if out is None:
+        out = torch.empty((B, T, H, d), dtype=torch.float32, device=q.device)
+    if state_out is None:
+        state_out = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device)
+    tensors += [out, state_out]
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if tuple(out.shape) != (B, T, H, d) or out.dtype != torch.float32:
+        raise ValueError("out must be (n_seqs, n_tokens, n_heads, head_dim) fp32")
+    if tuple(state_out.shape) != (B, H, d, d) or state_out.dtype != torch.float32:
+        raise ValueError("state_out must be (n_seqs, n_heads, head_dim, head_dim) fp32")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    with torch.cuda.device(q.device):
+        rc = L.gdn_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                              _ptr(out), _ptr(state_out), B, T, H, d, dt, PATHS[path],
+                              ws_ptr, ws_bytes, _stream_handle(stream))
+    if rc != OK:
+        raise GdnError(rc, "gdn_forward_ex")
+    return out, state_out

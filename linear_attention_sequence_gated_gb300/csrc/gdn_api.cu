@@ -1,0 +1,254 @@
+// C-ABI front end of libgdn.so: argument validation, path selection,
+// workspace handling and the device status word.  Every compute step runs in
+// the kernels of gdn_recurrent.cu and gdn_chunked.cu; this file launches
+// nothing else.  Declarations and the full contract are in include/gdn.h.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+// Device status word: kernels whose waits are bounded write GDN_ERR_TIMEOUT
+// here when a wait gives up.  One per device that loads the library.
+__device__ int g_device_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+int *status_word_for_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+// Bytes spanned by a dense tensor of `n` elements of `elt` bytes; false on overflow.
+bool span_bytes(unsigned long long n, unsigned long long elt, unsigned long long *out) {
+    if (n != 0 && elt > ULLONG_MAX / n) return false;
+    *out = n * elt;
+    return *out < (1ull << 62);
+}
+
+bool mul_ok(unsigned long long a, unsigned long long b, unsigned long long *out) {
+    if (a != 0 && b > ULLONG_MAX / a) return false;
+    *out = a * b;
+    return true;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+bool overlap(Range a, Range b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+Range range_of(const void *p, unsigned long long bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return {lo, p ? lo + (uintptr_t)bytes : lo};
+}
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tokens from which AUTO prefers the chunked path.
+constexpr int kChunkedMinTokens = 64;
+
+int select_path(int n_tokens, int head_dim) {
+    const int caps = gdn_supports(head_dim);
+    if (!caps) return GDN_ERR_HEADDIM;
+    if ((caps & 2) && n_tokens >= kChunkedMinTokens) return GDN_PATH_CHUNKED;
+    return GDN_PATH_RECURRENT;
+}
+
+struct Sizes {
+    unsigned long long qkv_bytes, gb_bytes, state_bytes, out_bytes;
+};
+
+// Host-side validation; fills `sz`.  Launches nothing.
+int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
+             const float *state_in, const float *out, const float *state_out, int B, int T,
+             int H, int d, int dtype, int path, Sizes *sz) {
+    if (B < 0 || T < 0 || H < 0 || d <= 0) return GDN_ERR_ARG;
+    if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_ARG;
+    if (path != GDN_PATH_AUTO && path != GDN_PATH_RECURRENT && path != GDN_PATH_CHUNKED)
+        return GDN_ERR_ARG;
+    const int caps = gdn_supports(d);
+    if (!caps) return GDN_ERR_HEADDIM;
+    if (path == GDN_PATH_RECURRENT && !(caps & 1)) return GDN_ERR_HEADDIM;
+    if (path == GDN_PATH_CHUNKED && !(caps & 2)) return GDN_ERR_HEADDIM;
+
+    unsigned long long bth, bthd, bh, bhdd;
+    if (!mul_ok((unsigned long long)B * (unsigned long long)T, (unsigned long long)H, &bth))
+        return GDN_ERR_ARG;
+    if (!mul_ok(bth, (unsigned long long)d, &bthd)) return GDN_ERR_ARG;
+    bh = (unsigned long long)B * (unsigned long long)H;
+    if (!mul_ok(bh, (unsigned long long)d * (unsigned long long)d, &bhdd)) return GDN_ERR_ARG;
+    if (bh > (unsigned long long)INT_MAX) return GDN_ERR_ARG;  // one block row per (b, h)
+    const unsigned long long elt = dtype == GDN_DTYPE_BF16 ? 2 : 4;
+    if (!span_bytes(bthd, elt, &sz->qkv_bytes) || !span_bytes(bth, 4, &sz->gb_bytes) ||
+        !span_bytes(bhdd, 4, &sz->state_bytes) || !span_bytes(bthd, 4, &sz->out_bytes))
+        return GDN_ERR_ARG;
+
+    if (bh == 0) return GDN_OK;  // nothing to do, nothing to check
+    if (!state_out) return GDN_ERR_ARG;
+    if (bth > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_ARG;
+
+    const uintptr_t A16 = 16;
+    if (!aligned(state_out, A16) || (state_in && !aligned(state_in, A16))) return GDN_ERR_ALIGN;
+    if (bth > 0) {
+        if (!aligned(q, A16) || !aligned(k, A16) || !aligned(v, A16) || !aligned(out, A16))
+            return GDN_ERR_ALIGN;
+        if (!aligned(g, 4) || !aligned(beta, 4)) return GDN_ERR_ALIGN;
+    }
+
+    const Range rq = range_of(q, sz->qkv_bytes), rk = range_of(k, sz->qkv_bytes),
+                rv = range_of(v, sz->qkv_bytes), rg = range_of(g, sz->gb_bytes),
+                rb = range_of(beta, sz->gb_bytes), rsi = range_of(state_in, sz->state_bytes),
+                ro = range_of(out, bth > 0 ? sz->out_bytes : 0),
+                rso = range_of(state_out, sz->state_bytes);
+    for (Range in : {rq, rk, rv, rg, rb, rsi, rso})
+        if (overlap(ro, in)) return GDN_ERR_ALIAS;
+    for (Range in : {rq, rk, rv, rg, rb})
+        if (overlap(rso, in)) return GDN_ERR_ALIAS;
+    if (state_in && state_in != state_out && overlap(rso, rsi)) return GDN_ERR_ALIAS;
+    return GDN_OK;
+}
+
+int run(const void *q, const void *k, const void *v, const float *g, const float *beta,
+        const float *state_in, float *out, float *state_out, int B, int T, int H, int d,
+        int dtype, int path, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Sizes sz{};
+    int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, T, H, d, dtype, path, &sz);
+    if (rc != GDN_OK) return rc;
+    if ((long long)B * H == 0) return GDN_OK;
+
+    if (T == 0) {  // no steps: the final state is the initial state
+        cudaError_t e;
+        if (!state_in)
+            e = cudaMemsetAsync(state_out, 0, sz.state_bytes, stream);
+        else if (state_in != state_out)
+            e = cudaMemcpyAsync(state_out, state_in, sz.state_bytes, cudaMemcpyDeviceToDevice,
+                                stream);
+        else
+            e = cudaSuccess;
+        return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+
+    if (path == GDN_PATH_AUTO) path = select_path(T, d);
+    const size_t need =
+        path == GDN_PATH_CHUNKED ? gdn::chunked_workspace_bytes(B, T, H, d, dtype) : 0;
+    if (need > 0 && workspace && (workspace_bytes < need || !aligned(workspace, 256)))
+        return GDN_ERR_WORKSPACE;
+
+    // Everything above is host-only validation; CUDA is touched from here on.
+    int *status = status_word_for_current_device();
+    if (!status) return GDN_ERR_CUDA;
+
+    gdn::Problem p{q, k, v, g, beta, state_in, out, state_out, B, T, H, d, dtype,
+                   (float)(1.0 / std::sqrt((double)d)), status};
+
+    if (path == GDN_PATH_RECURRENT) {
+        return gdn::launch_recurrent(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+
+    void *ws = workspace;
+    bool owned = false;
+    if (need > 0 && !ws) {
+        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return GDN_ERR_NOMEM;
+        owned = true;
+    }
+    const cudaError_t e = gdn::launch_chunked(p, ws, need, stream);
+    if (owned) {
+        const cudaError_t f = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess && f != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_forward(const float *q, const float *k, const float *v, const float *g,
+                const float *beta, const float *state_in, float *out, float *state_out,
+                int n_seqs, int n_tokens, int n_heads, int head_dim, gdn_stream_t stream) {
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
+               GDN_DTYPE_F32, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gdn_forward_bf16(const void *q, const void *k, const void *v, const float *g,
+                     const float *beta, const float *state_in, float *out, float *state_out,
+                     int n_seqs, int n_tokens, int n_heads, int head_dim, gdn_stream_t stream) {
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
+               GDN_DTYPE_BF16, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gdn_forward_ex(const void *q, const void *k, const void *v, const float *g,
+                   const float *beta, const float *state_in, float *out, float *state_out,
+                   int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype, int path,
+                   void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
+               dtype, path, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype,
+                           int path) {
+    if (n_seqs < 0 || n_tokens < 0 || n_heads < 0 || head_dim <= 0) return 0;
+    if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return 0;
+    if (n_tokens == 0 || (long long)n_seqs * n_heads == 0) return 0;
+    if (path == GDN_PATH_AUTO) path = select_path(n_tokens, head_dim);
+    if (path != GDN_PATH_CHUNKED) return 0;
+    if (!(gdn_supports(head_dim) & 2)) return 0;
+    return gdn::chunked_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype);
+}
+
+int gdn_select_path(int n_tokens, int head_dim) {
+    if (n_tokens < 0) return GDN_ERR_ARG;
+    return select_path(n_tokens, head_dim);
+}
+
+int gdn_supports(int head_dim) {
+    int caps = 0;
+    if (head_dim == 32 || head_dim == 64 || head_dim == 128 || head_dim == 256) caps |= 1;
+    if (gdn::chunked_supports(head_dim)) caps |= 2;
+    return caps;
+}
+
+int gdn_get_device_status(gdn_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_device_status, sizeof(int)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess)
+        return GDN_ERR_CUDA;
+    return value;
+}
+
+const char *gdn_status_string(int status) {
+    switch (status) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_ARG: return "invalid argument (null pointer, negative size or size overflow)";
+        case GDN_ERR_HEADDIM: return "head_dim not supported on the requested path";
+        case GDN_ERR_ALIGN: return "misaligned pointer (16 B for tensors, 4 B for g/beta)";
+        case GDN_ERR_ALIAS: return "an output overlaps an input or the other output";
+        case GDN_ERR_CUDA: return "CUDA launch or enqueue failed";
+        case GDN_ERR_TIMEOUT: return "a bounded device wait gave up";
+        case GDN_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+        case GDN_ERR_NOMEM: return "stream-ordered workspace allocation failed";
+        default: return "unknown status";
+    }
+}
+
+int gdn_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,33 @@
+// Internal interface between the C-ABI front end (gdn_api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace gdn {
+
+// One validated call.  All pointers are device pointers; sizes are >= 1.
+struct Problem {
+    const void *q, *k, *v;         // (B, T, H, d), dtype below
+    const float *g, *beta;         // (B, T, H)
+    const float *state_in;         // (B, H, d, d) [value][key] or nullptr (zeros)
+    float *out;                    // (B, T, H, d) fp32, scaled by 1/sqrt(d)
+    float *state_out;              // (B, H, d, d) [value][key]; may equal state_in
+    int B, T, H, d;
+    int dtype;                     // GDN_DTYPE_F32 / GDN_DTYPE_BF16
+    float scale;                   // (float)(1 / sqrt((double)d))
+    int *status;                   // device status word (bounded waits report here)
+};
+
+// Recurrent path (gdn_recurrent.cu): any T >= 1, d in {32, 64, 128, 256}.
+cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);
+
+// Chunked path (gdn_chunked.cu): T >= 1, d in {64, 128, 256}.
+size_t chunked_workspace_bytes(int B, int T, int H, int d, int dtype);
+cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream);
+bool chunked_supports(int d);
+
+}  // namespace gdn

@@ -1,0 +1,236 @@
+// Recurrent (token-by-token) path of the gated delta rule: the decode kernel.
+//
+// For one (sequence, head) the value rows of the state are independent of
+// each other: row i of S (the keys seen from value component i) evolves as
+//     s_k   = S[i,:] . k          s_q = S[i,:] . q          kq = k . q
+//     alpha = exp(g)
+//     delta = beta * (v_i - alpha * s_k)
+//     S[i,:] <- alpha * S[i,:] + delta * k
+//     o_i    = (alpha * s_q + delta * kq) / sqrt(d)
+// which is S_t = alpha S_{t-1}(I - beta k k^T) + beta v k^T, o = S_t q / sqrt(d)
+// restricted to one row: both dot products use the row before the update, so
+// a single fused reduction per token serves the read (S k), the output (S q)
+// and k.q.  ("marcsun13/ggml-gated-delta-net" model card, section "Ops":
+// state [value][key] keeps a row contiguous, the output carries
+// 1/sqrt(head_dim), g is exponentiated by the kernel.)
+//
+// Mapping on sm_103a: L lanes hold one state row in registers, each lane
+// NV 128-bit vectors (4 fp32 keys) interleaved so that every load
+// instruction of a warp covers whole 128-byte lines; a warp holds
+// R * (32 / L) rows; a 128-thread block holds 4 warps' rows of one head.
+// The row is loaded once, kept in registers for the whole token run, and
+// written once: the state streams through HBM exactly once per call.  q, k,
+// v, g, beta of the next token are prefetched while the current one is
+// computed.
+#include <cuda_bf16.h>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+// Raw 4-element vectors as loaded from memory.
+struct Raw4F32 { float4 x; };
+struct Raw4BF16 { uint2 x; };
+
+template <typename Tin> struct RawOf;
+template <> struct RawOf<float> { using type = Raw4F32; };
+template <> struct RawOf<__nv_bfloat16> { using type = Raw4BF16; };
+
+__device__ __forceinline__ Raw4F32 load_raw4(const float *p) {
+    return {__ldg(reinterpret_cast<const float4 *>(p))};
+}
+__device__ __forceinline__ Raw4BF16 load_raw4(const __nv_bfloat16 *p) {
+    return {__ldg(reinterpret_cast<const uint2 *>(p))};
+}
+__device__ __forceinline__ void unpack4(const Raw4F32 &r, float (&x)[4]) {
+    x[0] = r.x.x; x[1] = r.x.y; x[2] = r.x.z; x[3] = r.x.w;
+}
+// bf16 -> fp32 is exact: the bf16 word is the upper half of the fp32 word.
+__device__ __forceinline__ void unpack4(const Raw4BF16 &r, float (&x)[4]) {
+    x[0] = __uint_as_float(r.x.x << 16);
+    x[1] = __uint_as_float(r.x.x & 0xffff0000u);
+    x[2] = __uint_as_float(r.x.y << 16);
+    x[3] = __uint_as_float(r.x.y & 0xffff0000u);
+}
+__device__ __forceinline__ float load_scalar(const float *p) { return __ldg(p); }
+__device__ __forceinline__ float load_scalar(const __nv_bfloat16 *p) {
+    return __bfloat162float(__ldg(p));
+}
+
+template <int D, int L, int R, typename Tin>
+struct TokenInputs {
+    static constexpr int NV = D / (4 * L);
+    typename RawOf<Tin>::type q[NV], k[NV];
+    float v[R];
+    float g, beta;
+};
+
+template <int D, int L, int R, typename Tin>
+__global__ void __launch_bounds__(128)
+recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                 const Tin *__restrict__ v, const float *__restrict__ g,
+                 const float *__restrict__ beta, const float *state_in,
+                 float *state_out, float *__restrict__ out, int T, int H,
+                 float scale)
+{
+    constexpr int NV = D / (4 * L);   // 128-bit vectors per lane per row
+    constexpr int RU = 32 / L;        // rows per warp unit
+    constexpr int RW = R * RU;        // rows per warp
+    constexpr int RB = 4 * RW;        // rows per block
+    static_assert(D % RB == 0, "rows per block must divide head_dim");
+    static_assert(NV >= 1 && D == NV * 4 * L, "bad lane split");
+
+    const int bh = blockIdx.x;  // b * H + h
+    const int b = bh / H;
+    const int h = bh - b * H;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % L;
+    const int grp = lane / L;
+    const int row0 = blockIdx.y * RB + warp * RW + grp;  // unit u owns row0 + u*RU
+
+    // ---- state rows into registers --------------------------------------
+    float s[R][NV][4];
+    const size_t st_base = (size_t)bh * D * D;
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (state_in) {
+                const float4 t = __ldcs(reinterpret_cast<const float4 *>(
+                    state_in + st_base + (size_t)(row0 + u * RU) * D + (j * L + sub) * 4));
+                s[u][j][0] = t.x; s[u][j][1] = t.y; s[u][j][2] = t.z; s[u][j][3] = t.w;
+            } else {
+                s[u][j][0] = s[u][j][1] = s[u][j][2] = s[u][j][3] = 0.f;
+            }
+        }
+    }
+
+    const size_t tok_stride = (size_t)H * D;                 // between tokens of one head
+    const size_t in_base = ((size_t)b * T * H + h) * D;      // token 0 of (b, h)
+    const size_t gb_base = (size_t)b * T * H + h;
+    const Tin *qp = q + in_base;
+    const Tin *kp = k + in_base;
+    const Tin *vp = v + in_base;
+    const float *gp = g + gb_base;
+    const float *bp = beta + gb_base;
+    float *op = out + in_base;
+
+    using In = TokenInputs<D, L, R, Tin>;
+    auto load_token = [&](int t, In &x) {
+        const size_t o = (size_t)t * tok_stride;
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            x.q[j] = load_raw4(qp + o + (j * L + sub) * 4);
+            x.k[j] = load_raw4(kp + o + (j * L + sub) * 4);
+        }
+#pragma unroll
+        for (int u = 0; u < R; ++u) x.v[u] = load_scalar(vp + o + row0 + u * RU);
+        x.g = __ldg(gp + (size_t)t * H);
+        x.beta = __ldg(bp + (size_t)t * H);
+    };
+
+    In cur;
+    load_token(0, cur);
+    for (int t = 0; t < T; ++t) {
+        In nxt;
+        if (t + 1 < T) load_token(t + 1, nxt);
+
+        float qv[NV][4], kv[NV][4];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) { unpack4(cur.q[j], qv[j]); unpack4(cur.k[j], kv[j]); }
+
+        float kq = 0.f, pk[R], pq[R];
+#pragma unroll
+        for (int u = 0; u < R; ++u) { pk[u] = 0.f; pq[u] = 0.f; }
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kq = fmaf(kv[j][e], qv[j][e], kq);
+#pragma unroll
+                for (int u = 0; u < R; ++u) {
+                    pk[u] = fmaf(s[u][j][e], kv[j][e], pk[u]);
+                    pq[u] = fmaf(s[u][j][e], qv[j][e], pq[u]);
+                }
+            }
+        }
+        // butterfly over the L lanes of each row group: every lane gets the sums
+#pragma unroll
+        for (int off = L / 2; off > 0; off >>= 1) {
+            kq += __shfl_xor_sync(0xffffffffu, kq, off);
+#pragma unroll
+            for (int u = 0; u < R; ++u) {
+                pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], off);
+                pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], off);
+            }
+        }
+
+        const float alpha = expf(cur.g);
+        const size_t o = (size_t)t * tok_stride;
+#pragma unroll
+        for (int u = 0; u < R; ++u) {
+            const float delta = cur.beta * (cur.v[u] - alpha * pk[u]);
+#pragma unroll
+            for (int j = 0; j < NV; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s[u][j][e] = fmaf(alpha, s[u][j][e], delta * kv[j][e]);
+            const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
+            if (sub == 0) op[o + row0 + u * RU] = ov;
+        }
+        if (t + 1 < T) cur = nxt;
+    }
+
+    // ---- state rows back --------------------------------------------------
+#pragma unroll
+    for (int u = 0; u < R; ++u)
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            __stcs(reinterpret_cast<float4 *>(state_out + st_base + (size_t)(row0 + u * RU) * D +
+                                              (j * L + sub) * 4),
+                   make_float4(s[u][j][0], s[u][j][1], s[u][j][2], s[u][j][3]));
+}
+
+template <int D, int L, int R, typename Tin>
+cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
+    constexpr int RB = 4 * R * (32 / L);
+    dim3 grid((unsigned)p.B * (unsigned)p.H, D / RB);
+    recurrent_kernel<D, L, R, Tin><<<grid, 128, 0, stream>>>(
+        static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
+        static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H,
+        p.scale);
+    return cudaGetLastError();
+}
+
+template <int D, int L, typename Tin>
+cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
+    // Two rows per warp unit when there are enough blocks to fill the GPU
+    // several times over (more bytes in flight per thread); one otherwise.
+    constexpr int RB2 = 4 * 2 * (32 / L);
+    const long long blocks2 = (long long)p.B * p.H * (D / RB2);
+    if (D % RB2 == 0 && blocks2 >= 4 * 152) return launch_one<D, L, 2, Tin>(p, stream);
+    return launch_one<D, L, 1, Tin>(p, stream);
+}
+
+template <typename Tin>
+cudaError_t launch_dtype(const Problem &p, cudaStream_t stream) {
+    switch (p.d) {
+        case 32: return launch_one<32, 8, 1, Tin>(p, stream);
+        case 64: return launch_d<64, 8, Tin>(p, stream);
+        case 128: return launch_d<128, 8, Tin>(p, stream);
+        case 256: return launch_d<256, 16, Tin>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
+    if (p.dtype == GDN_DTYPE_BF16) return launch_dtype<__nv_bfloat16>(p, stream);
+    return launch_dtype<float>(p, stream);
+}
+
+}  // namespace gdn

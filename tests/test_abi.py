@@ -1,0 +1,134 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/gdn.h declares, answers the capability / workspace / path
+queries, and rejects bad arguments on the host before touching CUDA.
+
+Every call here that passes (made-up) device addresses is one the library
+must reject during host validation; no call in this file can reach a launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_sequence_gated_gb300 as gdn
+from linear_attention_sequence_gated_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return gdn.lib()
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(gdn_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_symbols()
+    assert "gdn_forward" in names and "gdn_forward_bf16" in names
+    for n in names:
+        assert hasattr(L, n), f"libgdn.so does not export {n}"
+    assert set(names) == set(gdn.EXPORTS)
+
+
+def test_library_is_built_for_sm_103a():
+    # the compile flags pin the single target architecture
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.NVCC_FLAGS)
+
+
+def test_supports(L):
+    assert gdn.supports(32) & 1
+    for d in (64, 128, 256):
+        assert gdn.supports(d) & 1
+    for d in (0, -1, 16, 48, 96, 100, 192, 512):
+        assert gdn.supports(d) == 0
+
+
+def test_status_strings(L):
+    for code in range(-8, 1):
+        s = gdn.status_string(code)
+        assert s and s != "unknown status"
+    assert gdn.status_string(-99) == "unknown status"
+    assert L.gdn_version() >= 100
+
+
+def test_workspace_and_path_queries(L):
+    assert L.gdn_workspace_bytes(1, 1, 32, 128, 1, 1) == 0          # recurrent needs none
+    assert L.gdn_workspace_bytes(-1, 1, 32, 128, 1, 0) == 0         # invalid sizes -> 0
+    assert L.gdn_workspace_bytes(1, 0, 32, 128, 1, 0) == 0          # no tokens -> 0
+    assert gdn.select_path(1, 128) == "recurrent"
+    assert gdn.select_path(5, 32) == "recurrent"
+    assert L.gdn_select_path(10, 48) == gdn.ERR_HEADDIM
+    assert L.gdn_select_path(-1, 128) == gdn.ERR_ARG
+
+
+# fake, well-aligned device addresses; every call below must fail validation
+BASE = 1 << 40
+MB = 1 << 20
+
+
+def call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, g=BASE + 192 * MB,
+         beta=BASE + 256 * MB, s_in=BASE + 320 * MB, out=BASE + 512 * MB,
+         s_out=BASE + 768 * MB, B=1, T=4, H=2, d=64, dtype=1, path=0, ws=None, ws_bytes=0):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.gdn_forward_ex(p(q), p(k), p(v), p(g), p(beta), p(s_in), p(out), p(s_out),
+                            B, T, H, d, dtype, path, p(ws), ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), gdn.ERR_ARG), (dict(T=-1), gdn.ERR_ARG), (dict(H=-2), gdn.ERR_ARG),
+    (dict(d=0), gdn.ERR_ARG), (dict(dtype=7), gdn.ERR_ARG), (dict(path=9), gdn.ERR_ARG),
+    (dict(d=48), gdn.ERR_HEADDIM), (dict(d=96), gdn.ERR_HEADDIM), (dict(d=512), gdn.ERR_HEADDIM),
+    (dict(q=None), gdn.ERR_ARG), (dict(k=None), gdn.ERR_ARG), (dict(v=None), gdn.ERR_ARG),
+    (dict(g=None), gdn.ERR_ARG), (dict(beta=None), gdn.ERR_ARG), (dict(out=None), gdn.ERR_ARG),
+    (dict(s_out=None), gdn.ERR_ARG),
+    (dict(q=BASE + 8), gdn.ERR_ALIGN), (dict(v=BASE + 128 * MB + 4), gdn.ERR_ALIGN),
+    (dict(out=BASE + 512 * MB + 2), gdn.ERR_ALIGN), (dict(s_in=BASE + 320 * MB + 8), gdn.ERR_ALIGN),
+    (dict(s_out=BASE + 768 * MB + 4), gdn.ERR_ALIGN), (dict(g=BASE + 192 * MB + 2), gdn.ERR_ALIGN),
+    (dict(out=BASE), gdn.ERR_ALIAS),                         # out on top of q
+    (dict(out=BASE + 256 * MB), gdn.ERR_ALIAS),              # out on top of beta
+    (dict(out=BASE + 768 * MB), gdn.ERR_ALIAS),              # out == state_out
+    (dict(s_out=BASE + 64 * MB), gdn.ERR_ALIAS),             # state_out on k
+    (dict(s_out=BASE + 320 * MB + 16), gdn.ERR_ALIAS),       # partial overlap with state_in
+    (dict(s_out=BASE + 192 * MB), gdn.ERR_ALIAS),            # state_out on g
+    (dict(B=1 << 20, T=1 << 20, H=1 << 20, d=256), gdn.ERR_ARG),   # size overflow
+    (dict(B=70000, H=70000, T=1), gdn.ERR_ARG),              # more (b, h) pairs than a grid row
+])
+def test_host_validation_rejects(L, kw, code):
+    assert call(L, **kw) == code
+
+
+def test_recurrent_path_rejects_unsupported_headdim(L):
+    assert call(L, d=48, path=1) == gdn.ERR_HEADDIM
+
+
+def test_empty_batch_is_a_no_op(L):
+    # n_seqs == 0 or n_heads == 0: nothing to do, no pointer needed, no CUDA call
+    assert call(L, B=0, q=None, k=None, v=None, g=None, beta=None, out=None, s_out=None) == gdn.OK
+    assert call(L, H=0, q=None, k=None, v=None, g=None, beta=None, out=None, s_out=None) == gdn.OK
+
+
+def test_typed_entry_points_validate(L):
+    p = ctypes.c_void_p
+    assert L.gdn_forward(p(BASE), p(BASE), p(BASE), p(BASE + 8), p(BASE), None, p(BASE),
+                         p(BASE), 1, 1, 1, 48, None) == gdn.ERR_HEADDIM
+    assert L.gdn_forward_bf16(p(BASE), p(BASE), p(BASE), p(BASE), p(BASE), None, None,
+                              p(BASE + 4096), 1, 1, 1, 64, None) == gdn.ERR_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(gdn, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(gdn, "_lib", None)
+    with pytest.raises(RuntimeError, match="libgdn.so not found"):
+        gdn.lib()

@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA library (called through its C ABI via the binding)
+against the float64 oracle on the same seeded inputs.
+
+Metric: max |gpu - oracle| / RMS(oracle) over the whole compared tensor,
+separately for out and final_state.  Bounds: 1e-4 for fp32 q/k/v and 3e-3 for
+bf16 q/k/v.  The recurrent path computes in fp32 throughout, so it is also
+held to 1e-4 for bf16 inputs (their upcast is exact).
+
+Workloads follow the shapes measured on the "marcsun13/ggml-gated-delta-net"
+model card (section "Measured": 32 value heads x head_dim 128, one token per
+step, 24 layers) plus batched decode and long prefill; see
+linear_attention_sequence_gated_gb300/workloads.py for the distributions.
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_sequence_gated_gb300 as gdn
+from linear_attention_sequence_gated_gb300 import workloads as W
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 3e-3}
+TOL_RECURRENT = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from linear_attention_sequence_gated_gb300 import _build
+    _build.build()
+    oracle.build()
+
+
+def run_gpu(inp, path="auto", state_out=None):
+    out, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                          path=path, state_out=state_out)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    return out, st
+
+
+def run_oracle(inp):
+    n = W.to_numpy_f32(inp)
+    return oracle.recurrent_c(n["q"], n["k"], n["v"], n["g"], n["beta"], n["state"])
+
+
+def errs(out, st, ref_out, ref_st):
+    return (oracle.parity_error(out.double().cpu().numpy(), ref_out),
+            oracle.parity_error(st.double().cpu().numpy(), ref_st))
+
+
+def check(inp, dtype, path="auto", tol=None):
+    out, st = run_gpu(inp, path)
+    ref_out, ref_st = run_oracle(inp)
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    tol = TOL[dtype] if tol is None else tol
+    assert e_out <= tol and e_st <= tol, (e_out, e_st, tol)
+    return e_out, e_st
+
+
+def paths_for(d, T):
+    caps = gdn.supports(d)
+    ps = []
+    if caps & 1:
+        ps.append("recurrent")
+    if caps & 2:
+        ps.append("chunked")
+    return ps
+
+
+# ---------------------------------------------------------------- workloads
+
+def test_tiny_workload_all_paths():
+    w = W.TINY
+    inp = W.make_inputs(w, "cuda")
+    for path in ["auto"] + paths_for(w.d, w.T):
+        tol = TOL_RECURRENT if path == "recurrent" else TOL[w.dtype]
+        check(inp, w.dtype, path, tol)
+
+
+def test_decode_24_layers():
+    w = W.DECODE_24L
+    for layer in range(w.layers):
+        inp = W.make_inputs(w, "cuda", layer=layer)
+        check(inp, w.dtype, "auto", TOL_RECURRENT)
+
+
+def test_batched_decode_b64():
+    w = W.DECODE_B64
+    inp = W.make_inputs(w, "cuda")
+    check(inp, w.dtype, "auto", TOL_RECURRENT)
+
+
+@pytest.mark.parametrize("path", ["auto", "recurrent", "chunked"])
+def test_prefill_4k_full(path):
+    w = W.PREFILL_4K
+    if path == "chunked" and not gdn.supports(w.d) & 2:
+        pytest.skip("chunked path not built")
+    inp = W.make_inputs(w, "cuda")
+    check(inp, w.dtype, path, TOL_RECURRENT if path == "recurrent" else None)
+
+
+def sampled_pairs(w, n):
+    r = np.random.default_rng(1234)
+    pairs = {(0, 0), (w.B - 1, w.H - 1)}
+    while len(pairs) < n:
+        pairs.add((int(r.integers(w.B)), int(r.integers(w.H))))
+    return sorted(pairs)
+
+
+@pytest.mark.parametrize("wname", [W.PREFILL_16K.name, W.PREFILL_16K_D64.name,
+                                   W.PREFILL_16K_D256.name])
+@pytest.mark.parametrize("path", ["auto", "recurrent"])
+def test_long_prefill_full_size_sampled(wname, path):
+    """Full-size launch (the configuration the benchmark times); the oracle
+    recomputes every output and the final state of a sample of (sequence,
+    head) pairs, which are independent problems."""
+    w = W.BY_NAME[wname]
+    inp = W.make_inputs(w, "cuda")
+    out, st = run_gpu(inp, path)
+    tol = TOL_RECURRENT if path == "recurrent" else TOL[w.dtype]
+    outs, refs, sts, ref_sts = [], [], [], []
+    for b, h in sampled_pairs(w, 6):
+        sl = {key: (None if val is None else
+                    (val[b:b + 1, :, h:h + 1] if val.dim() >= 3 and key != "state"
+                     else val[b:b + 1, h:h + 1]))
+              for key, val in inp.items()}
+        ro, rs = run_oracle(sl)
+        outs.append(out[b, :, h].double().cpu().numpy().ravel())
+        refs.append(ro.ravel())
+        sts.append(st[b, h].double().cpu().numpy().ravel())
+        ref_sts.append(rs.ravel())
+    e_out = oracle.parity_error(np.concatenate(outs), np.concatenate(refs))
+    e_st = oracle.parity_error(np.concatenate(sts), np.concatenate(ref_sts))
+    assert e_out <= tol and e_st <= tol, (e_out, e_st)
+
+
+# ------------------------------------------------------ shapes and dtypes
+
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("T", [1, 2, 7, 63, 64, 65, 200])
+def test_head_dims_dtypes_lengths(d, dtype, T):
+    w = W.Workload("matrix", 2, T, 3, d, dtype, 0.0, 0.02, seed=77)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    for path in ["auto"] + paths_for(d, T):
+        out, st = run_gpu(inp, path)
+        e_out, e_st = errs(out, st, ref_out, ref_st)
+        tol = TOL_RECURRENT if path == "recurrent" else TOL[dtype]
+        assert e_out <= tol and e_st <= tol, (path, e_out, e_st)
+
+
+@pytest.mark.parametrize("shift", [-2.0, 2.0, 6.0])
+def test_gate_regimes(shift):
+    """Slow (alpha ~ 0.88), fast (~0.12) and near-total (~0.002) decay."""
+    w = W.Workload("gates", 1, 300, 4, 128, "bf16", shift, 0.02, seed=31)
+    inp = W.make_inputs(w, "cuda")
+    for path in paths_for(w.d, w.T):
+        check(inp, "bf16", path, TOL_RECURRENT if path == "recurrent" else None)
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_extreme_gates_and_betas():
+    """g = 0 (no decay), g = -inf (total reset), g = -1e4, beta = 0 and 1."""
+    w = W.Workload("edge", 1, 130, 2, 64, "f32", 0.0, 0.05, seed=5)
+    inp = W.make_inputs(w, "cuda")
+    g, beta = inp["g"], inp["beta"]
+    g[:, 0:10] = 0.0
+    g[:, 17] = -float("inf")
+    g[:, 70] = -1e4
+    beta[:, 20:30] = 0.0
+    beta[:, 40:45] = 1.0
+    for path in paths_for(w.d, w.T):
+        check(inp, "f32", path, TOL["f32"])
+
+
+def test_null_state_means_zeros():
+    w = W.Workload("z", 2, 9, 3, 64, "bf16", 0.0, 0.0, seed=9)
+    inp = W.make_inputs(w, "cuda")
+    assert inp["state"] is None
+    check(inp, "bf16", "recurrent", TOL_RECURRENT)
+    zeros = dict(inp, state=torch.zeros(2, 3, 64, 64, device="cuda"))
+    o1, s1 = run_gpu(inp)
+    o2, s2 = run_gpu(zeros)
+    assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
+def test_in_place_state_update():
+    w = W.Workload("inplace", 2, 5, 4, 128, "bf16", 0.0, 0.02, seed=10)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    st = inp["state"].clone()
+    out, st2 = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st, state_out=st)
+    torch.cuda.synchronize()
+    assert st2.data_ptr() == st.data_ptr()
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL_RECURRENT and e_st <= TOL_RECURRENT
+
+
+def test_zero_tokens_copies_state():
+    w = W.Workload("t0", 2, 1, 2, 64, "f32", 0.0, 0.02, seed=11)
+    inp = W.make_inputs(w, "cuda")
+    e = lambda x: x[:, :0].contiguous()
+    out, st = gdn.forward(e(inp["q"]), e(inp["k"]), e(inp["v"]), e(inp["g"]), e(inp["beta"]),
+                          inp["state"])
+    torch.cuda.synchronize()
+    assert out.numel() == 0 and torch.equal(st, inp["state"])
+    out, st = gdn.forward(e(inp["q"]), e(inp["k"]), e(inp["v"]), e(inp["g"]), e(inp["beta"]), None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(st) == 0
+
+
+def test_state_carry_across_calls():
+    """[0, T) in one call == [0, T1) then [T1, T) with the state fed back,
+    including splits that are not chunk-aligned."""
+    w = W.Workload("carry", 2, 300, 4, 128, "bf16", 0.0, 0.02, seed=12)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    for t1 in (1, 64, 100, 257):
+        a = {key: (val[:, :t1].contiguous() if key != "state" else val) for key, val in inp.items()}
+        b = {key: (val[:, t1:].contiguous() if key != "state" else None) for key, val in inp.items()}
+        oa, sa = run_gpu(a)
+        b["state"] = sa
+        ob, sb = run_gpu(b)
+        e_out, e_st = errs(torch.cat([oa, ob], dim=1), sb, ref_out, ref_st)
+        assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (t1, e_out, e_st)
+
+
+def test_no_writes_outside_outputs():
+    """Outputs sit inside NaN-filled guard regions that must stay untouched."""
+    w = W.Workload("guard", 2, 70, 3, 64, "bf16", 0.0, 0.02, seed=13)
+    inp = W.make_inputs(w, "cuda")
+    B, T, H, d = 2, 70, 3, 64
+    pad = 4096
+    for path in paths_for(d, T):
+        ob = torch.full((B * T * H * d + 2 * pad,), float("nan"), device="cuda")
+        sb = torch.full((B * H * d * d + 2 * pad,), float("nan"), device="cuda")
+        out = ob[pad:pad + B * T * H * d].view(B, T, H, d)
+        st = sb[pad:pad + B * H * d * d].view(B, H, d, d)
+        gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                    out=out, state_out=st, path=path)
+        torch.cuda.synchronize()
+        for buf in (ob, sb):
+            assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all(), path
+        assert torch.isfinite(out).all() and torch.isfinite(st).all()
+
+
+def test_rejects_bad_arguments_without_launching():
+    """out overlapping state_in is rejected on the host; nothing is written."""
+    w = W.Workload("bad", 1, 4, 2, 64, "bf16", 0.0, 0.02, seed=14)
+    inp = W.make_inputs(w, "cuda")
+    before = inp["state"].clone()
+    bad_out = inp["state"].view(-1)[: 1 * 4 * 2 * 64].view(1, 4, 2, 64)
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                    out=bad_out)
+    torch.cuda.synchronize()
+    assert ei.value.status == gdn.ERR_ALIAS
+    assert torch.equal(inp["state"], before)
