@@ -404,6 +404,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--oracle-seconds", type=float, default=10.0)
+    ap.add_argument("--only", default=None,
+                    help="time only this named extra workload (for profiling); prints its "
+                         "entry as the JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -455,14 +458,22 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     timer = Timer(torch, stream, flush)
 
+    specs = [(W.DECODE_B64, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
+             (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
+    if args.only:
+        w, kind = next((w, k) for w, k in specs if w.name == args.only)
+        r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
+        if dist.rank == 0:
+            print(json.dumps(r))
+        dist.close()
+        return
+
     clocks = ClockSampler(dist.local)
     clocks.start()
     head = run_decode24(torch, gdn, W, dev, timer, args, dist, peaks)
     extra = []
     launches = head["launches"]
     if not args.no_extra:
-        specs = [(W.DECODE_B64, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
-                 (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
         for w, kind in specs:
             r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
             launches += r["launches_per_step"] * args.steps
