@@ -293,7 +293,7 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     out = torch.empty((B, T, H, d), dtype=torch.float32, device=dev)
     st = inp["state"] if inp["state"] is not None else None
     st_out = st if (in_place and st is not None) else torch.empty((B, H, d, d), device=dev)
-    path = gdn.select_path(T, d)
+    path = gdn.select_path(T, d, w.dtype)
     ws = None
     nws = gdn.workspace_bytes(B, T, H, d, w.dtype, path)
     if nws:

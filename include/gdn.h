@@ -73,7 +73,8 @@ enum gdn_status {
     GDN_ERR_CUDA = -5,      /* a CUDA launch / enqueue / allocation call failed */
     GDN_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (gdn_get_device_status) */
     GDN_ERR_WORKSPACE = -7, /* caller workspace NULL, too small or misaligned */
-    GDN_ERR_NOMEM = -8      /* stream-ordered workspace allocation failed */
+    GDN_ERR_NOMEM = -8,     /* stream-ordered workspace allocation failed */
+    GDN_ERR_DTYPE = -9      /* dtype not supported on the requested path (chunked: bf16 only) */
 };
 
 /* dtype of q, k, v */
@@ -125,16 +126,19 @@ int gdn_forward_ex(const void *q, const void *k, const void *v,
 size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
                            int dtype, int path);
 
-/* Which path AUTO selects for these sizes (GDN_PATH_RECURRENT or
- * GDN_PATH_CHUNKED), or a negative GDN_ERR_* for unsupported sizes. */
-int gdn_select_path(int n_tokens, int head_dim);
+/* Which path AUTO selects (GDN_PATH_RECURRENT or GDN_PATH_CHUNKED) for
+ * these sizes and dtype, or a negative GDN_ERR_* for unsupported ones.
+ * AUTO takes the chunked path for bf16 q/k/v, head_dim 64/128/256 and at
+ * least 64 tokens; everything else runs the recurrent path. */
+int gdn_select_path(int n_tokens, int head_dim, int dtype);
 
 /*
  * gdn_supports -- capability query, the counterpart of the model card's
  * supports_gated_delta_net(head_dim) ("Ops" table and the note that the
  * head dim must be asked, not assumed).  Returns a bit mask: bit 0 (1) =
- * the recurrent path supports head_dim, bit 1 (2) = the chunked path does.
- * 0 means unsupported.  Supported: 32 (recurrent), 64, 128, 256 (both).
+ * the recurrent path supports head_dim, bit 1 (2) = the chunked path does
+ * (for bf16 q/k/v).  0 means unsupported.  Supported: 32 (recurrent only),
+ * 64, 128, 256 (both).
  */
 int gdn_supports(int head_dim);
 

@@ -24,8 +24,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 OK = 0
-ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NOMEM = \
-    -1, -2, -3, -4, -5, -6, -7, -8
+ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NOMEM, \
+    ERR_DTYPE = -1, -2, -3, -4, -5, -6, -7, -8, -9
 DTYPE_F32, DTYPE_BF16 = 0, 1
 PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
 
@@ -61,7 +61,7 @@ def lib():
             f.restype = i
         L.gdn_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.gdn_workspace_bytes.restype = sz
-        L.gdn_select_path.argtypes = [i, i]
+        L.gdn_select_path.argtypes = [i, i, i]
         L.gdn_select_path.restype = i
         L.gdn_supports.argtypes = [i]
         L.gdn_supports.restype = i
@@ -83,8 +83,9 @@ def supports(head_dim: int) -> int:
     return int(lib().gdn_supports(int(head_dim)))
 
 
-def select_path(n_tokens: int, head_dim: int) -> str:
-    r = int(lib().gdn_select_path(int(n_tokens), int(head_dim)))
+def select_path(n_tokens: int, head_dim: int, dtype: str = "bf16") -> str:
+    dt = DTYPE_BF16 if dtype in ("bf16", "bfloat16") else DTYPE_F32
+    r = int(lib().gdn_select_path(int(n_tokens), int(head_dim), dt))
     if r < 0:
         raise GdnError(r, "gdn_select_path")
     return {v: k for k, v in PATHS.items()}[r]

@@ -61,10 +61,12 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Tokens from which AUTO prefers the chunked path.
 constexpr int kChunkedMinTokens = 64;
 
-int select_path(int n_tokens, int head_dim) {
+int select_path(int n_tokens, int head_dim, int dtype) {
     const int caps = gdn_supports(head_dim);
     if (!caps) return GDN_ERR_HEADDIM;
-    if ((caps & 2) && n_tokens >= kChunkedMinTokens) return GDN_PATH_CHUNKED;
+    if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_ARG;
+    if ((caps & 2) && dtype == GDN_DTYPE_BF16 && n_tokens >= kChunkedMinTokens)
+        return GDN_PATH_CHUNKED;
     return GDN_PATH_RECURRENT;
 }
 
@@ -84,6 +86,7 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     if (!caps) return GDN_ERR_HEADDIM;
     if (path == GDN_PATH_RECURRENT && !(caps & 1)) return GDN_ERR_HEADDIM;
     if (path == GDN_PATH_CHUNKED && !(caps & 2)) return GDN_ERR_HEADDIM;
+    if (path == GDN_PATH_CHUNKED && dtype != GDN_DTYPE_BF16) return GDN_ERR_DTYPE;
 
     unsigned long long bth, bthd, bh, bhdd;
     if (!mul_ok((unsigned long long)B * (unsigned long long)T, (unsigned long long)H, &bth))
@@ -142,7 +145,7 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
 
-    if (path == GDN_PATH_AUTO) path = select_path(T, d);
+    if (path == GDN_PATH_AUTO) path = select_path(T, d, dtype);
     const size_t need =
         path == GDN_PATH_CHUNKED ? gdn::chunked_workspace_bytes(B, T, H, d, dtype) : 0;
     if (need > 0 && workspace && (workspace_bytes < need || !aligned(workspace, 256)))
@@ -204,15 +207,15 @@ size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, 
     if (n_seqs < 0 || n_tokens < 0 || n_heads < 0 || head_dim <= 0) return 0;
     if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return 0;
     if (n_tokens == 0 || (long long)n_seqs * n_heads == 0) return 0;
-    if (path == GDN_PATH_AUTO) path = select_path(n_tokens, head_dim);
-    if (path != GDN_PATH_CHUNKED) return 0;
+    if (path == GDN_PATH_AUTO) path = select_path(n_tokens, head_dim, dtype);
+    if (path != GDN_PATH_CHUNKED || dtype != GDN_DTYPE_BF16) return 0;
     if (!(gdn_supports(head_dim) & 2)) return 0;
     return gdn::chunked_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype);
 }
 
-int gdn_select_path(int n_tokens, int head_dim) {
+int gdn_select_path(int n_tokens, int head_dim, int dtype) {
     if (n_tokens < 0) return GDN_ERR_ARG;
-    return select_path(n_tokens, head_dim);
+    return select_path(n_tokens, head_dim, dtype);
 }
 
 int gdn_supports(int head_dim) {
@@ -245,6 +248,7 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_TIMEOUT: return "a bounded device wait gave up";
         case GDN_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
         case GDN_ERR_NOMEM: return "stream-ordered workspace allocation failed";
+        case GDN_ERR_DTYPE: return "dtype not supported on the requested path (chunked: bf16 only)";
         default: return "unknown status";
     }
 }

@@ -1,10 +1,634 @@
-// Chunked path placeholder: not built yet, so AUTO never selects it.
+// Chunked path of the gated delta rule on sm_103a tensor cores (tcgen05 +
+// TMEM + TMA), chunk size C = 64.
+//
+// Within a chunk of C tokens that starts from state S0 (d_v x d_k, stored
+// [value][key]), with G_r the running sum of g inside the chunk (inclusive),
+// gamma_r = exp(G_r) and u_r = beta_r (v_r - exp(g_r) S_{r-1} k_r) the
+// correction token r writes, the recurrence unrolls to
+//     S_r = gamma_r S0 + sum_{i<=r} exp(G_r - G_i) u_i k_i^T,
+// and the corrections solve a unit lower-triangular system
+//     (I + A) U = R,   A[r,i] = beta_r exp(G_r - G_i) (k_r . k_i)  (i < r)
+//                      R = diag(beta) V - diag(beta gamma) K S0^T.
+// With T = (I + A)^-1 (the UT transform of the chunk) and the causal decay
+// mask P[r,i] = exp(G_r - G_i) (q_r . k_i) (i <= r):
+//     U = T R,   O = (diag(gamma) Q S0^T + P U) / sqrt(d),
+//     S_C = gamma_{C-1} S0 + (diag(exp(G_{C-1} - G)) U)^T K.
+// "Gated Delta Net on AMD: why ROCm stumbles on hybrid-attention LLMs",
+// section "Why this bites AMD users specifically": the chunked form turns the
+// sequential recurrence into blocks that run in parallel; "marcsun13/
+// ggml-gated-delta-net" model card, section "Ops": one dispatch per run of
+// steps, state [value][key], 1/sqrt(head_dim) output scale, log-domain gate.
+//
+// GB300 mapping.  One CTA owns one (sequence, head) and a block of BV value
+// rows of the state (rows are independent), and walks the chunks in order:
+//   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile), the
+//      V block, and plain loads bring g, beta.
+//   2. MMA  [K;Q] K^T -> TMEM (M=128, N=64): K K^T and Q K^T in one tile.
+//   3. CUDA cores: A and P from it, T = (I + A)^-1 by 16x16 blocks, P T; the
+//      stacked Z = [T; P T] is written as bf16 hi + lo (two bf16 terms).
+//   4. MMA  [K;Q] S0^T -> TMEM: both K S0^T (for R) and Q S0^T (for O).
+//   5. R = beta V - beta gamma K S0^T, written as bf16 hi + lo.
+//   6. MMA  Z R -> TMEM: rows 0-63 are U = T R, rows 64-127 are P T R = P U.
+//   7. O = gamma Q S0^T + P U, scaled, to global; U scaled by
+//      exp(G_{C-1} - G_r) and written as bf16 hi + lo.
+//   8. MMA  K^T U~ -> TMEM: the transposed state increment, keys on lanes.
+//   9. S = gamma_{C-1} S + dS^T in fp32 registers; bf16 hi + lo for step 4.
+// Only raw bf16 inputs enter an MMA unsplit; every derived operand (S, Z,
+// R, U~) is carried as two bf16 terms so that products keep ~16 mantissa
+// bits, and all accumulation is fp32 in TMEM.  Waits on mbarriers are
+// bounded; a wait that gives up records GDN_ERR_TIMEOUT in the status word
+// and the CTA skips the remaining work and releases its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "../../include/gdn.h"
 #include "gdn_internal.h"
+#include "gdn_ptx.cuh"
 
 namespace gdn {
-bool chunked_supports(int) { return false; }
-size_t chunked_workspace_bytes(int, int, int, int, int) { return 0; }
-cudaError_t launch_chunked(const Problem &, void *, size_t, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int C = 64;            // chunk length (tokens)
+constexpr int NT = 256;          // threads per CTA (two warpgroups)
+constexpr int FST = 65;          // fp32 row stride of the 64x64 scratch matrices
+
+template <int D>
+struct Cfg {
+    static constexpr int BV = (D == 256) ? 32 : 64;       // value rows per CTA
+    static constexpr int KT = (D + 127) / 128;            // 128-key tiles of the state update
+    static constexpr int NSLAB = (D / 64 < 2) ? 2 : D / 64;  // 64-key slabs (d=64: + a zero slab)
+    // shared memory map (bytes from a 1024-aligned base)
+    static constexpr int OFF_QK = 0;                       // [K;Q]: NSLAB x (128 rows x 128 B)
+    static constexpr int OFF_V = OFF_QK + NSLAB * 16384;   // V block, 64 rows
+    static constexpr int OFF_Z = OFF_V + 8192;             // Z hi, Z lo: 128 rows x 128 B each
+    static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
+    static constexpr int OFF_UN = OFF_S + 2 * D * 128;     // union: {A, P, T, W} | {R/U~ hi, lo}
+    static constexpr int SZ_F = 64 * FST * 4;
+    static constexpr int OFF_A = OFF_UN;
+    static constexpr int OFF_P = OFF_A + SZ_F;
+    static constexpr int OFF_T = OFF_P + SZ_F;
+    static constexpr int OFF_W = OFF_T + SZ_F;             // 3 x 16x16 fp32
+    static constexpr int OFF_RU = OFF_UN;                  // R (then U~) hi, lo: 64 rows x 128 B
+    static constexpr int UN_BYTES = 3 * SZ_F + 3 * 256 * 4;
+    static constexpr int OFF_MISC = OFF_UN + UN_BYTES;     // G, beta, gamma, end-decay
+    static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;  // + alignment slack
+    // TMEM columns
+    static constexpr int COL_KQ = 0;
+    static constexpr int COL_X = 64;
+    static constexpr int COL_Y = 64 + BV;
+    static constexpr int COL_DS = 64 + 2 * BV;
+    static constexpr int TMEM_COLS = 256;
+    static_assert(COL_DS + KT * BV <= TMEM_COLS, "TMEM columns");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+struct Bars {
+    uint64_t tma;
+    uint64_t mma;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ float fast_exp(float x) { return expf(x); }
+
+// Store 16 consecutive fp32 values as bf16 hi / lo into two 128-B-swizzled
+// tiles at (row, col0 .. col0+15); col0 is a multiple of 8.
+__device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile, int row, int col0,
+                                              const float (&x)[16]) {
+#pragma unroll
+    for (int c = 0; c < 16; c += 8) {
+        uint32_t h[8], l[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ptx::split_bf16(x[c + e], h[e], l[e]);
+        const uint4 hv = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                                    h[6] | (h[7] << 16));
+        const uint4 lv = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16), l[4] | (l[5] << 16),
+                                    l[6] | (l[7] << 16));
+        const uint32_t off = ptx::sw128_offset(row, col0 + c);
+        *reinterpret_cast<uint4 *>(hi_tile + off) = hv;
+        *reinterpret_cast<uint4 *>(lo_tile + off) = lv;
+    }
 }
+
+template <int D>
+__global__ void __launch_bounds__(NT, 1)
+chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
+               const float *__restrict__ beta, const float *state_in, float *state_out,
+               float *__restrict__ out, int T, int H, float scale, int *status)
+{
+    using CF = Cfg<D>;
+    constexpr int BV = CF::BV;
+    constexpr int KT = CF::KT;
+    constexpr int HALF = BV / 2;          // value columns per warpgroup
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    __shared__ Bars bars;
+    float *sG = reinterpret_cast<float *>(sm + CF::OFF_MISC);
+    float *sBeta = sG + 64;
+    float *sGam = sG + 128;
+    float *sEnd = sG + 192;
+    float *sA = reinterpret_cast<float *>(sm + CF::OFF_A);
+    float *sP = reinterpret_cast<float *>(sm + CF::OFF_P);
+    float *sT = reinterpret_cast<float *>(sm + CF::OFF_T);
+    float *sW = reinterpret_cast<float *>(sm + CF::OFF_W);
+    uint8_t *sQK = sm + CF::OFF_QK;
+    uint8_t *sV = sm + CF::OFF_V;
+    uint8_t *sZhi = sm + CF::OFF_Z, *sZlo = sm + CF::OFF_Z + 16384;
+    uint8_t *sShi = sm + CF::OFF_S, *sSlo = sm + CF::OFF_S + D * 128;
+    uint8_t *sRhi = sm + CF::OFF_RU, *sRlo = sm + CF::OFF_RU + 8192;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int wg = tid >> 7;                 // warpgroup: which half of the value columns
+    const int row = tid & 127;               // TMEM lane this thread reads
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int bh = blockIdx.x;
+    const int b = bh / H, h = bh - b * H;
+    const int v0 = blockIdx.y * BV;
+    const int n_chunks = (T + C - 1) / C;
+
+    if (tid == 0) {
+        bars.abort = 0;
+        ptx::mbar_init(&bars.tma, 1);
+        ptx::mbar_init(&bars.mma, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&bars.tmem_base, CF::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    // zero: T scratch (its upper triangle is never written) and, for d=64,
+    // the second key slab that pads K^T to 128 rows in the state update
+    for (int i = tid; i < 64 * FST; i += NT) sT[i] = 0.f;
+    if (D == 64)
+        for (int i = tid; i < 16384 / 16; i += NT)
+            reinterpret_cast<uint4 *>(sQK + 16384)[i] = make_uint4(0, 0, 0, 0);
+
+    // ---- initial state block into registers: key = kt*128 + row, values
+    //      v0 + wg*HALF + j; coalesced over keys
+    float S[KT][HALF];
+    const size_t st_base = (size_t)bh * D * D;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+        const int key = kt * 128 + row;
+#pragma unroll
+        for (int j = 0; j < HALF; ++j) {
+            const int v = v0 + wg * HALF + j;
+            S[kt][j] = (state_in && key < D) ? state_in[st_base + (size_t)v * D + key] : 0.f;
+        }
+    }
+    // S hi / lo tiles: row = key, columns = value index within the block
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt) {
+        const int key = kt * 128 + row;
+        if (key < D) {
+#pragma unroll
+            for (int j = 0; j < HALF; j += 16) {
+                float x[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
+                store_split16(sShi, sSlo, key, wg * HALF + j, x);
+            }
+        }
+    }
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    volatile int *abort_flag = &bars.abort;
+
+    uint32_t mma_phase = 0;
+    auto fail = [&]() {
+        if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
+    };
+    // wait for the next MMA commit (all threads)
+    auto wait_mma = [&]() {
+        if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
+        mma_phase ^= 1;
+        ptx::tc_fence_after();
+    };
+
+    const uint32_t aQK = ptx::smem_u32(sQK);
+    const size_t tok_stride = (size_t)H * D;
+
+    for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
+        const int t0 = c * C;
+        const int n = min(C, T - t0);
+
+        // ---------------- 1. loads
+        if (tid == 0) {
+            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2;
+            ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
+#pragma unroll
+            for (int s = 0; s < D / 64; ++s) {
+                ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h, t0, b);
+                ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h, t0, b);
+            }
+            ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, t0, b);
+        }
+        if (tid < 64) {
+            const int r = tid;
+            float gr = 0.f, br = 0.f;
+            if (r < n) {
+                const size_t gi = ((size_t)b * T + t0 + r) * H + h;
+                gr = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
+                br = beta[gi];
+            }
+            // inclusive scan of g over the chunk (two warps)
+            float sacc = gr;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+                if (lane >= o) sacc += y;
+            }
+            sG[r] = sacc;       // warp 1 adds warp 0's total below
+            sBeta[r] = br;
+        }
+        __syncthreads();
+        if (tid >= 32 && tid < 64) sG[tid] += sG[31];
+        __syncthreads();
+        if (tid < 64) {
+            sGam[tid] = fast_exp(sG[tid]);
+            sEnd[tid] = fast_exp(sG[63] - sG[tid]);
+        }
+        if (!ptx::mbar_wait(&bars.tma, (uint32_t)(c & 1), abort_flag)) fail();
+        __syncthreads();
+        if (*abort_flag) break;
+
+        // ---------------- 2. MMA: [K;Q] K^T  (M=128, N=64, K=D)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t a = aQK + (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t da = ptx::smem_desc(a, 16, 1024);
+                ptx::mma_bf16(tmem + CF::COL_KQ, da, da, idesc, kk > 0);
+            }
+            ptx::mma_commit(&bars.mma);
+        }
+        wait_mma();
+
+        // ---------------- 3. A, P; T = (I + A)^-1; P T; Z hi / lo
+        {
+            // each thread: TMEM lane `row`, columns wg*32 .. +31
+            float kq[32];
+            ptx::tmem_ld16(tmem + lane_off + CF::COL_KQ + wg * 32, *reinterpret_cast<float(*)[16]>(kq));
+            ptx::tmem_ld16(tmem + lane_off + CF::COL_KQ + wg * 32 + 16,
+                           *reinterpret_cast<float(*)[16]>(kq + 16));
+            ptx::tmem_ld_wait();
+            const int r = row & 63;
+            const float Gr = sG[r];
+            if (row < 64) {
+                const float br = sBeta[r];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    sP[r * FST + i] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        // 3a. inverses of the four 16x16 diagonal blocks (unit lower triangular)
+        if (tid < 64) {
+            const int blk = tid >> 4, j = tid & 15;
+            const float *Ab = sA + (blk * 16) * FST + blk * 16;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
+                x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
+            }
+            float *Tb = sT + (blk * 16) * FST + blk * 16;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
+        }
+        __syncthreads();
+        // 3b. off-diagonal blocks, one block row at a time:
+        //     T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj
+        for (int bi = 1; bi < 4; ++bi) {
+            for (int o = tid; o < bi * 256; o += NT) {
+                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
+                float acc = 0.f;
+                for (int k = bj * 16; k < bi * 16; ++k)
+                    acc = fmaf(sA[(bi * 16 + r) * FST + k], sT[k * FST + bj * 16 + cc], acc);
+                sW[o] = acc;
+            }
+            __syncthreads();
+            for (int o = tid; o < bi * 256; o += NT) {
+                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
+                float acc = 0.f;
+                for (int m = 0; m <= r; ++m)
+                    acc = fmaf(sT[(bi * 16 + r) * FST + bi * 16 + m], sW[(bj << 8) + m * 16 + cc],
+                               acc);
+                sT[(bi * 16 + r) * FST + bj * 16 + cc] = -acc;
+            }
+            __syncthreads();
+        }
+        // 3c. Z rows: thread -> (row r = tid/4, columns 16*(tid%4) .. +15)
+        {
+            const int r = tid >> 2, c0 = (tid & 3) * 16;
+            float t[16], pt[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                t[e] = sT[r * FST + c0 + e];
+                pt[e] = 0.f;
+            }
+            // (P T)[r][j] = sum_{i=j}^{r} P[r][i] T[i][j]   (T[i][j] = 0 for i < j)
+            for (int i = c0; i <= r; ++i) {
+                const float p = sP[r * FST + i];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sT[i * FST + c0 + e], pt[e]);
+            }
+            store_split16(sZhi, sZlo, r, c0, t);
+            store_split16(sZhi, sZlo, 64 + r, c0, pt);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---------------- 4. MMA: [K;Q] S^T  (M=128, N=BV, K=D; S as hi + lo)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
+            const uint32_t bS[2] = {ptx::smem_u32(sShi), ptx::smem_u32(sSlo)};
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t da =
+                        ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t db = ptx::smem_desc(bS[part] + kk * 2048, 8192, 1024);
+                    ptx::mma_bf16(tmem + CF::COL_X, da, db, idesc, part > 0 || kk > 0);
+                }
+            }
+            ptx::mma_commit(&bars.mma);
+        }
+        wait_mma();
+
+        // ---------------- 5. R = beta V - beta gamma K S^T  (lanes 0-63)
+        float xq[HALF];   // Q S^T for this thread's output row (lanes 64-127)
+        {
+            float x[HALF];
+#pragma unroll
+            for (int j = 0; j < HALF; j += 16)
+                ptx::tmem_ld16(tmem + lane_off + CF::COL_X + wg * HALF + j,
+                               *reinterpret_cast<float(*)[16]>(x + j));
+            ptx::tmem_ld_wait();
+            if (row < 64) {
+                const int r = row;
+                const float br = sBeta[r], bg = br * sGam[r];
+#pragma unroll
+                for (int j = 0; j < HALF; j += 16) {
+                    float rr[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int vc = wg * HALF + j + e;
+                        float vv;
+                        if (BV == 64)
+                            vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                sV + ptx::sw128_offset(r, vc)));
+                        else
+                            vv = __bfloat162float(
+                                reinterpret_cast<const __nv_bfloat16 *>(sV)[r * BV + vc]);
+                        rr[e] = fmaf(br, vv, -bg * x[j + e]);
+                    }
+                    store_split16(sRhi, sRlo, r, wg * HALF + j, rr);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < HALF; ++j) xq[j] = x[j];
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---------------- 6. MMA: Z R  (M=128, N=BV, K=64; hi*hi + hi*lo + lo*hi)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
+            const uint32_t aZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZhi), ptx::smem_u32(sZlo)};
+            const uint32_t bR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo), ptx::smem_u32(sRhi)};
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t da = ptx::smem_desc(aZ[part] + kk * 32, 16, 1024);
+                    const uint64_t db = ptx::smem_desc(bR[part] + kk * 2048, 8192, 1024);
+                    ptx::mma_bf16(tmem + CF::COL_Y, da, db, idesc, part > 0 || kk > 0);
+                }
+            }
+            ptx::mma_commit(&bars.mma);
+        }
+        wait_mma();
+
+        // ---------------- 7. O (lanes 64-127) and U~ hi / lo (lanes 0-63)
+        {
+            float y[HALF];
+#pragma unroll
+            for (int j = 0; j < HALF; j += 16)
+                ptx::tmem_ld16(tmem + lane_off + CF::COL_Y + wg * HALF + j,
+                               *reinterpret_cast<float(*)[16]>(y + j));
+            ptx::tmem_ld_wait();
+            if (row >= 64) {
+                const int r = row - 64;
+                if (r < n) {
+                    const float gr = sGam[r];
+                    float *orow = out + ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D + v0 +
+                                  wg * HALF;
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 4) {
+                        float4 o4;
+                        o4.x = fmaf(gr, xq[j + 0], y[j + 0]) * scale;
+                        o4.y = fmaf(gr, xq[j + 1], y[j + 1]) * scale;
+                        o4.z = fmaf(gr, xq[j + 2], y[j + 2]) * scale;
+                        o4.w = fmaf(gr, xq[j + 3], y[j + 3]) * scale;
+                        *reinterpret_cast<float4 *>(orow + j) = o4;
+                    }
+                }
+            } else {
+                const int r = row;
+                const float er = sEnd[r];
+#pragma unroll
+                for (int j = 0; j < HALF; j += 16) {
+                    float u[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) u[e] = er * y[j + e];
+                    store_split16(sRhi, sRlo, r, wg * HALF + j, u);   // R no longer needed
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---------------- 8. MMA: K^T U~  (per 128-key tile: M=128, N=BV, K=64)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, true, true);
+            const uint32_t bU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t da =
+                            ptx::smem_desc(aQK + kt * 2 * 16384 + kk * 2048, 16384, 1024);
+                        const uint64_t db = ptx::smem_desc(bU[part] + kk * 2048, 8192, 1024);
+                        ptx::mma_bf16(tmem + CF::COL_DS + kt * BV, da, db, idesc,
+                                      part > 0 || kk > 0);
+                    }
+                }
+            }
+            ptx::mma_commit(&bars.mma);
+        }
+        wait_mma();
+
+        // ---------------- 9. S = gamma_C S + dS^T; S hi / lo for the next chunk
+        {
+            const float gC = sGam[63];
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+                float ds[HALF];
+#pragma unroll
+                for (int j = 0; j < HALF; j += 16)
+                    ptx::tmem_ld16(tmem + lane_off + CF::COL_DS + kt * BV + wg * HALF + j,
+                                   *reinterpret_cast<float(*)[16]>(ds + j));
+                ptx::tmem_ld_wait();
+                const int key = kt * 128 + row;
+#pragma unroll
+                for (int j = 0; j < HALF; ++j) S[kt][j] = fmaf(gC, S[kt][j], ds[j]);
+                if (key < D) {
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 16) {
+                        float x[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
+                        store_split16(sShi, sSlo, key, wg * HALF + j, x);
+                    }
+                }
+            }
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+
+    // ---- final state block
+    if (!*abort_flag) {
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+            const int key = kt * 128 + row;
+            if (key < D) {
+#pragma unroll
+                for (int j = 0; j < HALF; ++j) {
+                    const int v = v0 + wg * HALF + j;
+                    state_out[st_base + (size_t)v * D + key] = S[kt][j];
+                }
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, CF::TMEM_COLS);
+}
+
+// ------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 4-D map over a (B, T, H, d) bf16 tensor; box = {box0 elements of d, 1 head,
+// 64 tokens, 1 sequence}.  Tokens past T read as zeros.
+bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, int box0,
+              bool swizzle128) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2,
+                                   (cuuint64_t)T * H * d * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box0, 1, (cuuint32_t)C, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
+    using CF = Cfg<D>;
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, p.q, p.B, p.T, p.H, D, 64, true) ||
+        !make_map(&mk, p.k, p.B, p.T, p.H, D, 64, true) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, CF::BV == 64))
+        return cudaErrorInvalidValue;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(chunked_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    dim3 grid((unsigned)(p.B * p.H), D / CF::BV);
+    chunked_kernel<D><<<grid, NT, CF::SMEM, stream>>>(mq, mk, mv, p.g, p.beta, p.state_in,
+                                                      p.state_out, p.out, p.T, p.H, p.scale,
+                                                      p.status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunked_supports(int d) { return d == 64 || d == 128 || d == 256; }
+
+size_t chunked_workspace_bytes(int, int, int, int, int) { return 0; }
+
+cudaError_t launch_chunked(const Problem &p, void *, size_t, cudaStream_t stream) {
+    if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
+    switch (p.d) {
+        case 64: return launch_d<64>(p, stream);
+        case 128: return launch_d<128>(p, stream);
+        case 256: return launch_d<256>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace gdn

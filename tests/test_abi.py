@@ -48,15 +48,15 @@ def test_library_is_built_for_sm_103a():
 
 
 def test_supports(L):
-    assert gdn.supports(32) & 1
+    assert gdn.supports(32) == 1
     for d in (64, 128, 256):
-        assert gdn.supports(d) & 1
+        assert gdn.supports(d) == 3
     for d in (0, -1, 16, 48, 96, 100, 192, 512):
         assert gdn.supports(d) == 0
 
 
 def test_status_strings(L):
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = gdn.status_string(code)
         assert s and s != "unknown status"
     assert gdn.status_string(-99) == "unknown status"
@@ -69,8 +69,16 @@ def test_workspace_and_path_queries(L):
     assert L.gdn_workspace_bytes(1, 0, 32, 128, 1, 0) == 0          # no tokens -> 0
     assert gdn.select_path(1, 128) == "recurrent"
     assert gdn.select_path(5, 32) == "recurrent"
-    assert L.gdn_select_path(10, 48) == gdn.ERR_HEADDIM
-    assert L.gdn_select_path(-1, 128) == gdn.ERR_ARG
+    assert gdn.select_path(4096, 32) == "recurrent"
+    for d in (64, 128, 256):
+        assert gdn.select_path(63, d) == "recurrent"
+        assert gdn.select_path(64, d) == "chunked"
+        assert gdn.select_path(4096, d, "f32") == "recurrent"
+    assert L.gdn_select_path(10, 48, 1) == gdn.ERR_HEADDIM
+    assert L.gdn_select_path(-1, 128, 1) == gdn.ERR_ARG
+    assert L.gdn_select_path(10, 128, 5) == gdn.ERR_ARG
+    # the fused chunked kernel keeps everything on chip: no workspace
+    assert L.gdn_workspace_bytes(8, 16384, 32, 128, 1, 2) == 0
 
 
 # fake, well-aligned device addresses; every call below must fail validation
@@ -111,6 +119,11 @@ def test_host_validation_rejects(L, kw, code):
 
 def test_recurrent_path_rejects_unsupported_headdim(L):
     assert call(L, d=48, path=1) == gdn.ERR_HEADDIM
+
+
+def test_chunked_path_rejects_fp32_and_headdim_32(L):
+    assert call(L, dtype=0, path=2) == gdn.ERR_DTYPE
+    assert call(L, d=32, path=2) == gdn.ERR_HEADDIM
 
 
 def test_empty_batch_is_a_no_op(L):

@@ -59,12 +59,12 @@ def check(inp, dtype, path="auto", tol=None):
     return e_out, e_st
 
 
-def paths_for(d, T):
+def paths_for(d, T, dtype="bf16"):
     caps = gdn.supports(d)
     ps = []
     if caps & 1:
         ps.append("recurrent")
-    if caps & 2:
+    if caps & 2 and dtype == "bf16":
         ps.append("chunked")
     return ps
 
@@ -74,7 +74,7 @@ def paths_for(d, T):
 def test_tiny_workload_all_paths():
     w = W.TINY
     inp = W.make_inputs(w, "cuda")
-    for path in ["auto"] + paths_for(w.d, w.T):
+    for path in ["auto"] + paths_for(w.d, w.T, w.dtype):
         tol = TOL_RECURRENT if path == "recurrent" else TOL[w.dtype]
         check(inp, w.dtype, path, tol)
 
@@ -111,12 +111,14 @@ def sampled_pairs(w, n):
 
 @pytest.mark.parametrize("wname", [W.PREFILL_16K.name, W.PREFILL_16K_D64.name,
                                    W.PREFILL_16K_D256.name])
-@pytest.mark.parametrize("path", ["auto", "recurrent"])
+@pytest.mark.parametrize("path", ["auto", "recurrent", "chunked"])
 def test_long_prefill_full_size_sampled(wname, path):
     """Full-size launch (the configuration the benchmark times); the oracle
     recomputes every output and the final state of a sample of (sequence,
     head) pairs, which are independent problems."""
     w = W.BY_NAME[wname]
+    if path == "chunked" and not gdn.supports(w.d) & 2:
+        pytest.skip("chunked path not built")
     inp = W.make_inputs(w, "cuda")
     out, st = run_gpu(inp, path)
     tol = TOL_RECURRENT if path == "recurrent" else TOL[w.dtype]
@@ -145,7 +147,7 @@ def test_head_dims_dtypes_lengths(d, dtype, T):
     w = W.Workload("matrix", 2, T, 3, d, dtype, 0.0, 0.02, seed=77)
     inp = W.make_inputs(w, "cuda")
     ref_out, ref_st = run_oracle(inp)
-    for path in ["auto"] + paths_for(d, T):
+    for path in ["auto"] + paths_for(d, T, dtype):
         out, st = run_gpu(inp, path)
         e_out, e_st = errs(out, st, ref_out, ref_st)
         tol = TOL_RECURRENT if path == "recurrent" else TOL[dtype]
@@ -173,7 +175,7 @@ def test_extreme_gates_and_betas():
     g[:, 70] = -1e4
     beta[:, 20:30] = 0.0
     beta[:, 40:45] = 1.0
-    for path in paths_for(w.d, w.T):
+    for path in paths_for(w.d, w.T, "f32"):
         check(inp, "f32", path, TOL["f32"])
 
 
@@ -246,6 +248,15 @@ def test_no_writes_outside_outputs():
         for buf in (ob, sb):
             assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all(), path
         assert torch.isfinite(out).all() and torch.isfinite(st).all()
+
+
+def test_chunked_path_rejects_fp32_inputs():
+    w = W.Workload("f32chunk", 1, 64, 2, 64, "f32", 0.0, 0.02, seed=15)
+    inp = W.make_inputs(w, "cuda")
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                    path="chunked")
+    assert ei.value.status == gdn.ERR_DTYPE
 
 
 def test_rejects_bad_arguments_without_launching():
