@@ -407,6 +407,8 @@ def main():
     ap.add_argument("--only", default=None,
                     help="time only this named extra workload (for profiling); prints its "
                          "entry as the JSON line")
+    ap.add_argument("--only-seqs", type=int, default=None,
+                    help="with --only: override n_seqs (smaller profiling captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -462,6 +464,8 @@ def main():
              (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
     if args.only:
         w, kind = next((w, k) for w, k in specs if w.name == args.only)
+        if args.only_seqs:
+            w = w.replace(name=f"{w.name}_seqs{args.only_seqs}", B=args.only_seqs)
         r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
         if dist.rank == 0:
             print(json.dumps(r))
