@@ -554,6 +554,472 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0) ptx::tmem_dealloc(tmem, CF::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// head_dim 128: one CTA per (sequence, head) owns all 128 value rows, so the
+// chunk-local UT transform is built once per chunk and head.  The state is
+// held transposed with respect to chunked_kernel: TMEM lanes are value rows
+// and columns are keys, so it accumulates in place (S += U~^T K) and its
+// bf16 hi / lo split feeds the next chunk's MMA straight from TMEM (A
+// operand).  Per chunk (M = 128 value rows in every state product):
+//   X^T  = S [K;Q]^T            (A = S hi / lo in TMEM, B = [K;Q] from TMA)
+//   R^T  = beta V^T - beta gamma (K S^T)^T                  (CUDA cores)
+//   U^T  = R^T T^T,  (P U)^T = R^T (P T)^T       (B = rows of Z = [T; P T])
+//   O    = (gamma Q S^T + P U) / sqrt(d)                     (CUDA cores)
+//   S   += (diag(exp(G_C - G)) U)^T K   (S pre-scaled by gamma_C; B = K MN-major)
+// and chunk-local: [K;Q] K^T (M = 128) and P T (A = [P hi; P lo], B = T).
+namespace d128 {
+
+constexpr int D = 128;
+constexpr int NTH = 256;
+// shared memory map (bytes from a 1024-aligned base)
+constexpr int OFF_QK = 0;                      // 2 stages x [K;Q] (2 slabs x 128 rows x 128 B)
+constexpr int OFF_V = 65536;                   // 2 stages x V (2 boxes x 64 rows x 128 B)
+constexpr int OFF_Z = 98304;                   // Z hi | Z lo: 128 rows x 128 B each
+constexpr int OFF_UN = 131072;                 // union of the two areas below
+constexpr int OFF_PP = OFF_UN;                 //   P hi (rows 0-63) | P lo (rows 64-127)
+constexpr int OFF_A = OFF_UN + 16384;          //   A, T (fp32 64 x 65 each), W (3 x 256)
+constexpr int OFF_T = OFF_A + 64 * FST * 4;
+constexpr int OFF_W = OFF_T + 64 * FST * 4;
+constexpr int OFF_RT = OFF_UN;                 //   R^T (then U~^T) hi | lo: 128 rows x 128 B each
+constexpr int OFF_MISC = OFF_W + 3 * 256 * 4;  // 2 gate sets x {G, beta, gamma, end-decay}
+constexpr int SMEM = OFF_MISC + 2 * 4 * 64 * 4 + 1024;
+static_assert(OFF_MISC - OFF_UN >= 32768, "R^T hi/lo must fit the union");
+static_assert(SMEM <= 232448, "shared memory");
+// TMEM columns
+constexpr uint32_t C_SACC = 0;    // S (fp32): lane = value, column = key
+constexpr uint32_t C_SHI = 128;   // S hi, bf16 pairs (keys 2c, 2c+1 in column c)
+constexpr uint32_t C_SLO = 192;   // S lo
+constexpr uint32_t C_X = 256;     // X^T: columns 0-63 K part (then U^T), 64-127 Q part
+constexpr uint32_t C_PU = 384;    // (P U)^T
+constexpr uint32_t C_KQ = 448;    // [K;Q] K^T, then P T (lanes 0-63)
+
+struct Shared {
+    uint64_t tma[2];
+    uint64_t mma;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ float ex(float x) { return __expf(x); }
+
+// g, beta of chunk c into a gate set: G = inclusive cumsum of the clamped
+// gate, gamma = exp(G), end = exp(G_63 - G); tokens past T get g = 0, beta = 0.
+// All threads call it (it holds barriers).
+__device__ __forceinline__ void prep_gates(float *gs, const float *g, const float *beta, int b,
+                                           int h, int T, int H, int c, int tid) {
+    float *sG = gs, *sB = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
+    const int t0 = c * C;
+    const int n = min(C, T - t0);
+    if (tid < 64) {
+        float gr = 0.f, br = 0.f;
+        if (tid < n) {
+            const size_t gi = ((size_t)b * T + t0 + tid) * H + h;
+            gr = fmaxf(g[gi], -30.f);
+            br = beta[gi];
+        }
+        float acc = gr;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, acc, o);
+            if ((tid & 31) >= o) acc += y;
+        }
+        sG[tid] = acc;
+        sB[tid] = br;
+    }
+    __syncthreads();
+    if (tid >= 32 && tid < 64) sG[tid] += sG[31];
+    __syncthreads();
+    if (tid < 64) {
+        sGam[tid] = ex(sG[tid]);
+        sEnd[tid] = ex(sG[63] - sG[tid]);
+    }
+    __syncthreads();
+}
+
+// 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
+// columns, gamma * S -> 32 fp32 columns.
+__device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const float (&x)[32],
+                                            float gamma) {
+    uint32_t hi[16], lo[16], sc[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ptx::split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+    ptx::tmem_st16(tmem_lane + C_SHI + key0 / 2, hi);
+    ptx::tmem_st16(tmem_lane + C_SLO + key0 / 2, lo);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sc[e] = __float_as_uint(gamma * x[e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0, sc);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) sc[e] = __float_as_uint(gamma * x[16 + e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, sc);
+}
+
+__global__ void __launch_bounds__(NTH, 1)
+kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
+       const float *__restrict__ beta, const float *state_in, float *state_out,
+       float *__restrict__ out, int T, int H, float scale, int *status)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    __shared__ Shared sh;
+    float *sA = reinterpret_cast<float *>(sm + OFF_A);
+    float *sT = reinterpret_cast<float *>(sm + OFF_T);
+    float *sW = reinterpret_cast<float *>(sm + OFF_W);
+    float *gsets = reinterpret_cast<float *>(sm + OFF_MISC);
+    uint8_t *sZhi = sm + OFF_Z, *sZlo = sm + OFF_Z + 16384;
+    uint8_t *sPhi = sm + OFF_PP, *sPlo = sm + OFF_PP + 8192;
+    uint8_t *sRhi = sm + OFF_RT, *sRlo = sm + OFF_RT + 16384;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int wg = tid >> 7;                 // which half of the columns this thread handles
+    const int row = tid & 127;               // TMEM lane: value row, or [K;Q] row
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const int bh = blockIdx.x;
+    const int b = bh / H, h = bh - b * H;
+    const int n_chunks = (T + C - 1) / C;
+    const size_t tok_stride = (size_t)H * D;
+    const size_t st_base = (size_t)bh * D * D;
+
+    if (tid == 0) {
+        sh.abort = 0;
+        ptx::mbar_init(&sh.tma[0], 1);
+        ptx::mbar_init(&sh.tma[1], 1);
+        ptx::mbar_init(&sh.mma, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+        ptx::prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&sh.tmem_base, 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const uint32_t tl = tmem + lane_off;     // this warp's lane quarter
+    volatile int *abort_flag = &sh.abort;
+    uint32_t mma_phase = 0;
+
+    auto fail = [&]() {
+        if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
+    };
+    auto wait_mma = [&]() {
+        if (!ptx::mbar_wait(&sh.mma, mma_phase, abort_flag)) fail();
+        mma_phase ^= 1;
+        ptx::tc_fence_after();
+    };
+    auto issue_loads = [&](int c) {
+        const int st = c & 1;
+        uint8_t *qk = sm + OFF_QK + st * 32768;
+        uint8_t *vv = sm + OFF_V + st * 16384;
+        ptx::mbar_arrive_expect_tx(&sh.tma[st], 6 * 8192);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.tma[st], s * 64, h, c * C, b);
+            ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.tma[st], s * 64, h, c * C, b);
+            ptx::tma_load_4d(vv + s * 8192, &tm_v, &sh.tma[st], s * 64, h, c * C, b);
+        }
+    };
+    if (tid == 0) {
+        issue_loads(0);
+        if (n_chunks > 1) issue_loads(1);
+    }
+    prep_gates(gsets, g, beta, b, h, T, H, 0, tid);
+
+    // ---- initial state: thread (value row, key half) -> TMEM
+    {
+        const float gC = gsets[128 + 63];
+#pragma unroll
+        for (int kg = 0; kg < 64; kg += 32) {
+            const int key0 = wg * 64 + kg;
+            float x[32];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (state_in)
+                    t4 = *reinterpret_cast<const float4 *>(state_in + st_base + (size_t)row * D +
+                                                           key0 + e);
+                x[e] = t4.x; x[e + 1] = t4.y; x[e + 2] = t4.z; x[e + 3] = t4.w;
+            }
+            put_state32(tl, key0, x, gC);
+        }
+        ptx::tmem_st_wait();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+
+    for (int c = 0; c < n_chunks; ++c) {
+        if (*abort_flag) break;      // read right after a barrier: uniform
+        const int st = c & 1;
+        const int t0 = c * C;
+        const int n = min(C, T - t0);
+        const float *gs = gsets + st * 256;
+        const float *sG = gs, *sBeta = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
+        uint8_t *sQK = sm + OFF_QK + st * 32768;
+        uint8_t *sV = sm + OFF_V + st * 16384;
+        const uint32_t aQK = ptx::smem_u32(sQK);
+        const bool last = (c + 1 == n_chunks);
+
+        // gates of the next chunk (needed by this chunk's state epilogue)
+        if (!last) prep_gates(gsets + (st ^ 1) * 256, g, beta, b, h, T, H, c + 1, tid);
+        if (!ptx::mbar_wait(&sh.tma[st], (uint32_t)((c >> 1) & 1), abort_flag)) fail();
+        __syncthreads();
+        if (*abort_flag) break;
+
+        // ---- [K;Q] K^T  (M = 128, N = 64, K = 128)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t da = ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                ptx::mma_bf16(tmem + C_KQ, da, da, idesc, kk > 0);
+            }
+            ptx::mma_commit(&sh.mma);
+        }
+        wait_mma();
+
+        // ---- A (rows 0-63) to shared fp32; P (rows 64-127) as hi / lo rows
+        {
+            float kq[32];
+            ptx::tmem_ld32(tl + C_KQ + wg * 32, kq);
+            ptx::tmem_ld_wait();
+            const int r = row & 63;
+            const float Gr = sG[r];
+            if (row < 64) {
+                const float br = sBeta[r];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    sA[r * FST + i] = (i < r) ? br * ex(Gr - sG[i]) * kq[j] : 0.f;
+                }
+            } else {
+                float p[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    p[j] = (i <= r) ? ex(Gr - sG[i]) * kq[j] : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) ptx::store_split8(sPhi, sPlo, r, wg * 32 + j, p + j);
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block rows
+        if (tid < 64) {
+            const int blk = tid >> 4, j = tid & 15;
+            const float *Ab = sA + (blk * 16) * FST + blk * 16;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
+                x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
+            }
+            float *Tb = sT + (blk * 16) * FST + blk * 16;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
+        }
+        __syncthreads();
+        for (int bi = 1; bi < 4; ++bi) {
+            for (int o = tid; o < bi * 256; o += NTH) {
+                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
+                const float *arow = sA + (bi * 16 + r) * FST;
+                float acc = 0.f;
+                for (int k = bj * 16; k < bi * 16; ++k)
+                    acc = fmaf(arow[k], sT[k * FST + bj * 16 + cc], acc);
+                sW[o] = acc;
+            }
+            __syncthreads();
+            for (int o = tid; o < bi * 256; o += NTH) {
+                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
+                const float *trow = sT + (bi * 16 + r) * FST + bi * 16;
+                float acc = 0.f;
+                for (int m = 0; m <= r; ++m) acc = fmaf(trow[m], sW[(bj << 8) + m * 16 + cc], acc);
+                sT[(bi * 16 + r) * FST + bj * 16 + cc] = -acc;
+            }
+            __syncthreads();
+        }
+        // ---- T as hi / lo into Z rows 0-63 (upper blocks are zero)
+        {
+            const int r = tid >> 2, c0 = (tid & 3) * 16;
+            float t[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                const int j = c0 + e;
+                t[e] = ((j >> 4) > (r >> 4)) ? 0.f : sT[r * FST + j];
+            }
+            ptx::store_split8(sZhi, sZlo, r, c0, t);
+            ptx::store_split8(sZhi, sZlo, r, c0 + 8, t + 8);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---- P T (M = 128 rows of [P hi; P lo], N = 64, K = 64) and
+        //      X^T = S [K;Q]^T (A = S hi / lo from TMEM, M = 128, N = 128, K = 128)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            {
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, true);
+                const uint32_t aP[3] = {ptx::smem_u32(sPhi), ptx::smem_u32(sPhi), ptx::smem_u32(sPlo)};
+                const uint32_t bT[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(tmem + C_KQ, ptx::smem_desc(aP[part] + kk * 32, 16, 1024),
+                                      ptx::smem_desc(bT[part] + kk * 2048, 8192, 1024), idesc,
+                                      part > 0 || kk > 0);
+            }
+            {
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        ptx::mma_bf16_ts(tmem + C_X, tmem + (part ? C_SLO : C_SHI) + kk * 8,
+                                         ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32,
+                                                        16, 1024),
+                                         idesc, part > 0 || kk > 0);
+            }
+            ptx::mma_commit(&sh.mma);
+        }
+        wait_mma();
+
+        // ---- P T rows -> Z rows 64-127 (lanes 0-63); R^T (all threads)
+        if ((warp & 3) < 2) {
+            float pt[32];
+            ptx::tmem_ld32(tl + C_KQ + wg * 32, pt);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) ptx::store_split8(sZhi, sZlo, 64 + row, wg * 32 + j, pt + j);
+        }
+        {
+            const int v = row;
+            float x[32];
+            ptx::tmem_ld32(tl + C_X + wg * 32, x);
+            ptx::tmem_ld_wait();
+            const uint8_t *vbox = sV + (v >> 6) * 8192;
+            float rr[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = wg * 32 + j;
+                const float vv = __bfloat162float(
+                    *reinterpret_cast<const __nv_bfloat16 *>(vbox + ptx::sw128_offset(t, v & 63)));
+                const float bt = sBeta[t];
+                rr[j] = bt * (vv - sGam[t] * x[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) ptx::store_split8(sRhi, sRlo, v, wg * 32 + j, rr + j);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---- U^T = R^T T^T (into the K part of X), (P U)^T = R^T (P T)^T
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+            const uint32_t aR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+            const uint32_t bZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
+#pragma unroll
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(tmem + (half ? C_PU : C_X),
+                                      ptx::smem_desc(aR[part] + kk * 32, 16, 1024),
+                                      ptx::smem_desc(bZ[part] + half * 8192 + kk * 32, 16, 1024),
+                                      idesc, part > 0 || kk > 0);
+            ptx::mma_commit(&sh.mma);
+        }
+        wait_mma();
+
+        // ---- O (global) and U~^T hi / lo
+        {
+            const int v = row;
+            float xq[32], pu[32];
+            ptx::tmem_ld32(tl + C_X + 64 + wg * 32, xq);
+            ptx::tmem_ld32(tl + C_PU + wg * 32, pu);
+            ptx::tmem_ld_wait();
+            float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int t = wg * 32 + j;
+                if (t < n) ocol[(size_t)t * tok_stride] = fmaf(sGam[t], xq[j], pu[j]) * scale;
+            }
+            float u[32];
+            ptx::tmem_ld32(tl + C_X + wg * 32, u);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] *= sEnd[wg * 32 + j];
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) ptx::store_split8(sRhi, sRlo, v, wg * 32 + j, u + j);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncthreads();
+
+        // ---- S += U~^T K  (M = 128 values, N = 128 keys, K = 64 tokens)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+            const uint32_t aU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+#pragma unroll
+            for (int part = 0; part < 2; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::mma_bf16(tmem + C_SACC, ptx::smem_desc(aU[part] + kk * 32, 16, 1024),
+                                  ptx::smem_desc(aQK + kk * 2048, 16384, 1024), idesc, true);
+            ptx::mma_commit(&sh.mma);
+        }
+        wait_mma();
+        // this chunk's stage is free: bring chunk c + 2 into it
+        if (tid == 0 && c + 2 < n_chunks) issue_loads(c + 2);
+
+        // ---- S: split for the next chunk's X^T and pre-scale by its gamma_C,
+        //      or write the final state
+        {
+            const float gC = last ? 1.f : gsets[(st ^ 1) * 256 + 128 + 63];
+#pragma unroll
+            for (int kg = 0; kg < 64; kg += 32) {
+                const int key0 = wg * 64 + kg;
+                float x[32];
+                ptx::tmem_ld32(tl + C_SACC + key0, x);
+                ptx::tmem_ld_wait();
+                if (last) {
+                    float *dst = state_out + st_base + (size_t)row * D + key0;
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        *reinterpret_cast<float4 *>(dst + e) =
+                            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                } else {
+                    put_state32(tl, key0, x, gC);
+                }
+            }
+            if (!last) ptx::tmem_st_wait();
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+}
+
+}  // namespace d128
+
 // ------------------------------------------------------------------- host
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -615,6 +1081,24 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_d128(const Problem &p, cudaStream_t stream) {
+    CUtensorMap mq, mk, mv;
+    if (!make_map(&mq, p.q, p.B, p.T, p.H, 128, 64, true) ||
+        !make_map(&mk, p.k, p.B, p.T, p.H, 128, 64, true) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, 128, 64, true))
+        return cudaErrorInvalidValue;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(d128::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        d128::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    d128::kernel<<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
+        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 bool chunked_supports(int d) { return d == 64 || d == 128 || d == 256; }
@@ -625,7 +1109,7 @@ cudaError_t launch_chunked(const Problem &p, void *, size_t, cudaStream_t stream
     if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
     switch (p.d) {
         case 64: return launch_d<64>(p, stream);
-        case 128: return launch_d<128>(p, stream);
+        case 128: return launch_d128(p, stream);
         case 256: return launch_d<256>(p, stream);
         default: return cudaErrorInvalidValue;
     }
