@@ -113,6 +113,73 @@ __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile
     }
 }
 
+// One block row BI (1..3) of T = (I + A)^-1, 16x16 blocks, 256 threads:
+//   W = A[BI, :BI] T[:BI, :BI],  T[BI, j] = -T[BI, BI] W[:, j]   (j < BI)
+// The upper blocks of T must already be zero.  Thread (r, c) = (tid / 16,
+// tid % 16) owns row r, column c of every block of the row.
+template <int BI>
+__device__ __forceinline__ void ut_block_row(const float *sA, float *sT, float *sW, int tid) {
+    const int r = tid >> 4, c = tid & 15;
+    float acc[BI];
+#pragma unroll
+    for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
+    const float *arow = sA + (BI * 16 + r) * FST;
+#pragma unroll
+    for (int k = 0; k < BI * 16; ++k) {
+        const float a = arow[k];
+#pragma unroll
+        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(a, sT[k * FST + jb * 16 + c], acc[jb]);
+    }
+#pragma unroll
+    for (int jb = 0; jb < BI; ++jb) sW[r * 48 + jb * 16 + c] = acc[jb];
+    __syncthreads();
+#pragma unroll
+    for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
+    const float *trow = sT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        const float t = trow[m];
+#pragma unroll
+        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(t, sW[m * 48 + jb * 16 + c], acc[jb]);
+    }
+#pragma unroll
+    for (int jb = 0; jb < BI; ++jb) sT[(BI * 16 + r) * FST + jb * 16 + c] = -acc[jb];
+    __syncthreads();
+}
+
+// T = (I + A)^-1 for a strictly lower triangular 64x64 A (fp32, row stride
+// FST) on 256 threads: the four diagonal 16x16 blocks by column substitution,
+// then the three block rows below them.  T is written in full (zeros above
+// the diagonal).  Starts and ends with the caller's data visible to all.
+__device__ __forceinline__ void ut_transform(const float *sA, float *sT, float *sW, int tid) {
+    // zero the six blocks above the block diagonal
+    for (int e = tid; e < 6 * 256; e += 256) {
+        const int blk = e >> 8, w = e & 255;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        sT[(bi * 16 + (w >> 4)) * FST + bj * 16 + (w & 15)] = 0.f;
+    }
+    if (tid < 64) {
+        const int blk = tid >> 4, j = tid & 15;
+        const float *Ab = sA + (blk * 16) * FST + blk * 16;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
+            x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
+        }
+        float *Tb = sT + (blk * 16) * FST + blk * 16;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
+    }
+    __syncthreads();
+    ut_block_row<1>(sA, sT, sW, tid);
+    ut_block_row<2>(sA, sT, sW, tid);
+    ut_block_row<3>(sA, sT, sW, tid);
+}
+
 template <int D>
 __global__ void __launch_bounds__(NT, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -306,44 +373,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         ptx::tc_fence_before();
         __syncthreads();
-        // 3a. inverses of the four 16x16 diagonal blocks (unit lower triangular)
-        if (tid < 64) {
-            const int blk = tid >> 4, j = tid & 15;
-            const float *Ab = sA + (blk * 16) * FST + blk * 16;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
-                x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
-            }
-            float *Tb = sT + (blk * 16) * FST + blk * 16;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
-        }
-        __syncthreads();
-        // 3b. off-diagonal blocks, one block row at a time:
-        //     T_ij = -T_ii * sum_{k=j}^{i-1} A_ik T_kj
-        for (int bi = 1; bi < 4; ++bi) {
-            for (int o = tid; o < bi * 256; o += NT) {
-                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
-                float acc = 0.f;
-                for (int k = bj * 16; k < bi * 16; ++k)
-                    acc = fmaf(sA[(bi * 16 + r) * FST + k], sT[k * FST + bj * 16 + cc], acc);
-                sW[o] = acc;
-            }
-            __syncthreads();
-            for (int o = tid; o < bi * 256; o += NT) {
-                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m)
-                    acc = fmaf(sT[(bi * 16 + r) * FST + bi * 16 + m], sW[(bj << 8) + m * 16 + cc],
-                               acc);
-                sT[(bi * 16 + r) * FST + bj * 16 + cc] = -acc;
-            }
-            __syncthreads();
-        }
+        // 3a/3b. T = (I + A)^-1 by 16x16 blocks
+        ut_transform(sA, sT, sW, tid);
         // 3c. Z rows: thread -> (row r = tid/4, columns 16*(tid%4) .. +15)
         {
             const int r = tid >> 2, c0 = (tid & 3) * 16;
@@ -602,38 +633,42 @@ struct Shared {
 
 __device__ __forceinline__ float ex(float x) { return __expf(x); }
 
-// g, beta of chunk c into a gate set: G = inclusive cumsum of the clamped
-// gate, gamma = exp(G), end = exp(G_63 - G); tokens past T get g = 0, beta = 0.
-// All threads call it (it holds barriers).
-__device__ __forceinline__ void prep_gates(float *gs, const float *g, const float *beta, int b,
+// Gates of one chunk, held by threads 0-63 between the global loads and
+// the scan: lane l of warp w keeps g of tokens l and 32 + l (clamped at
+// -30, 0 past T) and beta of its own token w*32 + l.
+struct GateRegs {
+    float ga, gb, bown;
+};
+
+__device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const float *beta, int b,
                                            int h, int T, int H, int c, int tid) {
-    float *sG = gs, *sB = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
     const int t0 = c * C;
     const int n = min(C, T - t0);
-    if (tid < 64) {
-        float gr = 0.f, br = 0.f;
-        if (tid < n) {
-            const size_t gi = ((size_t)b * T + t0 + tid) * H + h;
-            gr = fmaxf(g[gi], -30.f);
-            br = beta[gi];
-        }
-        float acc = gr;
+    const int l = tid & 31, own = tid;
+    const size_t base = ((size_t)b * T + t0) * H + h;
+    r.ga = (l < n) ? fmaxf(g[base + (size_t)l * H], -30.f) : 0.f;
+    r.gb = (32 + l < n) ? fmaxf(g[base + (size_t)(32 + l) * H], -30.f) : 0.f;
+    r.bown = (own < n) ? beta[base + (size_t)own * H] : 0.f;
+}
+
+// G = inclusive cumsum, gamma = exp(G), end = exp(G_63 - G) into a gate set
+// {G, beta, gamma, end} (4 x 64 floats).  Threads 0-63, no barrier inside.
+__device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int tid) {
+    const int l = tid & 31;
+    float sa = r.ga, sb = r.gb;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, acc, o);
-            if ((tid & 31) >= o) acc += y;
-        }
-        sG[tid] = acc;
-        sB[tid] = br;
+    for (int o = 1; o < 32; o <<= 1) {
+        const float ya = __shfl_up_sync(0xffffffffu, sa, o);
+        const float yb = __shfl_up_sync(0xffffffffu, sb, o);
+        if (l >= o) { sa += ya; sb += yb; }
     }
-    __syncthreads();
-    if (tid >= 32 && tid < 64) sG[tid] += sG[31];
-    __syncthreads();
-    if (tid < 64) {
-        sGam[tid] = ex(sG[tid]);
-        sEnd[tid] = ex(sG[63] - sG[tid]);
-    }
-    __syncthreads();
+    const float tot0 = __shfl_sync(0xffffffffu, sa, 31);
+    const float tot = tot0 + __shfl_sync(0xffffffffu, sb, 31);
+    const float G = (tid < 32) ? sa : tot0 + sb;
+    gs[tid] = G;
+    gs[64 + tid] = r.bown;
+    gs[128 + tid] = ex(G);
+    gs[192 + tid] = ex(tot - G);
 }
 
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
@@ -728,7 +763,13 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         issue_loads(0);
         if (n_chunks > 1) issue_loads(1);
     }
-    prep_gates(gsets, g, beta, b, h, T, H, 0, tid);
+    GateRegs gr{0.f, 0.f, 0.f};     // gates of the next chunk (threads 0-63)
+    if (tid < 64) {
+        load_gates(gr, g, beta, b, h, T, H, 0, tid);
+        scan_gates(gr, gsets, tid);
+        if (n_chunks > 1) load_gates(gr, g, beta, b, h, T, H, 1, tid);
+    }
+    __syncthreads();
 
     // ---- initial state: thread (value row, key half) -> TMEM
     {
@@ -765,8 +806,6 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         const uint32_t aQK = ptx::smem_u32(sQK);
         const bool last = (c + 1 == n_chunks);
 
-        // gates of the next chunk (needed by this chunk's state epilogue)
-        if (!last) prep_gates(gsets + (st ^ 1) * 256, g, beta, b, h, T, H, c + 1, tid);
         if (!ptx::mbar_wait(&sh.tma[st], (uint32_t)((c >> 1) & 1), abort_flag)) fail();
         __syncthreads();
         if (*abort_flag) break;
@@ -812,50 +851,15 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         ptx::tc_fence_before();
         __syncthreads();
 
-        // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block rows
-        if (tid < 64) {
-            const int blk = tid >> 4, j = tid & 15;
-            const float *Ab = sA + (blk * 16) * FST + blk * 16;
-            float x[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
-                x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
-            }
-            float *Tb = sT + (blk * 16) * FST + blk * 16;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
-        }
-        __syncthreads();
-        for (int bi = 1; bi < 4; ++bi) {
-            for (int o = tid; o < bi * 256; o += NTH) {
-                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
-                const float *arow = sA + (bi * 16 + r) * FST;
-                float acc = 0.f;
-                for (int k = bj * 16; k < bi * 16; ++k)
-                    acc = fmaf(arow[k], sT[k * FST + bj * 16 + cc], acc);
-                sW[o] = acc;
-            }
-            __syncthreads();
-            for (int o = tid; o < bi * 256; o += NTH) {
-                const int bj = o >> 8, e = o & 255, r = e >> 4, cc = e & 15;
-                const float *trow = sT + (bi * 16 + r) * FST + bi * 16;
-                float acc = 0.f;
-                for (int m = 0; m <= r; ++m) acc = fmaf(trow[m], sW[(bj << 8) + m * 16 + cc], acc);
-                sT[(bi * 16 + r) * FST + bj * 16 + cc] = -acc;
-            }
-            __syncthreads();
-        }
+        // ---- T = (I + A)^-1 by 16x16 blocks
+        ut_transform(sA, sT, sW, tid);
         // ---- T as hi / lo into Z rows 0-63 (upper blocks are zero)
         {
             const int r = tid >> 2, c0 = (tid & 3) * 16;
             float t[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                const int j = c0 + e;
-                t[e] = ((j >> 4) > (r >> 4)) ? 0.f : sT[r * FST + j];
+                t[e] = sT[r * FST + c0 + e];
             }
             ptx::store_split8(sZhi, sZlo, r, c0, t);
             ptx::store_split8(sZhi, sZlo, r, c0 + 8, t + 8);
@@ -964,6 +968,12 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
             for (int j = 0; j < 32; ++j) u[j] *= sEnd[wg * 32 + j];
 #pragma unroll
             for (int j = 0; j < 32; j += 8) ptx::store_split8(sRhi, sRlo, v, wg * 32 + j, u + j);
+        }
+        // gates of the next chunk (its gamma_C pre-scales the state below);
+        // then start loading the chunk after it
+        if (tid < 64 && !last) {
+            scan_gates(gr, gsets + (st ^ 1) * 256, tid);
+            if (c + 2 < n_chunks) load_gates(gr, g, beta, b, h, T, H, c + 2, tid);
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
