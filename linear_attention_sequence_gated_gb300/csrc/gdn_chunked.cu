@@ -634,8 +634,8 @@ struct Shared {
 __device__ __forceinline__ float ex(float x) { return __expf(x); }
 
 // Gates of one chunk, held by threads 0-63 between the global loads and
-// the scan: lane l of warp w keeps g of tokens l and 32 + l (clamped at
-// -30, 0 past T) and beta of its own token w*32 + l.
+// the scan: lane l of warp w keeps g of tokens l and 32 + l (0 past T) and
+// beta of its own token w*32 + l.
 struct GateRegs {
     float ga, gb, bown;
 };
@@ -646,8 +646,10 @@ __device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const fl
     const int n = min(C, T - t0);
     const int l = tid & 31, own = tid;
     const size_t base = ((size_t)b * T + t0) * H + h;
-    r.ga = (l < n) ? fmaxf(g[base + (size_t)l * H], -30.f) : 0.f;
-    r.gb = (32 + l < n) ? fmaxf(g[base + (size_t)(32 + l) * H], -30.f) : 0.f;
+    // raw values only: the clamp happens in scan_gates, so these loads stay
+    // in flight until the scan, a chunk later
+    r.ga = (l < n) ? g[base + (size_t)l * H] : 0.f;
+    r.gb = (32 + l < n) ? g[base + (size_t)(32 + l) * H] : 0.f;
     r.bown = (own < n) ? beta[base + (size_t)own * H] : 0.f;
 }
 
@@ -655,7 +657,7 @@ __device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const fl
 // {G, beta, gamma, end} (4 x 64 floats).  Threads 0-63, no barrier inside.
 __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int tid) {
     const int l = tid & 31;
-    float sa = r.ga, sb = r.gb;
+    float sa = fmaxf(r.ga, -30.f), sb = fmaxf(r.gb, -30.f);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const float ya = __shfl_up_sync(0xffffffffu, sa, o);

@@ -82,6 +82,12 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     static_assert(D % RB == 0, "rows per block must divide head_dim");
     static_assert(NV >= 1 && D == NV * 4 * L, "bad lane split");
 
+    // Launched with programmatic stream serialization: this grid may be
+    // scheduled while the previous kernel on the stream is still running.
+    // Nothing is read before the previous grid has completed and flushed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
     const int bh = blockIdx.x;  // b * H + h
     const int b = bh / H;
     const int h = bh - b * H;
@@ -197,12 +203,21 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 template <int D, int L, int R, typename Tin>
 cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     constexpr int RB = 4 * R * (32 / L);
-    dim3 grid((unsigned)p.B * (unsigned)p.H, D / RB);
-    recurrent_kernel<D, L, R, Tin><<<grid, 128, 0, stream>>>(
-        static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
-        static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H,
-        p.scale);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.B * (unsigned)p.H, D / RB);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // back-to-back calls (e.g. the layers of one decode step) overlap launch
+    // latency with the tail of the previous kernel
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin>, static_cast<const Tin *>(p.q),
+                              static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v), p.g,
+                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale);
 }
 
 template <int D, int L, typename Tin>
