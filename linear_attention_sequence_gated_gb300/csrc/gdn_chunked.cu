@@ -124,7 +124,7 @@ __device__ __forceinline__ void ut_block_row(const float *sA, float *sT, float *
 #pragma unroll
     for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
     const float *arow = sA + (BI * 16 + r) * FST;
-#pragma unroll
+#pragma unroll 8
     for (int k = 0; k < BI * 16; ++k) {
         const float a = arow[k];
 #pragma unroll
@@ -691,7 +691,7 @@ __device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const 
 }
 
 __global__ void __launch_bounds__(NTH, 1)
-kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
        const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
        const float *__restrict__ beta, const float *state_in, float *state_out,
        float *__restrict__ out, int T, int H, float scale, int *status)
@@ -776,7 +776,7 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
     // ---- initial state: thread (value row, key half) -> TMEM
     {
         const float gC = gsets[128 + 63];
-#pragma unroll
+#pragma unroll 1
         for (int kg = 0; kg < 64; kg += 32) {
             const int key0 = wg * 64 + kg;
             float x[32];
@@ -826,28 +826,32 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         wait_mma();
 
         // ---- A (rows 0-63) to shared fp32; P (rows 64-127) as hi / lo rows
+        //      (16 columns per step: small code, the loop stays in the I-cache)
         {
-            float kq[32];
-            ptx::tmem_ld32(tl + C_KQ + wg * 32, kq);
-            ptx::tmem_ld_wait();
             const int r = row & 63;
             const float Gr = sG[r];
-            if (row < 64) {
-                const float br = sBeta[r];
+            const float br = sBeta[r];
+#pragma unroll 1
+            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                float kq[16];
+                ptx::tmem_ld16(tl + C_KQ + jc, kq);
+                ptx::tmem_ld_wait();
+                if (row < 64) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = wg * 32 + j;
-                    sA[r * FST + i] = (i < r) ? br * ex(Gr - sG[i]) * kq[j] : 0.f;
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = jc + j;
+                        sA[r * FST + i] = (i < r) ? br * ex(Gr - sG[i]) * kq[j] : 0.f;
+                    }
+                } else {
+                    float p[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int i = jc + j;
+                        p[j] = (i <= r) ? ex(Gr - sG[i]) * kq[j] : 0.f;
+                    }
+                    ptx::store_split8(sPhi, sPlo, r, jc, p);
+                    ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
                 }
-            } else {
-                float p[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = wg * 32 + j;
-                    p[j] = (i <= r) ? ex(Gr - sG[i]) * kq[j] : 0.f;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) ptx::store_split8(sPhi, sPlo, r, wg * 32 + j, p + j);
             }
         }
         ptx::tc_fence_before();
@@ -902,29 +906,34 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
 
         // ---- P T rows -> Z rows 64-127 (lanes 0-63); R^T (all threads)
         if ((warp & 3) < 2) {
-            float pt[32];
-            ptx::tmem_ld32(tl + C_KQ + wg * 32, pt);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) ptx::store_split8(sZhi, sZlo, 64 + row, wg * 32 + j, pt + j);
+#pragma unroll 1
+            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                float pt[16];
+                ptx::tmem_ld16(tl + C_KQ + jc, pt);
+                ptx::tmem_ld_wait();
+                ptx::store_split8(sZhi, sZlo, 64 + row, jc, pt);
+                ptx::store_split8(sZhi, sZlo, 64 + row, jc + 8, pt + 8);
+            }
         }
         {
             const int v = row;
-            float x[32];
-            ptx::tmem_ld32(tl + C_X + wg * 32, x);
-            ptx::tmem_ld_wait();
             const uint8_t *vbox = sV + (v >> 6) * 8192;
-            float rr[32];
+#pragma unroll 1
+            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                float x[16];
+                ptx::tmem_ld16(tl + C_X + jc, x);
+                ptx::tmem_ld_wait();
+                float rr[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = wg * 32 + j;
-                const float vv = __bfloat162float(
-                    *reinterpret_cast<const __nv_bfloat16 *>(vbox + ptx::sw128_offset(t, v & 63)));
-                const float bt = sBeta[t];
-                rr[j] = bt * (vv - sGam[t] * x[j]);
+                for (int j = 0; j < 16; ++j) {
+                    const int t = jc + j;
+                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                        vbox + ptx::sw128_offset(t, v & 63)));
+                    rr[j] = sBeta[t] * (vv - sGam[t] * x[j]);
+                }
+                ptx::store_split8(sRhi, sRlo, v, jc, rr);
+                ptx::store_split8(sRhi, sRlo, v, jc + 8, rr + 8);
             }
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) ptx::store_split8(sRhi, sRlo, v, wg * 32 + j, rr + j);
         }
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
@@ -953,23 +962,23 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         // ---- O (global) and U~^T hi / lo
         {
             const int v = row;
-            float xq[32], pu[32];
-            ptx::tmem_ld32(tl + C_X + 64 + wg * 32, xq);
-            ptx::tmem_ld32(tl + C_PU + wg * 32, pu);
-            ptx::tmem_ld_wait();
             float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
+#pragma unroll 1
+            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                float xq[16], pu[16], u[16];
+                ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
+                ptx::tmem_ld16(tl + C_PU + jc, pu);
+                ptx::tmem_ld16(tl + C_X + jc, u);
+                ptx::tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int t = wg * 32 + j;
-                if (t < n) ocol[(size_t)t * tok_stride] = fmaf(sGam[t], xq[j], pu[j]) * scale;
+                for (int j = 0; j < 16; ++j) {
+                    const int t = jc + j;
+                    if (t < n) ocol[(size_t)t * tok_stride] = fmaf(sGam[t], xq[j], pu[j]) * scale;
+                    u[j] *= sEnd[t];
+                }
+                ptx::store_split8(sRhi, sRlo, v, jc, u);
+                ptx::store_split8(sRhi, sRlo, v, jc + 8, u + 8);
             }
-            float u[32];
-            ptx::tmem_ld32(tl + C_X + wg * 32, u);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) u[j] *= sEnd[wg * 32 + j];
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) ptx::store_split8(sRhi, sRlo, v, wg * 32 + j, u + j);
         }
         // gates of the next chunk (its gamma_C pre-scales the state below);
         // then start loading the chunk after it
@@ -1002,7 +1011,7 @@ kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtenso
         //      or write the final state
         {
             const float gC = last ? 1.f : gsets[(st ^ 1) * 256 + 128 + 63];
-#pragma unroll
+#pragma unroll 1
             for (int kg = 0; kg < 64; kg += 32) {
                 const int key0 = wg * 64 + kg;
                 float x[32];
@@ -1102,11 +1111,11 @@ cudaError_t launch_d128(const Problem &p, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(d128::kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(d128::chunked_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         d128::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    d128::kernel<<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
+    d128::chunked_d128_kernel<<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
         mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
     return cudaGetLastError();
 }
