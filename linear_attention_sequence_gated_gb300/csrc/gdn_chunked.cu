@@ -113,56 +113,53 @@ __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile
     }
 }
 
-// One block row BI (1..3) of T = (I + A)^-1, 16x16 blocks, 256 threads:
+// One block row BI (1..3) of T = (I + A)^-1, 16x16 blocks, 256 threads,
+// computed in place over A (row stride FST):
 //   W = A[BI, :BI] T[:BI, :BI],  T[BI, j] = -T[BI, BI] W[:, j]   (j < BI)
-// The upper blocks of T must already be zero.  Thread (r, c) = (tid / 16,
-// tid % 16) owns row r, column c of every block of the row.
+// Rows above block row BI already hold T; row block BI still holds A left of
+// its diagonal block.  Entries above the diagonal are zero in both.  Thread
+// (r, c) = (t / 16, t % 16) owns row r, column c of every block of the row.
+// `bar` is a hardware barrier shared by exactly the 256 participating threads.
 template <int BI>
-__device__ __forceinline__ void ut_block_row(const float *sA, float *sT, float *sW, int tid) {
-    const int r = tid >> 4, c = tid & 15;
+__device__ __forceinline__ void ut_block_row(float *sAT, float *sW, int t, int bar) {
+    const int r = t >> 4, c = t & 15;
     float acc[BI];
 #pragma unroll
     for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
-    const float *arow = sA + (BI * 16 + r) * FST;
+    const float *arow = sAT + (BI * 16 + r) * FST;
 #pragma unroll 8
     for (int k = 0; k < BI * 16; ++k) {
         const float a = arow[k];
 #pragma unroll
-        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(a, sT[k * FST + jb * 16 + c], acc[jb]);
+        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(a, sAT[k * FST + jb * 16 + c], acc[jb]);
     }
 #pragma unroll
     for (int jb = 0; jb < BI; ++jb) sW[r * 48 + jb * 16 + c] = acc[jb];
-    __syncthreads();
+    ptx::named_sync(bar, 256);
 #pragma unroll
     for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
-    const float *trow = sT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
+    const float *trow = sAT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-        const float t = trow[m];
+        const float tv = trow[m];
 #pragma unroll
-        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(t, sW[m * 48 + jb * 16 + c], acc[jb]);
+        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(tv, sW[m * 48 + jb * 16 + c], acc[jb]);
     }
 #pragma unroll
-    for (int jb = 0; jb < BI; ++jb) sT[(BI * 16 + r) * FST + jb * 16 + c] = -acc[jb];
-    __syncthreads();
+    for (int jb = 0; jb < BI; ++jb) sAT[(BI * 16 + r) * FST + jb * 16 + c] = -acc[jb];
+    ptx::named_sync(bar, 256);
 }
 
-// T = (I + A)^-1 for a strictly lower triangular 64x64 A (fp32, row stride
-// FST) on 256 threads: the four diagonal 16x16 blocks by column substitution,
-// then the three block rows below them.  T is written in full (zeros above
-// the diagonal).  Starts and ends with the caller's data visible to all.
-__device__ __forceinline__ void ut_transform(const float *sA, float *sT, float *sW, int tid) {
-    // zero the six blocks above the block diagonal
-    for (int e = tid; e < 6 * 256; e += 256) {
-        const int blk = e >> 8, w = e & 255;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        sT[(bi * 16 + (w >> 4)) * FST + bj * 16 + (w & 15)] = 0.f;
-    }
-    if (tid < 64) {
-        const int blk = tid >> 4, j = tid & 15;
-        const float *Ab = sA + (blk * 16) * FST + blk * 16;
-        float x[16];
+// T = (I + A)^-1 in place, for a strictly lower triangular 64x64 A stored in
+// full (zeros on and above the diagonal), on 256 threads (t = 0..255): the
+// four diagonal 16x16 blocks by column substitution, then the three block
+// rows below them.  The result is T in full, zeros above the diagonal.
+// Entered and left with the matrix visible to all participants.
+__device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int bar) {
+    float x[16];
+    const int blk = t >> 4, j = t & 15;
+    if (t < 64) {
+        const float *Ab = sAT + (blk * 16) * FST + blk * 16;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
@@ -170,14 +167,17 @@ __device__ __forceinline__ void ut_transform(const float *sA, float *sT, float *
             for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
             x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
         }
-        float *Tb = sT + (blk * 16) * FST + blk * 16;
+    }
+    ptx::named_sync(bar, 256);
+    if (t < 64) {
+        float *Tb = sAT + (blk * 16) * FST + blk * 16;
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
     }
-    __syncthreads();
-    ut_block_row<1>(sA, sT, sW, tid);
-    ut_block_row<2>(sA, sT, sW, tid);
-    ut_block_row<3>(sA, sT, sW, tid);
+    ptx::named_sync(bar, 256);
+    ut_block_row<1>(sAT, sW, t, bar);
+    ut_block_row<2>(sAT, sW, t, bar);
+    ut_block_row<3>(sAT, sW, t, bar);
 }
 
 template <int D>
@@ -201,7 +201,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float *sEnd = sG + 192;
     float *sA = reinterpret_cast<float *>(sm + CF::OFF_A);
     float *sP = reinterpret_cast<float *>(sm + CF::OFF_P);
-    float *sT = reinterpret_cast<float *>(sm + CF::OFF_T);
     float *sW = reinterpret_cast<float *>(sm + CF::OFF_W);
     uint8_t *sQK = sm + CF::OFF_QK;
     uint8_t *sV = sm + CF::OFF_V;
@@ -233,9 +232,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::tmem_alloc(&bars.tmem_base, CF::TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    // zero: T scratch (its upper triangle is never written) and, for d=64,
-    // the second key slab that pads K^T to 128 rows in the state update
-    for (int i = tid; i < 64 * FST; i += NT) sT[i] = 0.f;
+    // zero, for d=64, the second key slab that pads K^T to 128 rows in the
+    // state update
     if (D == 64)
         for (int i = tid; i < 16384 / 16; i += NT)
             reinterpret_cast<uint4 *>(sQK + 16384)[i] = make_uint4(0, 0, 0, 0);
@@ -373,22 +371,22 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         ptx::tc_fence_before();
         __syncthreads();
-        // 3a/3b. T = (I + A)^-1 by 16x16 blocks
-        ut_transform(sA, sT, sW, tid);
+        // 3a/3b. T = (I + A)^-1 by 16x16 blocks, in place over A
+        ut_transform(sA, sW, tid, 0);
         // 3c. Z rows: thread -> (row r = tid/4, columns 16*(tid%4) .. +15)
         {
             const int r = tid >> 2, c0 = (tid & 3) * 16;
             float t[16], pt[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-                t[e] = sT[r * FST + c0 + e];
+                t[e] = sA[r * FST + c0 + e];
                 pt[e] = 0.f;
             }
             // (P T)[r][j] = sum_{i=j}^{r} P[r][i] T[i][j]   (T[i][j] = 0 for i < j)
             for (int i = c0; i <= r; ++i) {
                 const float p = sP[r * FST + i];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sT[i * FST + c0 + e], pt[e]);
+                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sA[i * FST + c0 + e], pt[e]);
             }
             store_split16(sZhi, sZlo, r, c0, t);
             store_split16(sZhi, sZlo, 64 + r, c0, pt);
@@ -601,20 +599,21 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 namespace d128 {
 
 constexpr int D = 128;
-constexpr int NTH = 256;
+constexpr int NS = 256;                 // threads per stream
+constexpr int NTH = 2 * NS;             // state stream (warps 0-7) + transform stream (8-15)
+constexpr int BAR_S = 1, BAR_Z = 2;     // hardware barrier of each stream
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int OFF_QK = 0;                      // 2 stages x [K;Q] (2 slabs x 128 rows x 128 B)
-constexpr int OFF_V = 65536;                   // 2 stages x V (2 boxes x 64 rows x 128 B)
-constexpr int OFF_Z = 98304;                   // Z hi | Z lo: 128 rows x 128 B each
-constexpr int OFF_UN = 131072;                 // union of the two areas below
-constexpr int OFF_PP = OFF_UN;                 //   P hi (rows 0-63) | P lo (rows 64-127)
-constexpr int OFF_A = OFF_UN + 16384;          //   A, T (fp32 64 x 65 each), W (3 x 256)
-constexpr int OFF_T = OFF_A + 64 * FST * 4;
-constexpr int OFF_W = OFF_T + 64 * FST * 4;
-constexpr int OFF_RT = OFF_UN;                 //   R^T (then U~^T) hi | lo: 128 rows x 128 B each
-constexpr int OFF_MISC = OFF_W + 3 * 256 * 4;  // 2 gate sets x {G, beta, gamma, end-decay}
-constexpr int SMEM = OFF_MISC + 2 * 4 * 64 * 4 + 1024;
-static_assert(OFF_MISC - OFF_UN >= 32768, "R^T hi/lo must fit the union");
+constexpr int OFF_QK = 0;               // 2 stages x [K;Q] (2 slabs x 128 rows x 128 B)
+constexpr int OFF_V = 65536;            // V of one chunk (2 boxes x 64 rows x 128 B)
+constexpr int OFF_Z = 81920;            // 2 buffers x {Z hi, Z lo} (128 rows x 128 B each)
+constexpr int OFF_PP = 147456;          // P hi (rows 0-63) | P lo (rows 64-127)
+constexpr int OFF_AT = 163840;          // A, then T in place: fp32 64 x FST
+constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 48 fp32
+constexpr int OFF_RT = 184320;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
+constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-decay}
+constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
+static_assert(OFF_W + 16 * 48 * 4 <= OFF_RT, "scratch overlaps R^T");
+static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
 static_assert(SMEM <= 232448, "shared memory");
 // TMEM columns
 constexpr uint32_t C_SACC = 0;    // S (fp32): lane = value, column = key
@@ -622,11 +621,15 @@ constexpr uint32_t C_SHI = 128;   // S hi, bf16 pairs (keys 2c, 2c+1 in column c
 constexpr uint32_t C_SLO = 192;   // S lo
 constexpr uint32_t C_X = 256;     // X^T: columns 0-63 K part (then U^T), 64-127 Q part
 constexpr uint32_t C_PU = 384;    // (P U)^T
-constexpr uint32_t C_KQ = 448;    // [K;Q] K^T, then P T (lanes 0-63)
+constexpr uint32_t C_KQ = 448;    // [K;Q] K^T, then P T (lanes 0-63): transform stream only
 
 struct Shared {
-    uint64_t tma[2];
-    uint64_t mma;
+    uint64_t qk_full[2];   // TMA: [K;Q] of the chunk in the stage has landed
+    uint64_t v_full;       // TMA: V of the chunk has landed
+    uint64_t z_ready[2];   // transform stream: Z = [T; P T] of the chunk is in its buffer
+    uint64_t z_free[2];    // state stream MMA: the last reads of a Z buffer have completed
+    uint64_t g_ready[4];   // transform stream: the chunk's gate set is written
+    uint64_t mma_s, mma_z; // each stream's MMA completions
     uint32_t tmem_base;
     int abort;
 };
@@ -641,22 +644,21 @@ struct GateRegs {
 };
 
 __device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const float *beta, int b,
-                                           int h, int T, int H, int c, int tid) {
+                                           int h, int T, int H, int c, int t) {
     const int t0 = c * C;
     const int n = min(C, T - t0);
-    const int l = tid & 31, own = tid;
+    const int l = t & 31;
     const size_t base = ((size_t)b * T + t0) * H + h;
-    // raw values only: the clamp happens in scan_gates, so these loads stay
-    // in flight until the scan, a chunk later
     r.ga = (l < n) ? g[base + (size_t)l * H] : 0.f;
     r.gb = (32 + l < n) ? g[base + (size_t)(32 + l) * H] : 0.f;
-    r.bown = (own < n) ? beta[base + (size_t)own * H] : 0.f;
+    r.bown = (t < n) ? beta[base + (size_t)t * H] : 0.f;
 }
 
-// G = inclusive cumsum, gamma = exp(G), end = exp(G_63 - G) into a gate set
-// {G, beta, gamma, end} (4 x 64 floats).  Threads 0-63, no barrier inside.
-__device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int tid) {
-    const int l = tid & 31;
+// G = inclusive cumsum of max(g, -30), gamma = exp(G), end = exp(G_63 - G)
+// into a gate set {G, beta, gamma, end} (4 x 64 floats).  Threads 0-63 of a
+// stream (t), no barrier inside.
+__device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) {
+    const int l = t & 31;
     float sa = fmaxf(r.ga, -30.f), sb = fmaxf(r.gb, -30.f);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -666,52 +668,64 @@ __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int tid
     }
     const float tot0 = __shfl_sync(0xffffffffu, sa, 31);
     const float tot = tot0 + __shfl_sync(0xffffffffu, sb, 31);
-    const float G = (tid < 32) ? sa : tot0 + sb;
-    gs[tid] = G;
-    gs[64 + tid] = r.bown;
-    gs[128 + tid] = ex(G);
-    gs[192 + tid] = ex(tot - G);
+    const float G = (t < 32) ? sa : tot0 + sb;
+    gs[t] = G;
+    gs[64 + t] = r.bown;
+    gs[128 + t] = ex(G);
+    gs[192 + t] = ex(tot - G);
 }
 
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
 // columns, gamma * S -> 32 fp32 columns.
 __device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const float (&x)[32],
                                             float gamma) {
-    uint32_t hi[16], lo[16], sc[16];
+    uint32_t w[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) ptx::split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
-    ptx::tmem_st16(tmem_lane + C_SHI + key0 / 2, hi);
-    ptx::tmem_st16(tmem_lane + C_SLO + key0 / 2, lo);
+    for (int e = 0; e < 16; ++e) {
+        uint32_t lo;
+        ptx::split_pair(x[2 * e], x[2 * e + 1], w[e], lo);
+        (void)lo;
+    }
+    ptx::tmem_st16(tmem_lane + C_SHI + key0 / 2, w);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) sc[e] = __float_as_uint(gamma * x[e]);
-    ptx::tmem_st16(tmem_lane + C_SACC + key0, sc);
+    for (int e = 0; e < 16; ++e) {
+        uint32_t hi;
+        ptx::split_pair(x[2 * e], x[2 * e + 1], hi, w[e]);
+        (void)hi;
+    }
+    ptx::tmem_st16(tmem_lane + C_SLO + key0 / 2, w);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) sc[e] = __float_as_uint(gamma * x[16 + e]);
-    ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, sc);
+    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(gamma * x[e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0, w);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(gamma * x[16 + e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, w);
 }
 
 __global__ void __launch_bounds__(NTH, 1)
-chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-       const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
-       const float *__restrict__ beta, const float *state_in, float *state_out,
-       float *__restrict__ out, int T, int H, float scale, int *status)
+chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
+                    const float *__restrict__ beta, const float *state_in, float *state_out,
+                    float *__restrict__ out, int T, int H, float scale, int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     __shared__ Shared sh;
-    float *sA = reinterpret_cast<float *>(sm + OFF_A);
-    float *sT = reinterpret_cast<float *>(sm + OFF_T);
+    float *sAT = reinterpret_cast<float *>(sm + OFF_AT);
     float *sW = reinterpret_cast<float *>(sm + OFF_W);
-    float *gsets = reinterpret_cast<float *>(sm + OFF_MISC);
-    uint8_t *sZhi = sm + OFF_Z, *sZlo = sm + OFF_Z + 16384;
+    float *gsets = reinterpret_cast<float *>(sm + OFF_G);
     uint8_t *sPhi = sm + OFF_PP, *sPlo = sm + OFF_PP + 8192;
     uint8_t *sRhi = sm + OFF_RT, *sRlo = sm + OFF_RT + 16384;
+    uint8_t *sV = sm + OFF_V;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
-    const int wg = tid >> 7;                 // which half of the columns this thread handles
-    const int row = tid & 127;               // TMEM lane: value row, or [K;Q] row
+    const bool zstream = tid >= NS;          // transform stream
+    const int t = tid & (NS - 1);            // thread index within the stream
+    const int wg = t >> 7;                   // which half of the columns this thread handles
+    const int row = t & 127;                 // TMEM lane: value row, or [K;Q] row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh - b * H;
@@ -721,9 +735,16 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
     if (tid == 0) {
         sh.abort = 0;
-        ptx::mbar_init(&sh.tma[0], 1);
-        ptx::mbar_init(&sh.tma[1], 1);
-        ptx::mbar_init(&sh.mma, 1);
+        ptx::mbar_init(&sh.qk_full[0], 1);
+        ptx::mbar_init(&sh.qk_full[1], 1);
+        ptx::mbar_init(&sh.v_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sh.z_ready[i], 1);
+            ptx::mbar_init(&sh.z_free[i], 1);
+        }
+        for (int i = 0; i < 4; ++i) ptx::mbar_init(&sh.g_ready[i], 1);
+        ptx::mbar_init(&sh.mma_s, 1);
+        ptx::mbar_init(&sh.mma_z, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
@@ -744,140 +765,126 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     auto fail = [&]() {
         if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
     };
-    auto wait_mma = [&]() {
-        if (!ptx::mbar_wait(&sh.mma, mma_phase, abort_flag)) fail();
-        mma_phase ^= 1;
-        ptx::tc_fence_after();
+    auto wait = [&](uint64_t *bar, uint32_t parity) {
+        if (!ptx::mbar_wait(bar, parity, abort_flag)) fail();
     };
-    auto issue_loads = [&](int c) {
+    auto issue_qk = [&](int c) {
         const int st = c & 1;
         uint8_t *qk = sm + OFF_QK + st * 32768;
-        uint8_t *vv = sm + OFF_V + st * 16384;
-        ptx::mbar_arrive_expect_tx(&sh.tma[st], 6 * 8192);
+        ptx::mbar_arrive_expect_tx(&sh.qk_full[st], 4 * 8192);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
-            ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.tma[st], s * 64, h, c * C, b);
-            ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.tma[st], s * 64, h, c * C, b);
-            ptx::tma_load_4d(vv + s * 8192, &tm_v, &sh.tma[st], s * 64, h, c * C, b);
+            ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.qk_full[st], s * 64, h, c * C, b);
+            ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.qk_full[st], s * 64, h, c * C, b);
         }
     };
+    auto issue_v = [&](int c) {
+        ptx::mbar_arrive_expect_tx(&sh.v_full, 2 * 8192);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+            ptx::tma_load_4d(sV + s * 8192, &tm_v, &sh.v_full, s * 64, h, c * C, b);
+    };
     if (tid == 0) {
-        issue_loads(0);
-        if (n_chunks > 1) issue_loads(1);
+        issue_qk(0);
+        if (n_chunks > 1) issue_qk(1);
+        issue_v(0);
     }
-    GateRegs gr{0.f, 0.f, 0.f};     // gates of the next chunk (threads 0-63)
-    if (tid < 64) {
-        load_gates(gr, g, beta, b, h, T, H, 0, tid);
-        scan_gates(gr, gsets, tid);
-        if (n_chunks > 1) load_gates(gr, g, beta, b, h, T, H, 1, tid);
-    }
-    __syncthreads();
 
-    // ---- initial state: thread (value row, key half) -> TMEM
-    {
-        const float gC = gsets[128 + 63];
-#pragma unroll 1
-        for (int kg = 0; kg < 64; kg += 32) {
-            const int key0 = wg * 64 + kg;
-            float x[32];
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-                float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (state_in)
-                    t4 = *reinterpret_cast<const float4 *>(state_in + st_base + (size_t)row * D +
-                                                           key0 + e);
-                x[e] = t4.x; x[e + 1] = t4.y; x[e + 2] = t4.z; x[e + 3] = t4.w;
+    if (zstream) {
+        // ================= transform stream: Z = [T; P T] of every chunk
+        for (int c = 0; c < n_chunks; ++c) {
+            const int st = c & 1;
+            const uint32_t aQK = ptx::smem_u32(sm + OFF_QK + st * 32768);
+            float *gs = gsets + (c & 3) * 256;
+            const float *sG = gs, *sBeta = gs + 64;
+            uint8_t *sZhi = sm + OFF_Z + st * 32768, *sZlo = sZhi + 16384;
+
+            if (t < 64) {
+                GateRegs gr;
+                load_gates(gr, g, beta, b, h, T, H, c, t);
+                scan_gates(gr, gs, t);
             }
-            put_state32(tl, key0, x, gC);
-        }
-        ptx::tmem_st_wait();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-
-    for (int c = 0; c < n_chunks; ++c) {
-        if (*abort_flag) break;      // read right after a barrier: uniform
-        const int st = c & 1;
-        const int t0 = c * C;
-        const int n = min(C, T - t0);
-        const float *gs = gsets + st * 256;
-        const float *sG = gs, *sBeta = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
-        uint8_t *sQK = sm + OFF_QK + st * 32768;
-        uint8_t *sV = sm + OFF_V + st * 16384;
-        const uint32_t aQK = ptx::smem_u32(sQK);
-        const bool last = (c + 1 == n_chunks);
-
-        if (!ptx::mbar_wait(&sh.tma[st], (uint32_t)((c >> 1) & 1), abort_flag)) fail();
-        __syncthreads();
-        if (*abort_flag) break;
-
-        // ---- [K;Q] K^T  (M = 128, N = 64, K = 128)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+            wait(&sh.qk_full[st], (uint32_t)((c >> 1) & 1));
+            ptx::named_sync(BAR_Z, NS);
+            const bool ok = !*abort_flag;
+            if (t == 0) {
+                ptx::mbar_arrive(&sh.g_ready[c & 3]);
+                // [K;Q] K^T  (M = 128, N = 64, K = 128)
+                if (ok) {
+                    ptx::tc_fence_after();
+                    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t da = ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                ptx::mma_bf16(tmem + C_KQ, da, da, idesc, kk > 0);
-            }
-            ptx::mma_commit(&sh.mma);
-        }
-        wait_mma();
-
-        // ---- A (rows 0-63) to shared fp32; P (rows 64-127) as hi / lo rows
-        //      (16 columns per step: small code, the loop stays in the I-cache)
-        {
-            const int r = row & 63;
-            const float Gr = sG[r];
-            const float br = sBeta[r];
-#pragma unroll 1
-            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                float kq[16];
-                ptx::tmem_ld16(tl + C_KQ + jc, kq);
-                ptx::tmem_ld_wait();
-                if (row < 64) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = jc + j;
-                        sA[r * FST + i] = (i < r) ? br * ex(Gr - sG[i]) * kq[j] : 0.f;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t da =
+                            ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        ptx::mma_bf16(tmem + C_KQ, da, da, idesc, kk > 0);
                     }
-                } else {
-                    float p[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int i = jc + j;
-                        p[j] = (i <= r) ? ex(Gr - sG[i]) * kq[j] : 0.f;
-                    }
-                    ptx::store_split8(sPhi, sPlo, r, jc, p);
-                    ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
+                    ptx::mma_commit(&sh.mma_z);
                 }
             }
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- T = (I + A)^-1 by 16x16 blocks
-        ut_transform(sA, sT, sW, tid);
-        // ---- T as hi / lo into Z rows 0-63 (upper blocks are zero)
-        {
-            const int r = tid >> 2, c0 = (tid & 3) * 16;
-            float t[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                t[e] = sT[r * FST + c0 + e];
-            }
-            ptx::store_split8(sZhi, sZlo, r, c0, t);
-            ptx::store_split8(sZhi, sZlo, r, c0 + 8, t + 8);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-
-        // ---- P T (M = 128 rows of [P hi; P lo], N = 64, K = 64) and
-        //      X^T = S [K;Q]^T (A = S hi / lo from TMEM, M = 128, N = 128, K = 128)
-        if (tid == 0) {
+            wait(&sh.mma_z, mma_phase);
+            mma_phase ^= 1;
             ptx::tc_fence_after();
+
+            // A (rows 0-63) as fp32; P (rows 64-127) as hi / lo rows
             {
+                const int r = row & 63;
+                const float Gr = sG[r];
+                const float br = sBeta[r];
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float kq[16];
+                    ptx::tmem_ld16(tl + C_KQ + jc, kq);
+                    ptx::tmem_ld_wait();
+                    const float4 *g4 = reinterpret_cast<const float4 *>(sG + jc);
+                    float gi[16];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float4 v4 = g4[q];
+                        gi[4 * q] = v4.x; gi[4 * q + 1] = v4.y; gi[4 * q + 2] = v4.z; gi[4 * q + 3] = v4.w;
+                    }
+                    if (row < 64) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int i = jc + j;
+                            sAT[r * FST + i] = (i < r) ? br * ex(Gr - gi[j]) * kq[j] : 0.f;
+                        }
+                    } else {
+                        float p[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int i = jc + j;
+                            p[j] = (i <= r) ? ex(Gr - gi[j]) * kq[j] : 0.f;
+                        }
+                        ptx::store_split8(sPhi, sPlo, r, jc, p);
+                        ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(BAR_Z, NS);
+
+            // T = (I + A)^-1 in place
+            ut_transform(sAT, sW, t, BAR_Z);
+
+            // T as hi / lo into rows 0-63 of this chunk's Z buffer, once the
+            // state stream has finished with the chunk that used it before
+            if (c >= 2) wait(&sh.z_free[st], (uint32_t)(((c - 2) >> 1) & 1));
+            {
+                const int r = t >> 2, c0 = (t & 3) * 16;
+                float tv[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) tv[e] = sAT[r * FST + c0 + e];
+                ptx::store_split8(sZhi, sZlo, r, c0, tv);
+                ptx::store_split8(sZhi, sZlo, r, c0 + 8, tv + 8);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(BAR_Z, NS);
+
+            // P T  (A = [P hi; P lo] 128 rows, B = T rows (MN-major), N = 64, K = 64)
+            if (t == 0 && !*abort_flag) {
+                ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, true);
                 const uint32_t aP[3] = {ptx::smem_u32(sPhi), ptx::smem_u32(sPhi), ptx::smem_u32(sPlo)};
                 const uint32_t bT[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
@@ -888,8 +895,70 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                         ptx::mma_bf16(tmem + C_KQ, ptx::smem_desc(aP[part] + kk * 32, 16, 1024),
                                       ptx::smem_desc(bT[part] + kk * 2048, 8192, 1024), idesc,
                                       part > 0 || kk > 0);
+                ptx::mma_commit(&sh.mma_z);
             }
-            {
+            wait(&sh.mma_z, mma_phase);
+            mma_phase ^= 1;
+            ptx::tc_fence_after();
+
+            // P T rows -> Z rows 64-127 (TMEM lanes 0-63)
+            if ((warp & 3) < 2) {
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float pt[16];
+                    ptx::tmem_ld16(tl + C_KQ + jc, pt);
+                    ptx::tmem_ld_wait();
+                    ptx::store_split8(sZhi, sZlo, 64 + row, jc, pt);
+                    ptx::store_split8(sZhi, sZlo, 64 + row, jc + 8, pt + 8);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(BAR_Z, NS);
+            if (t == 0) ptx::mbar_arrive(&sh.z_ready[st]);
+        }
+    } else {
+        // ================= state stream
+        // initial state: thread (value row, key half) -> TMEM, pre-scaled by
+        // the first chunk's gamma_C for the in-place accumulation
+        wait(&sh.g_ready[0], 0);
+        {
+            const float gC = gsets[128 + 63];
+#pragma unroll 1
+            for (int kg = 0; kg < 64; kg += 32) {
+                const int key0 = wg * 64 + kg;
+                float x[32];
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (state_in)
+                        t4 = *reinterpret_cast<const float4 *>(state_in + st_base +
+                                                               (size_t)row * D + key0 + e);
+                    x[e] = t4.x; x[e + 1] = t4.y; x[e + 2] = t4.z; x[e + 3] = t4.w;
+                }
+                put_state32(tl, key0, x, gC);
+            }
+            ptx::tmem_st_wait();
+        }
+        ptx::tc_fence_before();
+        ptx::named_sync(BAR_S, NS);
+
+        for (int c = 0; c < n_chunks; ++c) {
+            const int st = c & 1;
+            const int t0 = c * C;
+            const int n = min(C, T - t0);
+            const bool last = (c + 1 == n_chunks);
+            const float *gs = gsets + (c & 3) * 256;
+            const float *sBeta = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
+            const uint32_t aQK = ptx::smem_u32(sm + OFF_QK + st * 32768);
+            uint8_t *sZhi = sm + OFF_Z + st * 32768, *sZlo = sZhi + 16384;
+
+            wait(&sh.g_ready[c & 3], (uint32_t)((c >> 2) & 1));
+            wait(&sh.qk_full[st], (uint32_t)((c >> 1) & 1));
+
+            // X^T = S [K;Q]^T  (A = S hi / lo from TMEM, M = 128, N = 128, K = 128)
+            if (t == 0 && !*abort_flag) {
+                ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -899,123 +968,120 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                          ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32,
                                                         16, 1024),
                                          idesc, part > 0 || kk > 0);
+                ptx::mma_commit(&sh.mma_s);
             }
-            ptx::mma_commit(&sh.mma);
-        }
-        wait_mma();
-
-        // ---- P T rows -> Z rows 64-127 (lanes 0-63); R^T (all threads)
-        if ((warp & 3) < 2) {
-#pragma unroll 1
-            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                float pt[16];
-                ptx::tmem_ld16(tl + C_KQ + jc, pt);
-                ptx::tmem_ld_wait();
-                ptx::store_split8(sZhi, sZlo, 64 + row, jc, pt);
-                ptx::store_split8(sZhi, sZlo, 64 + row, jc + 8, pt + 8);
-            }
-        }
-        {
-            const int v = row;
-            const uint8_t *vbox = sV + (v >> 6) * 8192;
-#pragma unroll 1
-            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                float x[16];
-                ptx::tmem_ld16(tl + C_X + jc, x);
-                ptx::tmem_ld_wait();
-                float rr[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = jc + j;
-                    const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        vbox + ptx::sw128_offset(t, v & 63)));
-                    rr[j] = sBeta[t] * (vv - sGam[t] * x[j]);
-                }
-                ptx::store_split8(sRhi, sRlo, v, jc, rr);
-                ptx::store_split8(sRhi, sRlo, v, jc + 8, rr + 8);
-            }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- U^T = R^T T^T (into the K part of X), (P U)^T = R^T (P T)^T
-        if (tid == 0) {
+            wait(&sh.mma_s, mma_phase);
+            mma_phase ^= 1;
             ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
-            const uint32_t aR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
-            const uint32_t bZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
+
+            // R^T = beta V^T - beta gamma (K S^T)^T  (value row v, tokens of this half)
+            wait(&sh.v_full, (uint32_t)(c & 1));
+            {
+                const int v = row;
+                const uint8_t *vbox = sV + (v >> 6) * 8192;
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float x[16];
+                    ptx::tmem_ld16(tl + C_X + jc, x);
+                    ptx::tmem_ld_wait();
+                    float rr[16];
 #pragma unroll
-            for (int half = 0; half < 2; ++half)
+                    for (int j = 0; j < 16; ++j) {
+                        const int tk = jc + j;
+                        const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                            vbox + ptx::sw128_offset(tk, v & 63)));
+                        rr[j] = sBeta[tk] * (vv - sGam[tk] * x[j]);
+                    }
+                    ptx::store_split8(sRhi, sRlo, v, jc, rr);
+                    ptx::store_split8(sRhi, sRlo, v, jc + 8, rr + 8);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(BAR_S, NS);
+            if (t == 0 && !last && !*abort_flag) issue_v(c + 1);   // V of this chunk consumed
+
+            // U^T = R^T T^T (into the K part of X), (P U)^T = R^T (P T)^T
+            wait(&sh.z_ready[st], (uint32_t)((c >> 1) & 1));
+            if (t == 0 && !*abort_flag) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+                const uint32_t aR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+                const uint32_t bZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
 #pragma unroll
-                for (int part = 0; part < 3; ++part)
+                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            ptx::mma_bf16(tmem + (half ? C_PU : C_X),
+                                          ptx::smem_desc(aR[part] + kk * 32, 16, 1024),
+                                          ptx::smem_desc(bZ[part] + half * 8192 + kk * 32, 16, 1024),
+                                          idesc, part > 0 || kk > 0);
+                ptx::mma_commit(&sh.mma_s);
+                ptx::mma_commit(&sh.z_free[st]);
+            }
+            wait(&sh.mma_s, mma_phase);
+            mma_phase ^= 1;
+            ptx::tc_fence_after();
+
+            // O (global) and U~^T hi / lo
+            {
+                const int v = row;
+                float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float xq[16], pu[16], u[16];
+                    ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
+                    ptx::tmem_ld16(tl + C_PU + jc, pu);
+                    ptx::tmem_ld16(tl + C_X + jc, u);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tk = jc + j;
+                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(sGam[tk], xq[j], pu[j]) * scale;
+                        u[j] *= sEnd[tk];
+                    }
+                    ptx::store_split8(sRhi, sRlo, v, jc, u);
+                    ptx::store_split8(sRhi, sRlo, v, jc + 8, u + 8);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(BAR_S, NS);
+
+            // S += U~^T K  (M = 128 values, N = 128 keys, K = 64 tokens)
+            if (t == 0 && !*abort_flag) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+                const uint32_t aU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+#pragma unroll
+                for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        ptx::mma_bf16(tmem + (half ? C_PU : C_X),
-                                      ptx::smem_desc(aR[part] + kk * 32, 16, 1024),
-                                      ptx::smem_desc(bZ[part] + half * 8192 + kk * 32, 16, 1024),
-                                      idesc, part > 0 || kk > 0);
-            ptx::mma_commit(&sh.mma);
-        }
-        wait_mma();
-
-        // ---- O (global) and U~^T hi / lo
-        {
-            const int v = row;
-            float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
-#pragma unroll 1
-            for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                float xq[16], pu[16], u[16];
-                ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
-                ptx::tmem_ld16(tl + C_PU + jc, pu);
-                ptx::tmem_ld16(tl + C_X + jc, u);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = jc + j;
-                    if (t < n) ocol[(size_t)t * tok_stride] = fmaf(sGam[t], xq[j], pu[j]) * scale;
-                    u[j] *= sEnd[t];
-                }
-                ptx::store_split8(sRhi, sRlo, v, jc, u);
-                ptx::store_split8(sRhi, sRlo, v, jc + 8, u + 8);
+                        ptx::mma_bf16(tmem + C_SACC, ptx::smem_desc(aU[part] + kk * 32, 16, 1024),
+                                      ptx::smem_desc(aQK + kk * 2048, 16384, 1024), idesc, true);
+                ptx::mma_commit(&sh.mma_s);
             }
-        }
-        // gates of the next chunk (its gamma_C pre-scales the state below);
-        // then start loading the chunk after it
-        if (tid < 64 && !last) {
-            scan_gates(gr, gsets + (st ^ 1) * 256, tid);
-            if (c + 2 < n_chunks) load_gates(gr, g, beta, b, h, T, H, c + 2, tid);
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-
-        // ---- S += U~^T K  (M = 128 values, N = 128 keys, K = 64 tokens)
-        if (tid == 0) {
+            wait(&sh.mma_s, mma_phase);
+            mma_phase ^= 1;
             ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
-            const uint32_t aU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
-#pragma unroll
-            for (int part = 0; part < 2; ++part)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    ptx::mma_bf16(tmem + C_SACC, ptx::smem_desc(aU[part] + kk * 32, 16, 1024),
-                                  ptx::smem_desc(aQK + kk * 2048, 16384, 1024), idesc, true);
-            ptx::mma_commit(&sh.mma);
-        }
-        wait_mma();
-        // this chunk's stage is free: bring chunk c + 2 into it
-        if (tid == 0 && c + 2 < n_chunks) issue_loads(c + 2);
+            // this stage is free: bring chunk c + 2 into it
+            if (t == 0 && c + 2 < n_chunks && !*abort_flag) issue_qk(c + 2);
 
-        // ---- S: split for the next chunk's X^T and pre-scale by its gamma_C,
-        //      or write the final state
-        {
-            const float gC = last ? 1.f : gsets[(st ^ 1) * 256 + 128 + 63];
+            // S: split for the next chunk's X^T and pre-scale by its gamma_C,
+            // or write the final state
+            float gC = 1.f;
+            if (!last) {
+                wait(&sh.g_ready[(c + 1) & 3], (uint32_t)(((c + 1) >> 2) & 1));
+                gC = gsets[((c + 1) & 3) * 256 + 128 + 63];
+            }
 #pragma unroll 1
             for (int kg = 0; kg < 64; kg += 32) {
                 const int key0 = wg * 64 + kg;
                 float x[32];
-                ptx::tmem_ld32(tl + C_SACC + key0, x);
+                ptx::tmem_ld16(tl + C_SACC + key0, *reinterpret_cast<float(*)[16]>(x));
+                ptx::tmem_ld16(tl + C_SACC + key0 + 16, *reinterpret_cast<float(*)[16]>(x + 16));
                 ptx::tmem_ld_wait();
                 if (last) {
                     float *dst = state_out + st_base + (size_t)row * D + key0;
@@ -1028,10 +1094,9 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
             }
             if (!last) ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::named_sync(BAR_S, NS);
         }
-        ptx::tc_fence_before();
-        __syncthreads();
-        ptx::tc_fence_after();
     }
 
     ptx::tc_fence_before();

@@ -234,6 +234,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Barrier among `nthreads` threads (a multiple of 32) using hardware barrier
+// `id` (1..15; 0 is __syncthreads).
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ------------------------------------------------------------- bf16 helpers
 
 // Round-to-nearest-even fp32 -> bf16 bits, and the exact residual.
