@@ -53,7 +53,7 @@ namespace {
 
 constexpr int C = 64;            // chunk length (tokens)
 constexpr int NT = 256;          // threads per CTA (two warpgroups)
-constexpr int FST = 65;          // fp32 row stride of the 64x64 scratch matrices
+constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrices (16-B rows)
 
 template <int D>
 struct Cfg {
@@ -92,7 +92,13 @@ struct Bars {
     int abort;
 };
 
-__device__ __forceinline__ float fast_exp(float x) { return expf(x); }
+// exp(x) via the hardware 2^x; results below the fp32 normal range flush to
+// zero (a decay factor under 1e-38 is zero for every purpose here).
+__device__ __forceinline__ float fast_exp(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+    return y;
+}
 
 // Store 16 consecutive fp32 values as bf16 hi / lo into two 128-B-swizzled
 // tiles at (row, col0 .. col0+15); col0 is a multiple of 8.
@@ -113,48 +119,65 @@ __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile
     }
 }
 
-// One block row BI (1..3) of T = (I + A)^-1, 16x16 blocks, 256 threads,
-// computed in place over A (row stride FST):
+// One block row BI (1..3) of T = (I + A)^-1 (16x16 blocks, row stride FST),
+// computed in place over A:
 //   W = A[BI, :BI] T[:BI, :BI],  T[BI, j] = -T[BI, BI] W[:, j]   (j < BI)
 // Rows above block row BI already hold T; row block BI still holds A left of
-// its diagonal block.  Entries above the diagonal are zero in both.  Thread
-// (r, c) = (t / 16, t % 16) owns row r, column c of every block of the row.
-// `bar` is a hardware barrier shared by exactly the 256 participating threads.
+// its diagonal block; entries above the diagonal are zero in both.  Thread
+// (r, q) = (t / (4 BI), t % (4 BI)) for t < 64 BI owns row r and the four
+// columns 4q .. 4q+3 of the row block, so each 128-bit load feeds four FMAs.
+// `bar` is a hardware barrier shared by exactly 256 threads (t = 0..255).
 template <int BI>
 __device__ __forceinline__ void ut_block_row(float *sAT, float *sW, int t, int bar) {
-    const int r = t >> 4, c = t & 15;
-    float acc[BI];
+    constexpr int NQ = 4 * BI;               // column quads per row
+    const bool act = t < 16 * NQ;
+    const int r = t / NQ, q = t % NQ;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
+        const float *arow = sAT + (BI * 16 + r) * FST;
+#pragma unroll 4
+        for (int k4 = 0; k4 < BI * 16; k4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(arow + k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-    for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
-    const float *arow = sAT + (BI * 16 + r) * FST;
-#pragma unroll 8
-    for (int k = 0; k < BI * 16; ++k) {
-        const float a = arow[k];
-#pragma unroll
-        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(a, sAT[k * FST + jb * 16 + c], acc[jb]);
+            for (int e = 0; e < 4; ++e) {
+                const float4 tq = *reinterpret_cast<const float4 *>(sAT + (k4 + e) * FST + 4 * q);
+                acc.x = fmaf(av[e], tq.x, acc.x);
+                acc.y = fmaf(av[e], tq.y, acc.y);
+                acc.z = fmaf(av[e], tq.z, acc.z);
+                acc.w = fmaf(av[e], tq.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(sW + r * 48 + 4 * q) = acc;
     }
-#pragma unroll
-    for (int jb = 0; jb < BI; ++jb) sW[r * 48 + jb * 16 + c] = acc[jb];
     ptx::named_sync(bar, 256);
+    if (act) {
+        acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *trow = sAT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
 #pragma unroll
-    for (int jb = 0; jb < BI; ++jb) acc[jb] = 0.f;
-    const float *trow = sAT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 tv = *reinterpret_cast<const float4 *>(trow + m4);
+            const float tvv[4] = {tv.x, tv.y, tv.z, tv.w};
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const float tv = trow[m];
-#pragma unroll
-        for (int jb = 0; jb < BI; ++jb) acc[jb] = fmaf(tv, sW[m * 48 + jb * 16 + c], acc[jb]);
+            for (int e = 0; e < 4; ++e) {
+                const float4 w = *reinterpret_cast<const float4 *>(sW + (m4 + e) * 48 + 4 * q);
+                acc.x = fmaf(tvv[e], w.x, acc.x);
+                acc.y = fmaf(tvv[e], w.y, acc.y);
+                acc.z = fmaf(tvv[e], w.z, acc.z);
+                acc.w = fmaf(tvv[e], w.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(sAT + (BI * 16 + r) * FST + 4 * q) =
+            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-#pragma unroll
-    for (int jb = 0; jb < BI; ++jb) sAT[(BI * 16 + r) * FST + jb * 16 + c] = -acc[jb];
     ptx::named_sync(bar, 256);
 }
 
 // T = (I + A)^-1 in place, for a strictly lower triangular 64x64 A stored in
-// full (zeros on and above the diagonal), on 256 threads (t = 0..255): the
-// four diagonal 16x16 blocks by column substitution, then the three block
-// rows below them.  The result is T in full, zeros above the diagonal.
-// Entered and left with the matrix visible to all participants.
+// full (zeros on and above the diagonal, row stride FST), on 256 threads
+// (t = 0..255): the four diagonal 16x16 blocks by column substitution, then
+// the three block rows below them.  The result is T in full, zeros above the
+// diagonal.  Entered and left with the matrix visible to all participants.
 __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int bar) {
     float x[16];
     const int blk = t >> 4, j = t & 15;
@@ -162,9 +185,17 @@ __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int b
         const float *Ab = sAT + (blk * 16) * FST + blk * 16;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+            float a[16];
+#pragma unroll
+            for (int i4 = 0; i4 < 16; i4 += 4) {
+                if (i4 < r) {
+                    const float4 v = *reinterpret_cast<const float4 *>(Ab + r * FST + i4);
+                    a[i4] = v.x; a[i4 + 1] = v.y; a[i4 + 2] = v.z; a[i4 + 3] = v.w;
+                }
+            }
             float acc = 0.f;
 #pragma unroll
-            for (int i = 0; i < r; ++i) acc = fmaf(Ab[r * FST + i], x[i], acc);
+            for (int i = 0; i < r; ++i) acc = fmaf(a[i], x[i], acc);
             x[r] = (r == j) ? 1.f : ((r > j) ? -acc : 0.f);
         }
     }
@@ -634,7 +665,15 @@ struct Shared {
     int abort;
 };
 
-__device__ __forceinline__ float ex(float x) { return __expf(x); }
+constexpr float LOG2E = 1.4426950408889634f;
+
+// 2^x; results below the fp32 normal range flush to zero (a decay factor
+// under 1e-38 is zero for every purpose here).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Gates of one chunk, held by threads 0-63 between the global loads and
 // the scan: lane l of warp w keeps g of tokens l and 32 + l (0 past T) and
@@ -654,9 +693,10 @@ __device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const fl
     r.bown = (t < n) ? beta[base + (size_t)t * H] : 0.f;
 }
 
-// G = inclusive cumsum of max(g, -30), gamma = exp(G), end = exp(G_63 - G)
-// into a gate set {G, beta, gamma, end} (4 x 64 floats).  Threads 0-63 of a
-// stream (t), no barrier inside.
+// G = inclusive cumsum of max(g, -30), kept in log2 units (G2 = G log2 e),
+// gamma = exp(G) = 2^G2, end = exp(G_63 - G) into a gate set
+// {G2, beta, gamma, end} (4 x 64 floats).  Threads 0-63 of a stream (t), no
+// barrier inside.
 __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) {
     const int l = t & 31;
     float sa = fmaxf(r.ga, -30.f), sb = fmaxf(r.gb, -30.f);
@@ -669,10 +709,10 @@ __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) 
     const float tot0 = __shfl_sync(0xffffffffu, sa, 31);
     const float tot = tot0 + __shfl_sync(0xffffffffu, sb, 31);
     const float G = (t < 32) ? sa : tot0 + sb;
-    gs[t] = G;
+    gs[t] = G * LOG2E;
     gs[64 + t] = r.bown;
-    gs[128 + t] = ex(G);
-    gs[192 + t] = ex(tot - G);
+    gs[128 + t] = ex2(G * LOG2E);
+    gs[192 + t] = ex2((tot - G) * LOG2E);
 }
 
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
@@ -844,17 +884,22 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                         gi[4 * q] = v4.x; gi[4 * q + 1] = v4.y; gi[4 * q + 2] = v4.z; gi[4 * q + 3] = v4.w;
                     }
                     if (row < 64) {
+                        float a[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int i = jc + j;
-                            sAT[r * FST + i] = (i < r) ? br * ex(Gr - gi[j]) * kq[j] : 0.f;
+                            a[j] = (i < r) ? br * ex2(Gr - gi[j]) * kq[j] : 0.f;
                         }
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(sAT + r * FST + jc + j) =
+                                make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
                     } else {
                         float p[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int i = jc + j;
-                            p[j] = (i <= r) ? ex(Gr - gi[j]) * kq[j] : 0.f;
+                            p[j] = (i <= r) ? ex2(Gr - gi[j]) * kq[j] : 0.f;
                         }
                         ptx::store_split8(sPhi, sPlo, r, jc, p);
                         ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
@@ -984,13 +1029,20 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     float x[16];
                     ptx::tmem_ld16(tl + C_X + jc, x);
                     ptx::tmem_ld_wait();
-                    float rr[16];
+                    float rr[16], bt[16], gm[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + jc + j);
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
+                        bt[j] = b4.x; bt[j + 1] = b4.y; bt[j + 2] = b4.z; bt[j + 3] = b4.w;
+                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int tk = jc + j;
                         const float vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                             vbox + ptx::sw128_offset(tk, v & 63)));
-                        rr[j] = sBeta[tk] * (vv - sGam[tk] * x[j]);
+                        rr[j] = bt[j] * (vv - gm[j] * x[j]);
                     }
                     ptx::store_split8(sRhi, sRlo, v, jc, rr);
                     ptx::store_split8(sRhi, sRlo, v, jc + 8, rr + 8);
@@ -1036,11 +1088,19 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     ptx::tmem_ld16(tl + C_PU + jc, pu);
                     ptx::tmem_ld16(tl + C_X + jc, u);
                     ptx::tmem_ld_wait();
+                    float gm[16], en[16];
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
+                        const float4 e4 = *reinterpret_cast<const float4 *>(sEnd + jc + j);
+                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
+                        en[j] = e4.x; en[j + 1] = e4.y; en[j + 2] = e4.z; en[j + 3] = e4.w;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int tk = jc + j;
-                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(sGam[tk], xq[j], pu[j]) * scale;
-                        u[j] *= sEnd[tk];
+                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(gm[j], xq[j], pu[j]) * scale;
+                        u[j] *= en[j];
                     }
                     ptx::store_split8(sRhi, sRlo, v, jc, u);
                     ptx::store_split8(sRhi, sRlo, v, jc + 8, u + 8);
