@@ -629,7 +629,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 // and chunk-local: [K;Q] K^T (M = 128) and P T (A = [P hi; P lo], B = T).
 namespace d128 {
 
-constexpr int D = 128;
 constexpr int NS = 256;                 // threads per stream
 constexpr int NTH = 2 * NS;             // state stream (warps 0-7) + transform stream (8-15)
 constexpr int BAR_S = 1, BAR_Z = 2;     // hardware barrier of each stream
@@ -742,6 +741,7 @@ __device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const 
     ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, w);
 }
 
+template <int D>
 __global__ void __launch_bounds__(NTH, 1)
 chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -760,6 +760,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint8_t *sRhi = sm + OFF_RT, *sRlo = sm + OFF_RT + 16384;
     uint8_t *sV = sm + OFF_V;
 
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    constexpr int NSLAB = D / 64;            // 64-key slabs of [K;Q] and 64-value boxes of V
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const bool zstream = tid >= NS;          // transform stream
@@ -811,17 +813,17 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
     auto issue_qk = [&](int c) {
         const int st = c & 1;
         uint8_t *qk = sm + OFF_QK + st * 32768;
-        ptx::mbar_arrive_expect_tx(&sh.qk_full[st], 4 * 8192);
+        ptx::mbar_arrive_expect_tx(&sh.qk_full[st], NSLAB * 2 * 8192);
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < NSLAB; ++s) {
             ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.qk_full[st], s * 64, h, c * C, b);
             ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.qk_full[st], s * 64, h, c * C, b);
         }
     };
     auto issue_v = [&](int c) {
-        ptx::mbar_arrive_expect_tx(&sh.v_full, 2 * 8192);
+        ptx::mbar_arrive_expect_tx(&sh.v_full, NSLAB * 8192);
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < NSLAB; ++s)
             ptx::tma_load_4d(sV + s * 8192, &tm_v, &sh.v_full, s * 64, h, c * C, b);
     };
     if (tid == 0) {
@@ -832,6 +834,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 
     if (zstream) {
         // ================= transform stream: Z = [T; P T] of every chunk
+        GateRegs gr{0.f, 0.f, 0.f};          // gates of the chunk about to start
+        if (t < 64) load_gates(gr, g, beta, b, h, T, H, 0, t);
         for (int c = 0; c < n_chunks; ++c) {
             const int st = c & 1;
             const uint32_t aQK = ptx::smem_u32(sm + OFF_QK + st * 32768);
@@ -840,9 +844,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             uint8_t *sZhi = sm + OFF_Z + st * 32768, *sZlo = sZhi + 16384;
 
             if (t < 64) {
-                GateRegs gr;
-                load_gates(gr, g, beta, b, h, T, H, c, t);
                 scan_gates(gr, gs, t);
+                if (c + 1 < n_chunks) load_gates(gr, g, beta, b, h, T, H, c + 1, t);
             }
             wait(&sh.qk_full[st], (uint32_t)((c >> 1) & 1));
             ptx::named_sync(BAR_Z, NS);
@@ -854,7 +857,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     ptx::tc_fence_after();
                     constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
+                    for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t da =
                             ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                         ptx::mma_bf16(tmem + C_KQ, da, da, idesc, kk > 0);
@@ -967,11 +970,12 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         // initial state: thread (value row, key half) -> TMEM, pre-scaled by
         // the first chunk's gamma_C for the in-place accumulation
         wait(&sh.g_ready[0], 0);
-        {
+        const bool vrow = row < D;               // this lane is a value row of the state
+        if (vrow) {
             const float gC = gsets[128 + 63];
 #pragma unroll 1
-            for (int kg = 0; kg < 64; kg += 32) {
-                const int key0 = wg * 64 + kg;
+            for (int kg = 0; kg < D / 2; kg += 32) {
+                const int key0 = wg * (D / 2) + kg;
                 float x[32];
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
@@ -1008,7 +1012,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
+                    for (int kk = 0; kk < D / 16; ++kk)
                         ptx::mma_bf16_ts(tmem + C_X, tmem + (part ? C_SLO : C_SHI) + kk * 8,
                                          ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32,
                                                         16, 1024),
@@ -1021,7 +1025,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 
             // R^T = beta V^T - beta gamma (K S^T)^T  (value row v, tokens of this half)
             wait(&sh.v_full, (uint32_t)(c & 1));
-            {
+            if (vrow) {
                 const int v = row;
                 const uint8_t *vbox = sV + (v >> 6) * 8192;
 #pragma unroll 1
@@ -1078,7 +1082,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::tc_fence_after();
 
             // O (global) and U~^T hi / lo
-            {
+            if (vrow) {
                 const int v = row;
                 float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
 #pragma unroll 1
@@ -1113,7 +1117,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             // S += U~^T K  (M = 128 values, N = 128 keys, K = 64 tokens)
             if (t == 0 && !*abort_flag) {
                 ptx::tc_fence_after();
-                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, true);
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, D, false, true);
                 const uint32_t aU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
@@ -1137,8 +1141,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 gC = gsets[((c + 1) & 3) * 256 + 128 + 63];
             }
 #pragma unroll 1
-            for (int kg = 0; kg < 64; kg += 32) {
-                const int key0 = wg * 64 + kg;
+            for (int kg = 0; kg < (vrow ? D / 2 : 0); kg += 32) {
+                const int key0 = wg * (D / 2) + kg;
                 float x[32];
                 ptx::tmem_ld16(tl + C_SACC + key0, *reinterpret_cast<float(*)[16]>(x));
                 ptx::tmem_ld16(tl + C_SACC + key0 + 16, *reinterpret_cast<float(*)[16]>(x + 16));
@@ -1153,7 +1157,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     put_state32(tl, key0, x, gC);
                 }
             }
-            if (!last) ptx::tmem_st_wait();
+            if (!last && vrow) ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
         }
@@ -1227,20 +1231,21 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_d128(const Problem &p, cudaStream_t stream) {
+template <int D>
+cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, p.B, p.T, p.H, 128, 64, true) ||
-        !make_map(&mk, p.k, p.B, p.T, p.H, 128, 64, true) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, 128, 64, true))
+    if (!make_map(&mq, p.q, p.B, p.T, p.H, D, 64, true) ||
+        !make_map(&mk, p.k, p.B, p.T, p.H, D, 64, true) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true))
         return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(d128::chunked_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        d128::SMEM);
+        attr_err = cudaFuncSetAttribute(d128::chunked_d128_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, d128::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    d128::chunked_d128_kernel<<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
+    d128::chunked_d128_kernel<D><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
         mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
     return cudaGetLastError();
 }
@@ -1254,8 +1259,8 @@ size_t chunked_workspace_bytes(int, int, int, int, int) { return 0; }
 cudaError_t launch_chunked(const Problem &p, void *, size_t, cudaStream_t stream) {
     if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
     switch (p.d) {
-        case 64: return launch_d<64>(p, stream);
-        case 128: return launch_d128(p, stream);
+        case 64: return launch_ws<64>(p, stream);
+        case 128: return launch_ws<128>(p, stream);
         case 256: return launch_d<256>(p, stream);
         default: return cudaErrorInvalidValue;
     }
