@@ -41,6 +41,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
                   "sm_max_mhz": 2070.0}
 N_SMS = 152
 L2_FLUSH_BYTES = 512 << 20
+# DRAM bytes per launch measured with ncu, keyed by workload; an entry only
+# counts while the kernel sources it was measured on are unchanged.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
 # ----------------------------------------------------------------- helpers
@@ -55,6 +58,34 @@ def load_peaks():
     p = dict(FALLBACK_PEAKS)
     p["source"] = "fallback"
     return p
+
+
+def sources_sha(rel_paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in rel_paths.split("+"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def load_traffic():
+    """{workload: dram bytes per launch} for entries whose sources still match."""
+    out = {}
+    if not os.path.exists(TRAFFIC_FILE):
+        return out
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            parts = line.split()
+            if not parts or parts[0].startswith("#") or len(parts) < 4:
+                continue
+            workload, srcs, sha, nbytes = parts[:4]
+            try:
+                if sources_sha(srcs) == sha:
+                    out[workload] = float(nbytes)
+            except OSError:
+                continue
+    return out
 
 
 def alu_fp32_tflops(peaks):
@@ -251,7 +282,7 @@ def run_decode24(torch, gdn, W, dev, timer, args, dist, peaks):
     launch_s = ms / 1e3 / L
     achieved = bytes_launch / launch_s / 1e9
     roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-            "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+            "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic().get(w.name),
             "kernel": "recurrent_kernel<128,8,1,bf16>",
             "bytes_per_launch": bytes_launch,
             "note": "per-launch time = graph step time / 24 (includes inter-kernel gaps); "
@@ -316,7 +347,8 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
         res.update({"metric": "decode us/step", "value": ms * 1e3, "unit": "us/step",
                     "roofline": {"bound": "hbm", "achieved": achieved,
                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                 "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                                 "frac": achieved / peaks["hbm_gbs"],
+                                 "traffic": load_traffic().get(w.name),
                                  "bytes_per_launch": bytes_launch}})
     else:
         toks = B * T
@@ -328,7 +360,8 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
             ach = fl / (ms / 1e3) / 1e12
             peak = peaks["bf16_tflops"]
             res["roofline"] = {"bound": "tensor", "achieved": ach, "peak": peak,
-                               "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                               "unit": "TFLOP/s", "frac": ach / peak,
+                               "traffic": load_traffic().get(w.name),
                                "flops_per_launch": fl,
                                "hbm_achieved_gbs": hbm_ach,
                                "hbm_frac": hbm_ach / peaks["hbm_gbs"]}

@@ -1081,31 +1081,21 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             mma_phase ^= 1;
             ptx::tc_fence_after();
 
-            // O (global) and U~^T hi / lo
+            // U~^T hi / lo first: it is all the state update needs
             if (vrow) {
                 const int v = row;
-                float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
 #pragma unroll 1
                 for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                    float xq[16], pu[16], u[16];
-                    ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
-                    ptx::tmem_ld16(tl + C_PU + jc, pu);
+                    float u[16], en[16];
                     ptx::tmem_ld16(tl + C_X + jc, u);
-                    ptx::tmem_ld_wait();
-                    float gm[16], en[16];
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
                         const float4 e4 = *reinterpret_cast<const float4 *>(sEnd + jc + j);
-                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
                         en[j] = e4.x; en[j + 1] = e4.y; en[j + 2] = e4.z; en[j + 3] = e4.w;
                     }
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int tk = jc + j;
-                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(gm[j], xq[j], pu[j]) * scale;
-                        u[j] *= en[j];
-                    }
+                    for (int j = 0; j < 16; ++j) u[j] *= en[j];
                     ptx::store_split8(sRhi, sRlo, v, jc, u);
                     ptx::store_split8(sRhi, sRlo, v, jc + 8, u + 8);
                 }
@@ -1114,7 +1104,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
 
-            // S += U~^T K  (M = 128 values, N = 128 keys, K = 64 tokens)
+            // S += U~^T K  (M = 128 values, N = D keys, K = 64 tokens)
             if (t == 0 && !*abort_flag) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, D, false, true);
@@ -1126,6 +1116,30 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                         ptx::mma_bf16(tmem + C_SACC, ptx::smem_desc(aU[part] + kk * 32, 16, 1024),
                                       ptx::smem_desc(aQK + kk * 2048, 16384, 1024), idesc, true);
                 ptx::mma_commit(&sh.mma_s);
+            }
+
+            // O = (gamma Q S^T + P U) / sqrt(d) to global while the update runs
+            // (X^T Q part and (P U)^T are not touched by it)
+            if (vrow) {
+                const int v = row;
+                float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float xq[16], pu[16], gm[16];
+                    ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
+                    ptx::tmem_ld16(tl + C_PU + jc, pu);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
+                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
+                    }
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int tk = jc + j;
+                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(gm[j], xq[j], pu[j]) * scale;
+                    }
+                }
             }
             wait(&sh.mma_s, mma_phase);
             mma_phase ^= 1;
