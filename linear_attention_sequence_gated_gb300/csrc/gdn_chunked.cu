@@ -70,9 +70,9 @@ struct Cfg {
     static constexpr int OFF_A = OFF_UN;
     static constexpr int OFF_P = OFF_A + SZ_F;
     static constexpr int OFF_T = OFF_P + SZ_F;
-    static constexpr int OFF_W = OFF_T + SZ_F;             // 3 x 16x16 fp32
+    static constexpr int OFF_W = OFF_T + SZ_F;             // 16 x 96 fp32
     static constexpr int OFF_RU = OFF_UN;                  // R (then U~) hi, lo: 64 rows x 128 B
-    static constexpr int UN_BYTES = 3 * SZ_F + 3 * 256 * 4;
+    static constexpr int UN_BYTES = 3 * SZ_F + 16 * 96 * 4;
     static constexpr int OFF_MISC = OFF_UN + UN_BYTES;     // G, beta, gamma, end-decay
     static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;  // + alignment slack
     // TMEM columns
@@ -119,25 +119,28 @@ __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile
     }
 }
 
-// One block row BI (1..3) of T = (I + A)^-1 (16x16 blocks, row stride FST),
-// computed in place over A:
-//   W = A[BI, :BI] T[:BI, :BI],  T[BI, j] = -T[BI, BI] W[:, j]   (j < BI)
-// Rows above block row BI already hold T; row block BI still holds A left of
-// its diagonal block; entries above the diagonal are zero in both.  Thread
-// (r, q) = (t / (4 BI), t % (4 BI)) for t < 64 BI owns row r and the four
-// columns 4q .. 4q+3 of the row block, so each 128-bit load feeds four FMAs.
-// `bar` is a hardware barrier shared by exactly 256 threads (t = 0..255).
+// T = (I + A)^-1 for a strictly lower triangular 64x64 A stored in full
+// (zeros on and above the diagonal, row stride FST), in place, on 256
+// threads t = 0..255 sharing hardware barrier `bar`, with 16x16 blocks:
+//   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks (column substitution)
+//   2. X_i = T_ii A[i, :i] for i = 1..3, all at once (into W, 16 x 96 fp32)
+//   3. T[i, :i] = -X_i T[:i, :i] for i = 1, 2, 3 in turn
+// which is block forward substitution: (I + A)_ii T_ij + sum_k A_ik T_kj = 0.
+// Each thread of steps 2 and 3 owns one row and four consecutive columns, so
+// every 128-bit shared-memory load feeds four FMAs.  The result is T in full
+// (zeros above the diagonal); entered and left with the matrix visible to all.
 template <int BI>
-__device__ __forceinline__ void ut_block_row(float *sAT, float *sW, int t, int bar) {
-    constexpr int NQ = 4 * BI;               // column quads per row
-    const bool act = t < 16 * NQ;
-    const int r = t / NQ, q = t % NQ;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (act) {
-        const float *arow = sAT + (BI * 16 + r) * FST;
+__device__ __forceinline__ void ut_solve_row(float *sAT, const float *sW, int t) {
+    // T[BI, :BI] = -X_BI T[:BI, :BI]; X_BI lives at W columns 16 (BI-1) BI / 2 ...
+    constexpr int NQ = 4 * BI;
+    constexpr int XOFF = 8 * (BI - 1) * BI;          // 0, 16, 48: start column of X_BI in W
+    if (t < 16 * NQ) {
+        const int r = t / NQ, q = t % NQ;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *xrow = sW + r * 96 + XOFF;
 #pragma unroll 4
         for (int k4 = 0; k4 < BI * 16; k4 += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(arow + k4);
+            const float4 a = *reinterpret_cast<const float4 *>(xrow + k4);
             const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -148,37 +151,13 @@ __device__ __forceinline__ void ut_block_row(float *sAT, float *sW, int t, int b
                 acc.w = fmaf(av[e], tq.w, acc.w);
             }
         }
-        *reinterpret_cast<float4 *>(sW + r * 48 + 4 * q) = acc;
-    }
-    ptx::named_sync(bar, 256);
-    if (act) {
-        acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float *trow = sAT + (BI * 16 + r) * FST + BI * 16;   // diagonal block, zero above
-#pragma unroll
-        for (int m4 = 0; m4 < 16; m4 += 4) {
-            const float4 tv = *reinterpret_cast<const float4 *>(trow + m4);
-            const float tvv[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 w = *reinterpret_cast<const float4 *>(sW + (m4 + e) * 48 + 4 * q);
-                acc.x = fmaf(tvv[e], w.x, acc.x);
-                acc.y = fmaf(tvv[e], w.y, acc.y);
-                acc.z = fmaf(tvv[e], w.z, acc.z);
-                acc.w = fmaf(tvv[e], w.w, acc.w);
-            }
-        }
         *reinterpret_cast<float4 *>(sAT + (BI * 16 + r) * FST + 4 * q) =
             make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
-    ptx::named_sync(bar, 256);
 }
 
-// T = (I + A)^-1 in place, for a strictly lower triangular 64x64 A stored in
-// full (zeros on and above the diagonal, row stride FST), on 256 threads
-// (t = 0..255): the four diagonal 16x16 blocks by column substitution, then
-// the three block rows below them.  The result is T in full, zeros above the
-// diagonal.  Entered and left with the matrix visible to all participants.
 __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int bar) {
+    // 1. diagonal blocks
     float x[16];
     const int blk = t >> 4, j = t & 15;
     if (t < 64) {
@@ -206,9 +185,38 @@ __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int b
         for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
     }
     ptx::named_sync(bar, 256);
-    ut_block_row<1>(sAT, sW, t, bar);
-    ut_block_row<2>(sAT, sW, t, bar);
-    ut_block_row<3>(sAT, sW, t, bar);
+    // 2. X_i = T_ii A[i, :i]: 16 rows x 96 columns (X_1 | X_2 | X_3), thread
+    //    (r, q) -> row r, columns 4q .. 4q+3 for q < 24 (384 items, 256 threads)
+    for (int it = t; it < 16 * 24; it += 256) {
+        const int r = it / 24, q = it % 24;
+        const int bi = q < 4 ? 1 : (q < 12 ? 2 : 3);        // X_bi holds columns [16(bi-1)bi/2, ...)
+        const int col = 4 * q - 8 * (bi - 1) * bi;          // column within A[bi, :bi]
+        const float *trow = sAT + (bi * 16 + r) * FST + bi * 16;   // T_ii row r (zero above)
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m4 = 0; m4 < 16; m4 += 4) {
+            const float4 tv = *reinterpret_cast<const float4 *>(trow + m4);
+            const float tvv[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 a = *reinterpret_cast<const float4 *>(
+                    sAT + (bi * 16 + m4 + e) * FST + col);
+                acc.x = fmaf(tvv[e], a.x, acc.x);
+                acc.y = fmaf(tvv[e], a.y, acc.y);
+                acc.z = fmaf(tvv[e], a.z, acc.z);
+                acc.w = fmaf(tvv[e], a.w, acc.w);
+            }
+        }
+        *reinterpret_cast<float4 *>(sW + r * 96 + 4 * q) = acc;
+    }
+    ptx::named_sync(bar, 256);
+    // 3. block rows in turn (each needs the rows above it)
+    ut_solve_row<1>(sAT, sW, t);
+    ptx::named_sync(bar, 256);
+    ut_solve_row<2>(sAT, sW, t);
+    ptx::named_sync(bar, 256);
+    ut_solve_row<3>(sAT, sW, t);
+    ptx::named_sync(bar, 256);
 }
 
 template <int D>
@@ -638,11 +646,11 @@ constexpr int OFF_V = 65536;            // V of one chunk (2 boxes x 64 rows x 1
 constexpr int OFF_Z = 81920;            // 2 buffers x {Z hi, Z lo} (128 rows x 128 B each)
 constexpr int OFF_PP = 147456;          // P hi (rows 0-63) | P lo (rows 64-127)
 constexpr int OFF_AT = 163840;          // A, then T in place: fp32 64 x FST
-constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 48 fp32
-constexpr int OFF_RT = 184320;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
+constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 96 fp32
+constexpr int OFF_RT = 187392;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
 constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-decay}
 constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
-static_assert(OFF_W + 16 * 48 * 4 <= OFF_RT, "scratch overlaps R^T");
+static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT, "scratch overlaps R^T");
 static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
 static_assert(SMEM <= 232448, "shared memory");
 // TMEM columns
