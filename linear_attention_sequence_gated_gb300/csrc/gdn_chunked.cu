@@ -65,14 +65,13 @@ struct Cfg {
     static constexpr int OFF_V = OFF_QK + NSLAB * 16384;   // V block, 64 rows
     static constexpr int OFF_Z = OFF_V + 8192;             // Z hi, Z lo: 128 rows x 128 B each
     static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
-    static constexpr int OFF_UN = OFF_S + 2 * D * 128;     // union: {A, P, T, W} | {R/U~ hi, lo}
+    static constexpr int OFF_UN = OFF_S + 2 * D * 128;     // union: {A then T, P, W} | {R/U~ hi, lo}
     static constexpr int SZ_F = 64 * FST * 4;
     static constexpr int OFF_A = OFF_UN;
     static constexpr int OFF_P = OFF_A + SZ_F;
-    static constexpr int OFF_T = OFF_P + SZ_F;
-    static constexpr int OFF_W = OFF_T + SZ_F;             // 16 x 96 fp32
+    static constexpr int OFF_W = OFF_P + SZ_F;             // 16 x 96 fp32
     static constexpr int OFF_RU = OFF_UN;                  // R (then U~) hi, lo: 64 rows x 128 B
-    static constexpr int UN_BYTES = 3 * SZ_F + 16 * 96 * 4;
+    static constexpr int UN_BYTES = 2 * SZ_F + 16 * 96 * 4;
     static constexpr int OFF_MISC = OFF_UN + UN_BYTES;     // G, beta, gamma, end-decay
     static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;  // + alignment slack
     // TMEM columns
@@ -82,7 +81,7 @@ struct Cfg {
     static constexpr int COL_DS = 64 + 2 * BV;
     static constexpr int TMEM_COLS = 256;
     static_assert(COL_DS + KT * BV <= TMEM_COLS, "TMEM columns");
-    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(SMEM + 64 <= 232448, "shared memory (dynamic + static)");
 };
 
 struct Bars {
@@ -652,7 +651,7 @@ constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-de
 constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
 static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT, "scratch overlaps R^T");
 static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
-static_assert(SMEM <= 232448, "shared memory");
+static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
 // TMEM columns
 constexpr uint32_t C_SACC = 0;    // S (fp32): lane = value, column = key
 constexpr uint32_t C_SHI = 128;   // S hi, bf16 pairs (keys 2c, 2c+1 in column c)
