@@ -752,7 +752,8 @@ template <int D>
 __global__ void __launch_bounds__(NTH, 1)
 chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *state_in, float *state_out,
                     float *__restrict__ out, int T, int H, float scale, int *status)
 {
@@ -798,6 +799,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         ptx::prefetch_tmap(&tm_q);
         ptx::prefetch_tmap(&tm_k);
         ptx::prefetch_tmap(&tm_v);
+        ptx::prefetch_tmap(&tm_o);
     }
     if (warp == 0) {
         ptx::tmem_alloc(&sh.tmem_base, 512);
@@ -1125,11 +1127,16 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 ptx::mma_commit(&sh.mma_s);
             }
 
-            // O = (gamma Q S^T + P U) / sqrt(d) to global while the update runs
-            // (X^T Q part and (P U)^T are not touched by it)
+            wait(&sh.mma_s, mma_phase);
+            mma_phase ^= 1;
+            ptx::tc_fence_after();
+
+            // O = (gamma Q S^T + P U) / sqrt(d): staged as a [token][value] fp32
+            // tile in the R^T buffer (free now), written by one TMA store that
+            // clips tokens past T
             if (vrow) {
                 const int v = row;
-                float *ocol = out + ((size_t)b * T + t0) * tok_stride + (size_t)h * D + v;
+                float *ot = reinterpret_cast<float *>(sRhi);
 #pragma unroll 1
                 for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
                     float xq[16], pu[16], gm[16];
@@ -1142,15 +1149,15 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int tk = jc + j;
-                        if (tk < n) ocol[(size_t)tk * tok_stride] = fmaf(gm[j], xq[j], pu[j]) * scale;
-                    }
+                    for (int j = 0; j < 16; ++j) ot[(jc + j) * D + v] = fmaf(gm[j], xq[j], pu[j]) * scale;
                 }
             }
-            wait(&sh.mma_s, mma_phase);
-            mma_phase ^= 1;
-            ptx::tc_fence_after();
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(BAR_S, NS);
+            if (t == 0 && !*abort_flag) {
+                ptx::tma_store_4d(&tm_o, sRhi, 0, h, t0, b);
+                ptx::bulk_commit_group();
+            }
             // this stage is free: bring chunk c + 2 into it
             if (t == 0 && c + 2 < n_chunks && !*abort_flag) issue_qk(c + 2);
 
@@ -1179,9 +1186,11 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             if (!last && vrow) ptx::tmem_st_wait();
+            if (t == 0) ptx::bulk_wait_read_all();   // the O tile has left the R^T buffer
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
         }
+        if (t == 0) ptx::bulk_wait_all();
     }
 
     ptx::tc_fence_before();
@@ -1230,6 +1239,23 @@ bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, in
            CUDA_SUCCESS;
 }
 
+// 4-D map over the (B, T, H, d) fp32 output; box = {d, 1 head, 64 tokens,
+// 1 sequence}, unswizzled: a [token][value] tile of one chunk.  Tokens past
+// T are clipped by the store.
+bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4,
+                                   (cuuint64_t)T * H * d * 4};
+    const cuuint32_t box[4] = {(cuuint32_t)d, 1, (cuuint32_t)C, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
 template <int D>
 cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     using CF = Cfg<D>;
@@ -1254,10 +1280,11 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
 
 template <int D>
 cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, p.q, p.B, p.T, p.H, D, 64, true) ||
         !make_map(&mk, p.k, p.B, p.T, p.H, D, 64, true) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true))
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true) ||
+        !make_map_out(&mo, p.out, p.B, p.T, p.H, D))
         return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1267,7 +1294,7 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     d128::chunked_d128_kernel<D><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
-        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
+        mq, mk, mv, mo, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
     return cudaGetLastError();
 }
 
