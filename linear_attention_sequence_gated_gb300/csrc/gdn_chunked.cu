@@ -656,8 +656,11 @@ static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
 constexpr uint32_t C_SACC = 0;    // S (fp32): lane = value, column = key
 constexpr uint32_t C_SHI = 128;   // S hi, bf16 pairs (keys 2c, 2c+1 in column c)
 constexpr uint32_t C_SLO = 192;   // S lo
-constexpr uint32_t C_X = 256;     // X^T: columns 0-63 K part (then U^T), 64-127 Q part
-constexpr uint32_t C_PU = 384;    // (P U)^T
+constexpr uint32_t C_Y = 256;     // [U^T | (P U)^T] (128 columns, one MMA); PU half = K part of X
+constexpr uint32_t C_U = 256;     //   U^T
+constexpr uint32_t C_PU = 320;    //   (P U)^T
+constexpr uint32_t C_X = 320;     // X^T: columns 0-63 K part (consumed before C_PU is written),
+                                  //      64-127 Q part (columns 384-447)
 constexpr uint32_t C_KQ = 448;    // [K;Q] K^T, then P T (lanes 0-63): transform stream only
 
 struct Shared {
@@ -1066,23 +1069,20 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::named_sync(BAR_S, NS);
             if (t == 0 && !last && !*abort_flag) issue_v(c + 1);   // V of this chunk consumed
 
-            // U^T = R^T T^T (into the K part of X), (P U)^T = R^T (P T)^T
+            // [U^T | (P U)^T] = R^T Z^T with Z = [T; P T]: one N = 128 product
             wait(&sh.z_ready[st], (uint32_t)((c >> 1) & 1));
             if (t == 0 && !*abort_flag) {
                 ptx::tc_fence_after();
-                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
                 const uint32_t aR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
                 const uint32_t bZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
 #pragma unroll
-                for (int half = 0; half < 2; ++half)
+                for (int part = 0; part < 3; ++part)
 #pragma unroll
-                    for (int part = 0; part < 3; ++part)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            ptx::mma_bf16(tmem + (half ? C_PU : C_X),
-                                          ptx::smem_desc(aR[part] + kk * 32, 16, 1024),
-                                          ptx::smem_desc(bZ[part] + half * 8192 + kk * 32, 16, 1024),
-                                          idesc, part > 0 || kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(tmem + C_Y, ptx::smem_desc(aR[part] + kk * 32, 16, 1024),
+                                      ptx::smem_desc(bZ[part] + kk * 32, 16, 1024), idesc,
+                                      part > 0 || kk > 0);
                 ptx::mma_commit(&sh.mma_s);
                 ptx::mma_commit(&sh.z_free[st]);
             }
@@ -1096,7 +1096,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll 1
                 for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
                     float u[16], en[16];
-                    ptx::tmem_ld16(tl + C_X + jc, u);
+                    ptx::tmem_ld16(tl + C_U + jc, u);
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         const float4 e4 = *reinterpret_cast<const float4 *>(sEnd + jc + j);
