@@ -643,12 +643,14 @@ constexpr int BAR_S = 1, BAR_Z = 2;     // hardware barrier of each stream
 constexpr int OFF_QK = 0;               // 2 stages x [K;Q] (2 slabs x 128 rows x 128 B)
 constexpr int OFF_V = 65536;            // V of one chunk (2 boxes x 64 rows x 128 B)
 constexpr int OFF_Z = 81920;            // 2 buffers x {Z hi, Z lo} (128 rows x 128 B each)
-constexpr int OFF_A = 147456;           // A: fp32 64 x FST
-constexpr int OFF_RT = 164864;          // R^T (then U~^T, then the O tile) hi | lo: 2 x 16 KB
-constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G2, beta, gamma, end-decay}
+constexpr int OFF_PP = 147456;          // P hi (rows 0-63) | P lo (rows 64-127)
+constexpr int OFF_AT = 163840;          // A, then T in place: fp32 64 x FST
+constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 96 fp32
+constexpr int OFF_RT = 187392;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
+constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-decay}
 constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
-static_assert(OFF_A + 64 * FST * 4 <= OFF_RT, "A overlaps R^T");
-static_assert(OFF_RT % 1024 == 0, "R^T tiles must be 1024-byte aligned");
+static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT, "scratch overlaps R^T");
+static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
 static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
 // TMEM columns
 constexpr uint32_t C_SACC = 0;    // S (fp32): lane = value, column = key
@@ -722,29 +724,6 @@ __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) 
     gs[192 + t] = ex2((tot - G) * LOG2E);
 }
 
-// One row z of Z = [I; P] (I + A)^-1, i.e. a row of T or of P T: solves
-// z (I + A) = m by substitution from the right, in registers.  On entry w
-// holds m (a unit row for T, a row of P for P T); A (strictly lower, row
-// stride FST) is read from shared memory a row at a time (the same address
-// in every lane: broadcast).  Rows whose m vanishes beyond column IMAX stay
-// zero there, so only i <= IMAX is walked.
-template <int IMAX>
-__device__ __forceinline__ void z_row_solve(float (&w)[64], const float *sA) {
-#pragma unroll
-    for (int i = IMAX; i > 0; --i) {
-        const float wi = w[i];                    // final: every larger i is applied
-        const float *arow = sA + i * FST;
-#pragma unroll
-        for (int j4 = 0; j4 < i; j4 += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(arow + j4);
-            w[j4] = fmaf(-wi, a.x, w[j4]);
-            if (j4 + 1 < i) w[j4 + 1] = fmaf(-wi, a.y, w[j4 + 1]);
-            if (j4 + 2 < i) w[j4 + 2] = fmaf(-wi, a.z, w[j4 + 2]);
-            if (j4 + 3 < i) w[j4 + 3] = fmaf(-wi, a.w, w[j4 + 3]);
-        }
-    }
-}
-
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
 // columns, gamma * S -> 32 fp32 columns.
 __device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const float (&x)[32],
@@ -785,8 +764,10 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     __shared__ Shared sh;
-    float *sAT = reinterpret_cast<float *>(sm + OFF_A);
+    float *sAT = reinterpret_cast<float *>(sm + OFF_AT);
+    float *sW = reinterpret_cast<float *>(sm + OFF_W);
     float *gsets = reinterpret_cast<float *>(sm + OFF_G);
+    uint8_t *sPhi = sm + OFF_PP, *sPlo = sm + OFF_PP + 8192;
     uint8_t *sRhi = sm + OFF_RT, *sRlo = sm + OFF_RT + 16384;
     uint8_t *sV = sm + OFF_V;
 
@@ -802,6 +783,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh - b * H;
     const int n_chunks = (T + C - 1) / C;
+    const size_t tok_stride = (size_t)H * D;
     const size_t st_base = (size_t)bh * D * D;
 
     if (tid == 0) {
@@ -899,17 +881,13 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             mma_phase ^= 1;
             ptx::tc_fence_after();
 
-            // Rows of [K;Q] K^T -> rows of A (TMEM lanes 0-63, to shared fp32) and
-            // of P (lanes 64-127, kept in registers).  The owner of lane m
-            // (m < 64: half 0, m >= 64: half 1) later solves row m of Z.
-            const bool owner = (row < 64) == (wg == 0);
-            const int r = row & 63;
-            float w[64];
-            if (owner) {
+            // A (rows 0-63) as fp32; P (rows 64-127) as hi / lo rows
+            {
+                const int r = row & 63;
                 const float Gr = sG[r];
                 const float br = sBeta[r];
-#pragma unroll
-                for (int jc = 0; jc < 64; jc += 16) {
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
                     float kq[16];
                     ptx::tmem_ld16(tl + C_KQ + jc, kq);
                     ptx::tmem_ld_wait();
@@ -931,34 +909,71 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                         for (int j = 0; j < 16; j += 4)
                             *reinterpret_cast<float4 *>(sAT + r * FST + jc + j) =
                                 make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) w[jc + j] = (jc + j == r) ? 1.f : 0.f;
                     } else {
+                        float p[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int i = jc + j;
-                            w[jc + j] = (i <= r) ? ex2(Gr - gi[j]) * kq[j] : 0.f;
+                            p[j] = (i <= r) ? ex2(Gr - gi[j]) * kq[j] : 0.f;
                         }
+                        ptx::store_split8(sPhi, sPlo, r, jc, p);
+                        ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
                     }
                 }
             }
+            ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::named_sync(BAR_Z, NS);
 
-            // Z rows: T = (I + A)^-1 and P T, one row per owner thread
-            if (owner) {
-                if (r < 32) z_row_solve<31>(w, sAT);
-                else z_row_solve<63>(w, sAT);
-            }
-            // into this chunk's Z buffer, once the state stream has finished
-            // with the chunk that used it before
+            // T = (I + A)^-1 in place
+            ut_transform(sAT, sW, t, BAR_Z);
+
+            // T as hi / lo into rows 0-63 of this chunk's Z buffer, once the
+            // state stream has finished with the chunk that used it before
             if (c >= 2) wait(&sh.z_free[st], (uint32_t)(((c - 2) >> 1) & 1));
-            if (owner) {
-                const int zr = (row < 64) ? r : 64 + r;
+            {
+                const int r = t >> 2, c0 = (t & 3) * 16;
+                float tv[16];
 #pragma unroll
-                for (int j = 0; j < 64; j += 8) ptx::store_split8(sZhi, sZlo, zr, j, w + j);
+                for (int e = 0; e < 16; ++e) tv[e] = sAT[r * FST + c0 + e];
+                ptx::store_split8(sZhi, sZlo, r, c0, tv);
+                ptx::store_split8(sZhi, sZlo, r, c0 + 8, tv + 8);
             }
             ptx::fence_proxy_async_smem();
+            ptx::named_sync(BAR_Z, NS);
+
+            // P T  (A = [P hi; P lo] 128 rows, B = T rows (MN-major), N = 64, K = 64)
+            if (t == 0 && !*abort_flag) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, true);
+                const uint32_t aP[3] = {ptx::smem_u32(sPhi), ptx::smem_u32(sPhi), ptx::smem_u32(sPlo)};
+                const uint32_t bT[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
+#pragma unroll
+                for (int part = 0; part < 3; ++part)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        ptx::mma_bf16(tmem + C_KQ, ptx::smem_desc(aP[part] + kk * 32, 16, 1024),
+                                      ptx::smem_desc(bT[part] + kk * 2048, 8192, 1024), idesc,
+                                      part > 0 || kk > 0);
+                ptx::mma_commit(&sh.mma_z);
+            }
+            wait(&sh.mma_z, mma_phase);
+            mma_phase ^= 1;
+            ptx::tc_fence_after();
+
+            // P T rows -> Z rows 64-127 (TMEM lanes 0-63)
+            if ((warp & 3) < 2) {
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float pt[16];
+                    ptx::tmem_ld16(tl + C_KQ + jc, pt);
+                    ptx::tmem_ld_wait();
+                    ptx::store_split8(sZhi, sZlo, 64 + row, jc, pt);
+                    ptx::store_split8(sZhi, sZlo, 64 + row, jc + 8, pt + 8);
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
             ptx::named_sync(BAR_Z, NS);
             if (t == 0) ptx::mbar_arrive(&sh.z_ready[st]);
         }
