@@ -622,18 +622,27 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 }
 
 // ---------------------------------------------------------------------------
-// head_dim 128: one CTA per (sequence, head) owns all 128 value rows, so the
-// chunk-local UT transform is built once per chunk and head.  The state is
-// held transposed with respect to chunked_kernel: TMEM lanes are value rows
-// and columns are keys, so it accumulates in place (S += U~^T K) and its
+// head_dim 64 and 128: one CTA per (sequence, head) owns every value row, so
+// the chunk-local UT transform is built once per chunk and head.  The state
+// is held transposed with respect to chunked_kernel: TMEM lanes are value
+// rows and columns are keys, so it accumulates in place (S += U~^T K) and its
 // bf16 hi / lo split feeds the next chunk's MMA straight from TMEM (A
-// operand).  Per chunk (M = 128 value rows in every state product):
-//   X^T  = S [K;Q]^T            (A = S hi / lo in TMEM, B = [K;Q] from TMA)
-//   R^T  = beta V^T - beta gamma (K S^T)^T                  (CUDA cores)
-//   U^T  = R^T T^T,  (P U)^T = R^T (P T)^T       (B = rows of Z = [T; P T])
-//   O    = (gamma Q S^T + P U) / sqrt(d)                     (CUDA cores)
-//   S   += (diag(exp(G_C - G)) U)^T K   (S pre-scaled by gamma_C; B = K MN-major)
-// and chunk-local: [K;Q] K^T (M = 128) and P T (A = [P hi; P lo], B = T).
+// operand).  Two warp-specialised streams share the CTA:
+//   transform stream (warps 8-15), chunk c, one chunk ahead of the other:
+//     [K;Q] K^T (M = 128) -> A (fp32), P (hi / lo) -> T = (I + A)^-1 in
+//     place -> T (hi / lo) into Z rows 0-63 -> P T (A = [P hi; P lo],
+//     B = T, MN-major) -> P T (hi / lo) into Z rows 64-127
+//   state stream (warps 0-7), chunk c (M = 128 value rows in every product):
+//     X^T  = S [K;Q]^T             (A = S hi / lo in TMEM, B = [K;Q] from TMA)
+//     R^T  = beta V^T - beta gamma (K S^T)^T                   (CUDA cores)
+//     [U^T | (P U)^T] = R^T Z^T    (one N = 128 product, B = Z rows)
+//     S   += (diag(exp(G_C - G)) U)^T K   (S pre-scaled by gamma_C; B = K MN-major)
+//     O    = (gamma Q S^T + P U) / sqrt(d): staged in shared memory, one TMA
+//            store per chunk
+// The streams hand over through mbarriers: TMA stage full, V full, gates
+// ready (4 sets), Z ready / Z free (2 buffers), and each stream's MMA
+// completions.  For head_dim 64 the same code runs with TMEM lanes 64-127
+// carrying no value row (their results are never read).
 namespace d128 {
 
 constexpr int NS = 256;                 // threads per stream
