@@ -735,29 +735,19 @@ __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) 
 
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
 // columns, gamma * S -> 32 fp32 columns.
-__device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, const float (&x)[32],
+__device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, float (&x)[32],
                                             float gamma) {
-    uint32_t w[16];
+    uint32_t hi[16], lo[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        uint32_t lo;
-        ptx::split_pair(x[2 * e], x[2 * e + 1], w[e], lo);
-        (void)lo;
-    }
-    ptx::tmem_st16(tmem_lane + C_SHI + key0 / 2, w);
+    for (int e = 0; e < 16; ++e) ptx::split_pair(x[2 * e], x[2 * e + 1], hi[e], lo[e]);
+    ptx::tmem_st16(tmem_lane + C_SHI + key0 / 2, hi);
+    ptx::tmem_st16(tmem_lane + C_SLO + key0 / 2, lo);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-        uint32_t hi;
-        ptx::split_pair(x[2 * e], x[2 * e + 1], hi, w[e]);
-        (void)hi;
-    }
-    ptx::tmem_st16(tmem_lane + C_SLO + key0 / 2, w);
+    for (int e = 0; e < 16; ++e) hi[e] = __float_as_uint(gamma * x[e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0, hi);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(gamma * x[e]);
-    ptx::tmem_st16(tmem_lane + C_SACC + key0, w);
-#pragma unroll
-    for (int e = 0; e < 16; ++e) w[e] = __float_as_uint(gamma * x[16 + e]);
-    ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, w);
+    for (int e = 0; e < 16; ++e) lo[e] = __float_as_uint(gamma * x[16 + e]);
+    ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, lo);
 }
 
 template <int D>
