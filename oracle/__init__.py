@@ -24,7 +24,9 @@ section "What Gated Delta Net is, in plain language" (delta rule overwrites,
 the gate scales what is kept); "marcsun13/ggml-gated-delta-net" model card,
 section "Ops" and its shape table (signature, shapes, [value][key] state,
 zeros as the fresh state, identity key-head mapping, 1/sqrt(head_dim) on the
-output, log-domain gate exponentiated by the op).
+output, log-domain gate exponentiated by the op).  With fewer key heads than
+value heads (q, k carrying n_k heads), value head h reads key head h % n_k:
+the tiled convention the same model card's contract notes give for upstream.
 """
 from __future__ import annotations
 
@@ -59,7 +61,7 @@ def _load():
         lib = ctypes.CDLL(build())
         f = lib.gdn_oracle_forward
         f.restype = ctypes.c_int
-        f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 5
+        f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6
         lib.gdn_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -74,13 +76,15 @@ def _f32(x):
 
 
 def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0):
-    """float64 recurrence in C.  q, k, v: (B, T, H, d); g, beta: (B, T, H);
-    state: (B, H, d, d) [value][key] or None for zeros.  Inputs are taken as
-    float32 (exact for bf16 data).  Returns (out (B,T,H,d), state_out
-    (B,H,d,d)), both float64."""
+    """float64 recurrence in C.  q, k: (B, T, Hk, d); v: (B, T, H, d); g, beta:
+    (B, T, H); state: (B, H, d, d) [value][key] or None for zeros; value head
+    h reads key head h % Hk (Hk == H: identity).  Inputs are taken as float32
+    (exact for bf16 data).  Returns (out (B,T,H,d), state_out (B,H,d,d)), both
+    float64."""
     q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
-    B, T, H, d = q.shape
-    assert k.shape == q.shape and v.shape == q.shape
+    B, T, H, d = v.shape
+    Hk = q.shape[2]
+    assert k.shape == q.shape and q.shape == (B, T, Hk, d) and 1 <= Hk <= max(H, 1)
     assert g.shape == (B, T, H) and beta.shape == (B, T, H)
     st = None if state is None else _f32(state)
     if st is not None:
@@ -89,7 +93,7 @@ def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0):
     s_out = np.empty((B, H, d, d), dtype=np.float64)
     p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     rc = _load().gdn_oracle_forward(p(q), p(k), p(v), p(g), p(beta), p(st), p(out), p(s_out),
-                                    B, T, H, d, int(n_threads))
+                                    B, T, H, Hk, d, int(n_threads))
     if rc != 0:
         raise RuntimeError(f"gdn_oracle_forward failed ({rc})")
     return out, s_out
@@ -97,19 +101,22 @@ def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0):
 
 def recurrent_np(q, k, v, g, beta, state=None):
     """The same float64 recurrence in numpy, token by token:
-    decay, read r = S k, overwrite S += beta (v - r) k^T, emit S q / sqrt(d)."""
+    decay, read r = S k, overwrite S += beta (v - r) k^T, emit S q / sqrt(d).
+    q, k may carry fewer heads (Hk) than v: value head h reads key head h % Hk."""
     q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
-    B, T, H, d = q.shape
+    B, T, H, d = v.shape
+    Hk = q.shape[2]
     out = np.zeros((B, T, H, d))
     s_out = np.zeros((B, H, d, d))
     for b in range(B):
         for h in range(H):
+            hk = h % Hk
             S = np.zeros((d, d)) if state is None else np.array(state[b, h], dtype=np.float64)
             for t in range(T):
                 S = np.exp(g[b, t, h]) * S
-                r = S @ k[b, t, h]
-                S = S + beta[b, t, h] * np.outer(v[b, t, h] - r, k[b, t, h])
-                out[b, t, h] = S @ q[b, t, h] / np.sqrt(d)
+                r = S @ k[b, t, hk]
+                S = S + beta[b, t, h] * np.outer(v[b, t, h] - r, k[b, t, hk])
+                out[b, t, h] = S @ q[b, t, hk] / np.sqrt(d)
             s_out[b, h] = S
     return out, s_out
 

@@ -33,6 +33,10 @@
  *     g,beta (n_seqs, n_tokens, n_heads), state (n_seqs, n_heads, d, d);
  *     state indexed [value][key], a fresh state is zeros; one key head per
  *     value head; the output carries 1/sqrt(head_dim); g is a log-domain gate.
+ *   - same model card, the first contract note under the shape table: with
+ *     fewer key heads than value heads, upstream maps value head i to key
+ *     head i % n_k_heads (the tiled convention).  q and k then carry n_k_heads
+ *     heads; n_k_heads == n_heads is the identity mapping.
  *
  * Inputs are float32 (bf16 data is upcast exactly by the caller); every
  * operation is done in double.  No blocking, no reordering beyond the
@@ -48,11 +52,12 @@
 
 /* One (sequence, head) problem.  Element strides are given so the caller can
  * pass the (b, h) slice of a (B, T, H, d) array without copying:
- *   q/k/v/out: token t, component i at [t * tok_stride + i]
+ *   q/k:       token t, component j at [t * qk_stride + j]
+ *   v/out:     token t, component i at [t * tok_stride + i]
  *   g/beta:    token t at [t * gate_stride]
  *   state:     S[i][j] at [i * d + j]                                      */
 static void oracle_one_head(const float *q, const float *k, const float *v,
-                            const float *g, const float *beta,
+                            const float *g, const float *beta, long qk_stride,
                             long tok_stride, long gate_stride,
                             const float *state_in, double *out,
                             double *state_out, int T, int d, double *S,
@@ -64,8 +69,8 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
             S[(size_t)i * d + j] = state_in ? (double)state_in[(size_t)i * d + j] : 0.0;
 
     for (int t = 0; t < T; ++t) {
-        const float *qt = q + (size_t)t * tok_stride;
-        const float *kt = k + (size_t)t * tok_stride;
+        const float *qt = q + (size_t)t * qk_stride;
+        const float *kt = k + (size_t)t * qk_stride;
         const float *vt = v + (size_t)t * tok_stride;
         const double alpha = exp((double)g[(size_t)t * gate_stride]);
         const double b = (double)beta[(size_t)t * gate_stride];
@@ -99,7 +104,8 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
 }
 
 /* Full problem, all (b, h) pairs.  Layouts as on the model card:
- *   q, k, v, out : (B, T, H, d) contiguous
+ *   q, k         : (B, T, Hk, d) contiguous; value head h reads key head h % Hk
+ *   v, out       : (B, T, H, d) contiguous
  *   g, beta      : (B, T, H) contiguous
  *   state_in     : (B, H, d, d) contiguous, [value][key]; NULL means zeros
  *   state_out    : (B, H, d, d) contiguous, [value][key]
@@ -108,10 +114,11 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
 int gdn_oracle_forward(const float *q, const float *k, const float *v,
                        const float *g, const float *beta,
                        const float *state_in, double *out, double *state_out,
-                       int B, int T, int H, int d, int n_threads)
+                       int B, int T, int H, int Hk, int d, int n_threads)
 {
-    if (B < 0 || T < 0 || H < 0 || d <= 0)
+    if (B < 0 || T < 0 || H < 0 || d <= 0 || Hk <= 0 || Hk > (H > 0 ? H : 1))
         return -1;
+    const long qk_stride = (long)Hk * d;
     const long tok_stride = (long)H * d;
     const long gate_stride = H;
     const long n_pairs = (long)B * H;
@@ -136,10 +143,11 @@ int gdn_oracle_forward(const float *q, const float *k, const float *v,
                 continue;
             const long b = p / H, h = p % H;
             const size_t in_off = (size_t)b * T * H * d + (size_t)h * d;
+            const size_t qk_off = (size_t)b * T * Hk * d + (size_t)(h % Hk) * d;
             const size_t gb_off = (size_t)b * T * H + (size_t)h;
             const size_t st_off = (size_t)p * d * d;
-            oracle_one_head(q + in_off, k + in_off, v + in_off, g + gb_off,
-                            beta + gb_off, tok_stride, gate_stride,
+            oracle_one_head(q + qk_off, k + qk_off, v + in_off, g + gb_off,
+                            beta + gb_off, qk_stride, tok_stride, gate_stride,
                             state_in ? state_in + st_off : NULL,
                             out + in_off, state_out + st_off, T, d, S, r);
         }

@@ -233,9 +233,45 @@ def pin_definition_form(impl):
     return True
 
 
+def _key_head_problem(seed, H, Hk, T):
+    """q, k with Hk heads, v / g / beta / state with H heads."""
+    q, k, v, g, beta, S0 = rand_problem(seed, B=2, T=T, H=H)
+    return q[:, :, :Hk].copy(), k[:, :, :Hk].copy(), v, g, beta, S0
+
+
+def pin_key_heads_single_step(impl):
+    """Fewer key heads than value heads, one token from zeros: value head h
+    reads key head h % Hk (the tiled mapping of the model card's contract
+    notes), so S_1[h] = beta_h v_h k_{h%Hk}^T and o_1[h] = beta_h
+    (k_{h%Hk} . q_{h%Hk}) v_h / sqrt(d), written out head by head."""
+    for H, Hk in ((4, 2), (6, 3), (4, 1)):
+        q, k, v, g, beta, _ = _key_head_problem(30 + H + Hk, H, Hk, 1)
+        out, S = impl(q, k, v, g, beta, None)
+        d = q.shape[-1]
+        for h in range(H):
+            j = h % Hk
+            b = beta[:, 0, h]
+            want_S = b[:, None, None] * np.einsum("bi,bj->bij", v[:, 0, h], k[:, 0, j])
+            want_o = (b * np.sum(k[:, 0, j] * q[:, 0, j], axis=-1))[:, None] * v[:, 0, h] / math.sqrt(d)
+            if rel(S[:, h], want_S) > 1e-13 or rel(out[:, 0, h], want_o) > 1e-13:
+                return False
+    return True
+
+
+def pin_key_heads_tiled_expansion(impl):
+    """Fewer key heads equals passing q, k expanded by tiling the head axis
+    (heads 0..Hk-1 repeated H/Hk times), over several tokens and a state."""
+    H, Hk = 6, 2
+    q, k, v, g, beta, S0 = _key_head_problem(40, H, Hk, 5)
+    out, S = impl(q, k, v, g, beta, S0)
+    qe, ke = np.tile(q, (1, 1, H // Hk, 1)), np.tile(k, (1, 1, H // Hk, 1))
+    out_e, S_e = impl(qe, ke, v, g, beta, S0)
+    return rel(out, out_e) < 1e-13 and rel(S, S_e) < 1e-13
+
+
 PINS = [pin_golden_exact, pin_identity, pin_overwrite, pin_forgetting, pin_pure_decay,
         pin_single_step, pin_layout, pin_row_equivariance, pin_linearity, pin_state_carry,
-        pin_definition_form]
+        pin_definition_form, pin_key_heads_single_step, pin_key_heads_tiled_expansion]
 
 
 @pytest.mark.parametrize("impl", list(IMPLS))
@@ -257,6 +293,13 @@ def test_golden_fixture_is_current():
 
 def test_c_matches_numpy_twin():
     q, k, v, g, beta, S0 = rand_problem(12, B=3, T=11, H=2, d=16)
+    o1, S1 = oracle.recurrent_c(q, k, v, g, beta, S0)
+    o2, S2 = oracle.recurrent_np(q, k, v, g, beta, S0)
+    assert rel(o1, o2) < 1e-13 and rel(S1, S2) < 1e-13
+
+
+def test_c_matches_numpy_twin_key_heads():
+    q, k, v, g, beta, S0 = _key_head_problem(17, 6, 3, 9)
     o1, S1 = oracle.recurrent_c(q, k, v, g, beta, S0)
     o2, S2 = oracle.recurrent_np(q, k, v, g, beta, S0)
     assert rel(o1, o2) < 1e-13 and rel(S1, S2) < 1e-13
@@ -306,15 +349,17 @@ def test_chunked_algebra_fast_and_slow_gates():
 def _mutant(kind):
     def impl(q, k, v, g, beta, state=None):
         q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
-        B, T, H, d = q.shape
+        B, T, H, d = v.shape
+        Hk = q.shape[2]
         out = np.zeros((B, T, H, d))
         s_out = np.zeros((B, H, d, d))
         for b in range(B):
             for h in range(H):
+                hk = h // (H // Hk) if kind == "grouped_heads" else h % Hk
                 S = np.zeros((d, d)) if state is None else np.array(state[b, h], dtype=np.float64)
                 for t in range(T):
                     a = np.exp(-g[b, t, h]) if kind == "gate_sign" else np.exp(g[b, t, h])
-                    kt, vt, qt, bt = k[b, t, h], v[b, t, h], q[b, t, h], beta[b, t, h]
+                    kt, vt, qt, bt = k[b, t, hk], v[b, t, h], q[b, t, hk], beta[b, t, h]
                     if kind == "no_decay":
                         a = 1.0
                     S_old = S
@@ -347,7 +392,7 @@ def _mutant(kind):
 
 MUTANTS = ["gate_sign", "no_decay", "decay_after", "transposed", "delta_sign",
            "beta_on_v_only", "outer_swapped", "no_read", "emit_old_state", "emit_with_key",
-           "no_scale"]
+           "no_scale", "grouped_heads"]
 
 
 def test_unmutated_copy_passes_every_pin():
