@@ -98,6 +98,13 @@ def decode_bytes_per_head(d, in_bytes):
     return 8 * d * d + 3 * d * in_bytes + 4 * d + 8
 
 
+def run_bytes(B, T, H, Hk, d, in_bytes):
+    """Algorithmic bytes of one call on the recurrent path: the state read and
+    written once (fp32), q and k once per key head, v, out (fp32), g and beta
+    once per value head and token."""
+    return B * H * 8 * d * d + B * T * (2 * Hk * d * in_bytes + H * (d * in_bytes + 4 * d + 8))
+
+
 def prefill_bytes_per_token_head(d, in_bytes):
     return 3 * d * in_bytes + 4 * d + 8
 
@@ -324,7 +331,7 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     out = torch.empty((B, T, H, d), dtype=torch.float32, device=dev)
     st = inp["state"] if inp["state"] is not None else None
     st_out = st if (in_place and st is not None) else torch.empty((B, H, d, d), device=dev)
-    path = gdn.select_path(T, d, w.dtype)
+    path = gdn.select_path(B, T, H, d, w.dtype)
     ws = None
     nws = gdn.workspace_bytes(B, T, H, d, w.dtype, path)
     if nws:
@@ -342,7 +349,7 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     res = {"workload": w.name, "path": path, "ms_per_step": ms,
            "launches_per_step": LAUNCHES_PER_CALL[path]}
     if kind == "decode":
-        bytes_launch = B * H * decode_bytes_per_head(d, in_b)
+        bytes_launch = run_bytes(B, T, H, w.n_k, d, in_b)
         achieved = bytes_launch / (ms / 1e3) / 1e9
         res.update({"metric": "decode us/step", "value": ms * 1e3, "unit": "us/step",
                     "roofline": {"bound": "hbm", "achieved": achieved,
@@ -493,7 +500,8 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     timer = Timer(torch, stream, flush)
 
-    specs = [(W.DECODE_B64, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
+    specs = [(W.DECODE_B64, "decode"), (W.MULTITOKEN_B64_T4, "decode"),
+             (W.DECODE_B64_HK16, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
              (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
     if args.only:
         w, kind = next((w, k) for w, k in specs if w.name == args.only)

@@ -105,7 +105,13 @@ int gdn_forward_bf16(const void *q, const void *k, const void *v,
                      gdn_stream_t stream);
 
 /*
- * gdn_forward_ex -- explicit dtype, path and workspace.
+ * gdn_forward_ex -- explicit key-head count, dtype, path and workspace.
+ * n_k_heads: number of heads q and k carry; 0 means n_heads.  q and k are
+ *   then (n_seqs, n_tokens, n_k_heads, head_dim) and value head i reads key
+ *   (and query) head i % n_k_heads -- the tiled mapping that the model card's
+ *   contract notes under the "Ops" shape table give for upstream; with
+ *   n_k_heads == n_heads it is the identity.  n_k_heads must divide n_heads
+ *   (else GDN_ERR_ARG).  v, g, beta, out and the state keep n_heads heads.
  * dtype: GDN_DTYPE_*; path: GDN_PATH_*.
  * workspace: caller-owned device buffer of at least
  *   gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype, path)
@@ -117,7 +123,7 @@ int gdn_forward_bf16(const void *q, const void *k, const void *v,
 int gdn_forward_ex(const void *q, const void *k, const void *v,
                    const float *g, const float *beta, const float *state_in,
                    float *out, float *state_out,
-                   int n_seqs, int n_tokens, int n_heads, int head_dim,
+                   int n_seqs, int n_tokens, int n_heads, int n_k_heads, int head_dim,
                    int dtype, int path, void *workspace, size_t workspace_bytes,
                    gdn_stream_t stream);
 
@@ -129,8 +135,12 @@ size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
 /* Which path AUTO selects (GDN_PATH_RECURRENT or GDN_PATH_CHUNKED) for
  * these sizes and dtype, or a negative GDN_ERR_* for unsupported ones.
  * AUTO takes the chunked path for bf16 q/k/v, head_dim 64/128/256 and at
- * least 64 tokens; everything else runs the recurrent path. */
-int gdn_select_path(int n_tokens, int head_dim, int dtype);
+ * least T_switch tokens, everything else runs the recurrent path.  T_switch
+ * was measured on GB300 and depends on head_dim and on the number of
+ * (sequence, head) pairs P = n_seqs * n_heads:
+ *   head_dim 64: 48;  128: 40 (P < 128) or 24 (P >= 128);
+ *   256: 48 (P < 128) or 64 (P >= 128). */
+int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype);
 
 /*
  * gdn_supports -- capability query, the counterpart of the model card's

@@ -13,7 +13,9 @@ q, k, v: (n_seqs, n_tokens, n_heads, head_dim) bf16 or fp32 CUDA tensors,
 g, beta: (n_seqs, n_tokens, n_heads) fp32, state: (n_seqs, n_heads, head_dim,
 head_dim) fp32 [value][key] or None (zeros).  out is fp32 and already carries
 1/sqrt(head_dim).  ("marcsun13/ggml-gated-delta-net" model card, section
-"Ops" and its shape table.)
+"Ops" and its shape table.)  q and k may carry fewer heads n_k (dividing
+n_heads): value head i then reads key head i % n_k, the tiled mapping of the
+model card's contract notes.
 """
 from __future__ import annotations
 
@@ -56,12 +58,12 @@ def lib():
         fwd = [vp, vp, vp, fp, fp, fp, fp, fp, i, i, i, i]
         L.gdn_forward.argtypes = fwd + [vp]
         L.gdn_forward_bf16.argtypes = fwd + [vp]
-        L.gdn_forward_ex.argtypes = fwd + [i, i, vp, sz, vp]
+        L.gdn_forward_ex.argtypes = fwd[:11] + [i, i, i, i, vp, sz, vp]
         for f in (L.gdn_forward, L.gdn_forward_bf16, L.gdn_forward_ex):
             f.restype = i
         L.gdn_workspace_bytes.argtypes = [i, i, i, i, i, i]
         L.gdn_workspace_bytes.restype = sz
-        L.gdn_select_path.argtypes = [i, i, i]
+        L.gdn_select_path.argtypes = [i, i, i, i, i]
         L.gdn_select_path.restype = i
         L.gdn_supports.argtypes = [i]
         L.gdn_supports.restype = i
@@ -83,9 +85,11 @@ def supports(head_dim: int) -> int:
     return int(lib().gdn_supports(int(head_dim)))
 
 
-def select_path(n_tokens: int, head_dim: int, dtype: str = "bf16") -> str:
+def select_path(n_seqs: int, n_tokens: int, n_heads: int, head_dim: int,
+                dtype: str = "bf16") -> str:
+    """The path AUTO takes for these sizes: "recurrent" or "chunked"."""
     dt = DTYPE_BF16 if dtype in ("bf16", "bfloat16") else DTYPE_F32
-    r = int(lib().gdn_select_path(int(n_tokens), int(head_dim), dt))
+    r = int(lib().gdn_select_path(int(n_seqs), int(n_tokens), int(n_heads), int(head_dim), dt))
     if r < 0:
         raise GdnError(r, "gdn_select_path")
     return {v: k for k, v in PATHS.items()}[r]
@@ -128,10 +132,14 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
         dt = DTYPE_F32
     else:
         raise TypeError(f"q/k/v must be bf16 or fp32, got {q.dtype}")
-    if q.dim() != 4:
-        raise ValueError("q must be (n_seqs, n_tokens, n_heads, head_dim)")
-    B, T, H, d = q.shape
-    for name, t, shape, dtype in (("k", k, (B, T, H, d), q.dtype), ("v", v, (B, T, H, d), q.dtype),
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be (n_seqs, n_tokens, heads, head_dim)")
+    B, T, H, d = v.shape
+    Hk = q.shape[2]
+    if tuple(q.shape) != (B, T, Hk, d) or Hk < 1 or H % Hk != 0:
+        raise ValueError(f"q: expected (n_seqs, n_tokens, n_k, head_dim) with n_k dividing "
+                         f"{H}, got {tuple(q.shape)}")
+    for name, t, shape, dtype in (("k", k, (B, T, Hk, d), q.dtype), ("v", v, (B, T, H, d), q.dtype),
                                   ("g", g, (B, T, H), torch.float32),
                                   ("beta", beta, (B, T, H), torch.float32)):
         if tuple(t.shape) != shape or t.dtype != dtype:
@@ -158,7 +166,7 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
         rc = L.gdn_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                              _ptr(out), _ptr(state_out), B, T, H, d, dt, PATHS[path],
+                              _ptr(out), _ptr(state_out), B, T, H, Hk, d, dt, PATHS[path],
                               ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != OK:
         raise GdnError(rc, "gdn_forward_ex")

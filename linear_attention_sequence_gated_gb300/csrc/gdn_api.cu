@@ -58,27 +58,43 @@ Range range_of(const void *p, unsigned long long bytes) {
 }
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Tokens from which AUTO prefers the chunked path.
-constexpr int kChunkedMinTokens = 64;
+// Tokens from which AUTO prefers the chunked path, measured on GB300 with
+// bf16 q/k/v (both paths timed over T = 2..128 for 32, 128, 256 and 2048
+// (sequence, head) pairs).  The recurrent path costs a near-constant time
+// per token; the chunked path a near-constant time per 64-token chunk, so
+// the switch sits where one chunk's time equals the tokens' time.  With few
+// (sequence, head) pairs the recurrent kernel has more of the GPU per pair
+// and stays ahead longer.
+int chunked_min_tokens(long long pairs, int head_dim) {
+    const bool many = pairs >= 128;
+    switch (head_dim) {
+        case 64: return 48;
+        case 128: return many ? 24 : 40;
+        case 256: return many ? 64 : 48;
+        default: return INT_MAX;
+    }
+}
 
-int select_path(int n_tokens, int head_dim, int dtype) {
+int select_path(long long pairs, int n_tokens, int head_dim, int dtype) {
     const int caps = gdn_supports(head_dim);
     if (!caps) return GDN_ERR_HEADDIM;
     if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_ARG;
-    if ((caps & 2) && dtype == GDN_DTYPE_BF16 && n_tokens >= kChunkedMinTokens)
+    if ((caps & 2) && dtype == GDN_DTYPE_BF16 && n_tokens >= chunked_min_tokens(pairs, head_dim))
         return GDN_PATH_CHUNKED;
     return GDN_PATH_RECURRENT;
 }
 
 struct Sizes {
-    unsigned long long qkv_bytes, gb_bytes, state_bytes, out_bytes;
+    unsigned long long qk_bytes, v_bytes, gb_bytes, state_bytes, out_bytes;
 };
 
 // Host-side validation; fills `sz`.  Launches nothing.
 int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
              const float *state_in, const float *out, const float *state_out, int B, int T,
-             int H, int d, int dtype, int path, Sizes *sz) {
+             int H, int Hk, int d, int dtype, int path, Sizes *sz) {
     if (B < 0 || T < 0 || H < 0 || d <= 0) return GDN_ERR_ARG;
+    // key heads: value head i reads key head i % Hk; Hk must divide H
+    if (H > 0 && (Hk < 1 || Hk > H || H % Hk != 0)) return GDN_ERR_ARG;
     if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return GDN_ERR_ARG;
     if (path != GDN_PATH_AUTO && path != GDN_PATH_RECURRENT && path != GDN_PATH_CHUNKED)
         return GDN_ERR_ARG;
@@ -88,15 +104,17 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     if (path == GDN_PATH_CHUNKED && !(caps & 2)) return GDN_ERR_HEADDIM;
     if (path == GDN_PATH_CHUNKED && dtype != GDN_DTYPE_BF16) return GDN_ERR_DTYPE;
 
-    unsigned long long bth, bthd, bh, bhdd;
+    unsigned long long bth, bthd, bthkd, bh, bhdd;
     if (!mul_ok((unsigned long long)B * (unsigned long long)T, (unsigned long long)H, &bth))
         return GDN_ERR_ARG;
     if (!mul_ok(bth, (unsigned long long)d, &bthd)) return GDN_ERR_ARG;
+    bthkd = H > 0 ? bthd / (unsigned long long)H * (unsigned long long)Hk : 0;
     bh = (unsigned long long)B * (unsigned long long)H;
     if (!mul_ok(bh, (unsigned long long)d * (unsigned long long)d, &bhdd)) return GDN_ERR_ARG;
     if (bh > (unsigned long long)INT_MAX) return GDN_ERR_ARG;  // one block row per (b, h)
     const unsigned long long elt = dtype == GDN_DTYPE_BF16 ? 2 : 4;
-    if (!span_bytes(bthd, elt, &sz->qkv_bytes) || !span_bytes(bth, 4, &sz->gb_bytes) ||
+    if (!span_bytes(bthkd, elt, &sz->qk_bytes) || !span_bytes(bthd, elt, &sz->v_bytes) ||
+        !span_bytes(bth, 4, &sz->gb_bytes) ||
         !span_bytes(bhdd, 4, &sz->state_bytes) || !span_bytes(bthd, 4, &sz->out_bytes))
         return GDN_ERR_ARG;
 
@@ -112,8 +130,8 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
         if (!aligned(g, 4) || !aligned(beta, 4)) return GDN_ERR_ALIGN;
     }
 
-    const Range rq = range_of(q, sz->qkv_bytes), rk = range_of(k, sz->qkv_bytes),
-                rv = range_of(v, sz->qkv_bytes), rg = range_of(g, sz->gb_bytes),
+    const Range rq = range_of(q, sz->qk_bytes), rk = range_of(k, sz->qk_bytes),
+                rv = range_of(v, sz->v_bytes), rg = range_of(g, sz->gb_bytes),
                 rb = range_of(beta, sz->gb_bytes), rsi = range_of(state_in, sz->state_bytes),
                 ro = range_of(out, bth > 0 ? sz->out_bytes : 0),
                 rso = range_of(state_out, sz->state_bytes);
@@ -126,10 +144,11 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
 }
 
 int run(const void *q, const void *k, const void *v, const float *g, const float *beta,
-        const float *state_in, float *out, float *state_out, int B, int T, int H, int d,
+        const float *state_in, float *out, float *state_out, int B, int T, int H, int Hk, int d,
         int dtype, int path, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     Sizes sz{};
-    int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, T, H, d, dtype, path, &sz);
+    int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype, path,
+                      &sz);
     if (rc != GDN_OK) return rc;
     if ((long long)B * H == 0) return GDN_OK;
 
@@ -145,7 +164,7 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
         return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     }
 
-    if (path == GDN_PATH_AUTO) path = select_path(T, d, dtype);
+    if (path == GDN_PATH_AUTO) path = select_path((long long)B * H, T, d, dtype);
     const size_t need =
         path == GDN_PATH_CHUNKED ? gdn::chunked_workspace_bytes(B, T, H, d, dtype) : 0;
     if (need > 0 && workspace && (workspace_bytes < need || !aligned(workspace, 256)))
@@ -155,7 +174,7 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
     int *status = status_word_for_current_device();
     if (!status) return GDN_ERR_CUDA;
 
-    gdn::Problem p{q, k, v, g, beta, state_in, out, state_out, B, T, H, d, dtype,
+    gdn::Problem p{q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype,
                    (float)(1.0 / std::sqrt((double)d)), status};
 
     if (path == GDN_PATH_RECURRENT) {
@@ -183,23 +202,25 @@ extern "C" {
 int gdn_forward(const float *q, const float *k, const float *v, const float *g,
                 const float *beta, const float *state_in, float *out, float *state_out,
                 int n_seqs, int n_tokens, int n_heads, int head_dim, gdn_stream_t stream) {
-    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
-               GDN_DTYPE_F32, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, n_heads,
+               head_dim, GDN_DTYPE_F32, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gdn_forward_bf16(const void *q, const void *k, const void *v, const float *g,
                      const float *beta, const float *state_in, float *out, float *state_out,
                      int n_seqs, int n_tokens, int n_heads, int head_dim, gdn_stream_t stream) {
-    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
-               GDN_DTYPE_BF16, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, n_heads,
+               head_dim, GDN_DTYPE_BF16, GDN_PATH_AUTO, nullptr, 0, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gdn_forward_ex(const void *q, const void *k, const void *v, const float *g,
                    const float *beta, const float *state_in, float *out, float *state_out,
-                   int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype, int path,
-                   void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
-    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads, head_dim,
-               dtype, path, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
+                   int n_seqs, int n_tokens, int n_heads, int n_k_heads, int head_dim, int dtype,
+                   int path, void *workspace, size_t workspace_bytes, gdn_stream_t stream) {
+    if (n_k_heads < 0) return GDN_ERR_ARG;
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads,
+               n_k_heads == 0 ? n_heads : n_k_heads, head_dim, dtype, path, workspace,
+               workspace_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype,
@@ -207,15 +228,16 @@ size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, 
     if (n_seqs < 0 || n_tokens < 0 || n_heads < 0 || head_dim <= 0) return 0;
     if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return 0;
     if (n_tokens == 0 || (long long)n_seqs * n_heads == 0) return 0;
-    if (path == GDN_PATH_AUTO) path = select_path(n_tokens, head_dim, dtype);
+    if (path == GDN_PATH_AUTO)
+        path = select_path((long long)n_seqs * n_heads, n_tokens, head_dim, dtype);
     if (path != GDN_PATH_CHUNKED || dtype != GDN_DTYPE_BF16) return 0;
     if (!(gdn_supports(head_dim) & 2)) return 0;
     return gdn::chunked_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype);
 }
 
-int gdn_select_path(int n_tokens, int head_dim, int dtype) {
-    if (n_tokens < 0) return GDN_ERR_ARG;
-    return select_path(n_tokens, head_dim, dtype);
+int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype) {
+    if (n_seqs < 0 || n_tokens < 0 || n_heads < 0) return GDN_ERR_ARG;
+    return select_path((long long)n_seqs * n_heads, n_tokens, head_dim, dtype);
 }
 
 int gdn_supports(int head_dim) {

@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(NT, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
                const float *__restrict__ beta, const float *state_in, float *state_out,
-               float *__restrict__ out, int T, int H, float scale, int *status)
+               float *__restrict__ out, int T, int H, int Hk, float scale, int *status)
 {
     using CF = Cfg<D>;
     constexpr int BV = CF::BV;
@@ -334,8 +334,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
 #pragma unroll
             for (int s = 0; s < D / 64; ++s) {
-                ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h, t0, b);
-                ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h, t0, b);
+                ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h % Hk, t0, b);
+                ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h % Hk, t0, b);
             }
             ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, t0, b);
         }
@@ -757,7 +757,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *state_in, float *state_out,
-                    float *__restrict__ out, int T, int H, float scale, int *status)
+                    float *__restrict__ out, int T, int H, int Hk, float scale,
+                    int *status)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -782,7 +783,6 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
     const int bh = blockIdx.x;
     const int b = bh / H, h = bh - b * H;
     const int n_chunks = (T + C - 1) / C;
-    const size_t tok_stride = (size_t)H * D;
     const size_t st_base = (size_t)bh * D * D;
 
     if (tid == 0) {
@@ -827,8 +827,9 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         ptx::mbar_arrive_expect_tx(&sh.qk_full[st], NSLAB * 2 * 8192);
 #pragma unroll
         for (int s = 0; s < NSLAB; ++s) {
-            ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.qk_full[st], s * 64, h, c * C, b);
-            ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.qk_full[st], s * 64, h, c * C, b);
+            ptx::tma_load_4d(qk + s * 16384, &tm_k, &sh.qk_full[st], s * 64, h % Hk, c * C, b);
+            ptx::tma_load_4d(qk + s * 16384 + 8192, &tm_q, &sh.qk_full[st], s * 64, h % Hk, c * C,
+                             b);
         }
     };
     auto issue_v = [&](int c) {
@@ -1259,8 +1260,8 @@ template <int D>
 cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     using CF = Cfg<D>;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, p.B, p.T, p.H, D, 64, true) ||
-        !make_map(&mk, p.k, p.B, p.T, p.H, D, 64, true) ||
+    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
+        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, CF::BV == 64))
         return cudaErrorInvalidValue;
     static std::once_flag once;
@@ -1272,16 +1273,16 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     if (attr_err != cudaSuccess) return attr_err;
     dim3 grid((unsigned)(p.B * p.H), D / CF::BV);
     chunked_kernel<D><<<grid, NT, CF::SMEM, stream>>>(mq, mk, mv, p.g, p.beta, p.state_in,
-                                                      p.state_out, p.out, p.T, p.H, p.scale,
-                                                      p.status);
+                                                      p.state_out, p.out, p.T, p.H, p.Hk,
+                                                      p.scale, p.status);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, p.q, p.B, p.T, p.H, D, 64, true) ||
-        !make_map(&mk, p.k, p.B, p.T, p.H, D, 64, true) ||
+    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
+        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true) ||
         !make_map_out(&mo, p.out, p.B, p.T, p.H, D))
         return cudaErrorInvalidValue;
@@ -1293,7 +1294,8 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     });
     if (attr_err != cudaSuccess) return attr_err;
     d128::chunked_d128_kernel<D><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
-        mq, mk, mv, mo, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale, p.status);
+        mq, mk, mv, mo, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale,
+        p.status);
     return cudaGetLastError();
 }
 

@@ -10,12 +10,13 @@ namespace gdn {
 
 // One validated call.  All pointers are device pointers; sizes are >= 1.
 struct Problem {
-    const void *q, *k, *v;         // (B, T, H, d), dtype below
+    const void *q, *k;             // (B, T, Hk, d), dtype below
+    const void *v;                 // (B, T, H, d), dtype below
     const float *g, *beta;         // (B, T, H)
     const float *state_in;         // (B, H, d, d) [value][key] or nullptr (zeros)
     float *out;                    // (B, T, H, d) fp32, scaled by 1/sqrt(d)
     float *state_out;              // (B, H, d, d) [value][key]; may equal state_in
-    int B, T, H, d;
+    int B, T, H, Hk, d;            // value head h reads key head h % Hk (Hk divides H)
     int dtype;                     // GDN_DTYPE_F32 / GDN_DTYPE_BF16
     float scale;                   // (float)(1 / sqrt((double)d))
     int *status;                   // device status word (bounded waits report here)

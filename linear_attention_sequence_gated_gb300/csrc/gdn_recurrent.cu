@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(128)
 recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const Tin *__restrict__ v, const float *__restrict__ g,
                  const float *__restrict__ beta, const float *state_in,
-                 float *state_out, float *__restrict__ out, int T, int H,
+                 float *state_out, float *__restrict__ out, int T, int H, int Hk,
                  float scale)
 {
     constexpr int NV = D / (4 * L);   // 128-bit vectors per lane per row
@@ -114,11 +114,14 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
     }
 
-    const size_t tok_stride = (size_t)H * D;                 // between tokens of one head
+    // value head h reads query / key head h % Hk (Hk == H: the identity)
+    const size_t tok_stride = (size_t)H * D;                 // between tokens of one value head
+    const size_t qk_stride = (size_t)Hk * D;                 // between tokens of one key head
     const size_t in_base = ((size_t)b * T * H + h) * D;      // token 0 of (b, h)
+    const size_t qk_base = ((size_t)b * T * Hk + h % Hk) * D;
     const size_t gb_base = (size_t)b * T * H + h;
-    const Tin *qp = q + in_base;
-    const Tin *kp = k + in_base;
+    const Tin *qp = q + qk_base;
+    const Tin *kp = k + qk_base;
     const Tin *vp = v + in_base;
     const float *gp = g + gb_base;
     const float *bp = beta + gb_base;
@@ -126,11 +129,11 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
     using In = TokenInputs<D, L, R, Tin>;
     auto load_token = [&](int t, In &x) {
-        const size_t o = (size_t)t * tok_stride;
+        const size_t o = (size_t)t * tok_stride, oq = (size_t)t * qk_stride;
 #pragma unroll
         for (int j = 0; j < NV; ++j) {
-            x.q[j] = load_raw4(qp + o + (j * L + sub) * 4);
-            x.k[j] = load_raw4(kp + o + (j * L + sub) * 4);
+            x.q[j] = load_raw4(qp + oq + (j * L + sub) * 4);
+            x.k[j] = load_raw4(kp + oq + (j * L + sub) * 4);
         }
 #pragma unroll
         for (int u = 0; u < R; ++u) x.v[u] = load_scalar(vp + o + row0 + u * RU);
@@ -200,6 +203,217 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    make_float4(s[u][j][0], s[u][j][1], s[u][j][2], s[u][j][3]));
 }
 
+// ---------------------------------------------------------------------------
+// Multi-token runs (T >= 2).  The per-token work is short (three dot
+// products over a row, a butterfly, one update), so with a one-token
+// prefetch the loop waits on global-memory latency at every token.  Here the
+// inputs of WT consecutive tokens (q, k of the key head, the block's slice of
+// v, g, beta) are staged in shared memory by asynchronous copies, two windows
+// in flight: window w + 1 streams in while window w is computed.  The state
+// rows stay in registers for the whole run, exactly as in recurrent_kernel.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prev() {   // all but the latest group landed
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+__device__ __forceinline__ Raw4F32 lds_raw4(const float *p) {
+    return {*reinterpret_cast<const float4 *>(p)};
+}
+__device__ __forceinline__ Raw4BF16 lds_raw4(const __nv_bfloat16 *p) {
+    return {*reinterpret_cast<const uint2 *>(p)};
+}
+__device__ __forceinline__ float lds_scalar(const float *p) { return *p; }
+__device__ __forceinline__ float lds_scalar(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+template <int D, int RB, typename Tin, int WT>
+struct alignas(16) TokenWindow {
+    Tin q[WT][D];
+    Tin k[WT][D];
+    Tin v[WT][RB];
+    float g[WT];
+    float beta[WT];
+    float kq[WT];      // k . q of each token, shared by every row
+    float alpha[WT];   // exp(g) of each token
+};
+
+template <int D, int L, int R, typename Tin, int WT>
+__global__ void __launch_bounds__(128)
+recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
+                        const Tin *__restrict__ v, const float *__restrict__ g,
+                        const float *__restrict__ beta, const float *state_in,
+                        float *state_out, float *__restrict__ out, int T, int H, int Hk,
+                        float scale)
+{
+    constexpr int NV = D / (4 * L);
+    constexpr int RU = 32 / L;
+    constexpr int RW = R * RU;
+    constexpr int RB = 4 * RW;
+    constexpr int EPC = 16 / (int)sizeof(Tin);              // elements per 16-byte copy
+    constexpr int CPR = D / EPC;                            // copies per q (or k) row
+    constexpr int CPV = RB / EPC;                           // copies per token's v slice
+    static_assert(D % RB == 0 && NV >= 1 && D == NV * 4 * L, "bad lane split");
+    static_assert(RB % EPC == 0, "v slice must be whole 16-byte copies");
+    static_assert(WT <= 64, "g / beta copies use threads 0..WT-1 and 64..64+WT-1");
+    using Win = TokenWindow<D, RB, Tin, WT>;
+    __shared__ Win win[2];
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    const int bh = blockIdx.x;
+    const int b = bh / H;
+    const int h = bh - b * H;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int sub = lane % L;
+    const int grp = lane / L;
+    const int lrow0 = warp * RW + grp;                      // row within the block
+    const int row0 = blockIdx.y * RB + lrow0;
+
+    float s[R][NV][4];
+    const size_t st_base = (size_t)bh * D * D;
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (state_in) {
+                const float4 t = __ldcs(reinterpret_cast<const float4 *>(
+                    state_in + st_base + (size_t)(row0 + u * RU) * D + (j * L + sub) * 4));
+                s[u][j][0] = t.x; s[u][j][1] = t.y; s[u][j][2] = t.z; s[u][j][3] = t.w;
+            } else {
+                s[u][j][0] = s[u][j][1] = s[u][j][2] = s[u][j][3] = 0.f;
+            }
+        }
+    }
+
+    const size_t tok_stride = (size_t)H * D;
+    const size_t qk_stride = (size_t)Hk * D;
+    const Tin *qp = q + ((size_t)b * T * Hk + h % Hk) * D;
+    const Tin *kp = k + ((size_t)b * T * Hk + h % Hk) * D;
+    const Tin *vp = v + ((size_t)b * T * H + h) * D + blockIdx.y * RB;
+    const float *gp = g + (size_t)b * T * H + h;
+    const float *bp = beta + (size_t)b * T * H + h;
+    float *op = out + ((size_t)b * T * H + h) * D;
+
+    // stage window w (tokens w*WT .. min(T, (w+1)*WT) - 1) into buffer `buf`
+    auto issue = [&](int w, int buf) {
+        const int t0 = w * WT;
+        const int nt = min(WT, T - t0);
+        Win &W_ = win[buf];
+        for (int i = tid; i < 2 * WT * CPR; i += 128) {
+            const int which = i / (WT * CPR), rem = i - which * (WT * CPR);
+            const int j = rem / CPR, c = rem - j * CPR;
+            if (j < nt) {
+                const Tin *src = (which ? kp : qp) + (size_t)(t0 + j) * qk_stride + c * EPC;
+                cp_async16(which ? &W_.k[j][c * EPC] : &W_.q[j][c * EPC], src);
+            }
+        }
+        for (int i = tid; i < WT * CPV; i += 128) {
+            const int j = i / CPV, c = i - j * CPV;
+            if (j < nt) cp_async16(&W_.v[j][c * EPC], vp + (size_t)(t0 + j) * tok_stride + c * EPC);
+        }
+        if (tid < nt) cp_async4(&W_.g[tid], gp + (size_t)(t0 + tid) * H);
+        else if (tid >= 64 && tid - 64 < nt) cp_async4(&W_.beta[tid - 64], bp + (size_t)(t0 + tid - 64) * H);
+        cp_async_commit();
+    };
+
+    const int n_win = (T + WT - 1) / WT;
+    issue(0, 0);
+    for (int w = 0; w < n_win; ++w) {
+        if (w + 1 < n_win) issue(w + 1, (w + 1) & 1);
+        else cp_async_commit();                              // keep the group count uniform
+        cp_async_wait_prev();
+        __syncthreads();                                     // window w visible to all
+        Win &W_ = win[w & 1];
+        const int t0 = w * WT;
+        const int nt = min(WT, T - t0);
+        // the per-token scalars every row needs, once per token: one warp each
+        for (int j = warp; j < nt; j += 4) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = lane; e < D; e += 32)
+                acc = fmaf(lds_scalar(&W_.q[j][e]), lds_scalar(&W_.k[j][e]), acc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) {
+                W_.kq[j] = acc;
+                W_.alpha[j] = expf(W_.g[j]);
+            }
+        }
+        __syncthreads();
+        for (int j = 0; j < nt; ++j) {
+            float qv[NV][4], kv[NV][4];
+#pragma unroll
+            for (int jv = 0; jv < NV; ++jv) {
+                unpack4(lds_raw4(&W_.q[j][(jv * L + sub) * 4]), qv[jv]);
+                unpack4(lds_raw4(&W_.k[j][(jv * L + sub) * 4]), kv[jv]);
+            }
+            float pk[R], pq[R];
+#pragma unroll
+            for (int u = 0; u < R; ++u) { pk[u] = 0.f; pq[u] = 0.f; }
+#pragma unroll
+            for (int jv = 0; jv < NV; ++jv) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+#pragma unroll
+                    for (int u = 0; u < R; ++u) {
+                        pk[u] = fmaf(s[u][jv][e], kv[jv][e], pk[u]);
+                        pq[u] = fmaf(s[u][jv][e], qv[jv][e], pq[u]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int off = L / 2; off > 0; off >>= 1) {
+#pragma unroll
+                for (int u = 0; u < R; ++u) {
+                    pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], off);
+                    pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], off);
+                }
+            }
+            const float alpha = W_.alpha[j];
+            const float kq = W_.kq[j];
+            const float bt = W_.beta[j];
+            const size_t o = (size_t)(t0 + j) * tok_stride;
+#pragma unroll
+            for (int u = 0; u < R; ++u) {
+                const float vv = lds_scalar(&W_.v[j][lrow0 + u * RU]);
+                const float delta = bt * (vv - alpha * pk[u]);
+#pragma unroll
+                for (int jv = 0; jv < NV; ++jv)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s[u][jv][e] = fmaf(alpha, s[u][jv][e], delta * kv[jv][e]);
+                const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
+                if (sub == 0) op[o + row0 + u * RU] = ov;
+            }
+        }
+        __syncthreads();                                     // buffer w & 1 free for window w + 2
+    }
+
+#pragma unroll
+    for (int u = 0; u < R; ++u)
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            __stcs(reinterpret_cast<float4 *>(state_out + st_base + (size_t)(row0 + u * RU) * D +
+                                              (j * L + sub) * 4),
+                   make_float4(s[u][j][0], s[u][j][1], s[u][j][2], s[u][j][3]));
+}
+
+// Tokens staged per window by the multi-token kernel.
+constexpr int kWindow = 8;
+
 template <int D, int L, int R, typename Tin>
 cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     constexpr int RB = 4 * R * (32 / L);
@@ -215,9 +429,14 @@ cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.T >= 2)
+        return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow>,
+                                  static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
+                                  static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in,
+                                  p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
     return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin>, static_cast<const Tin *>(p.q),
                               static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v), p.g,
-                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.scale);
+                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
 }
 
 template <int D, int L, typename Tin>

@@ -27,13 +27,18 @@ class Workload:
     name: str
     B: int                # n_seqs
     T: int                # n_tokens
-    H: int                # n_heads (one key head per value head)
+    H: int                # n_heads (value heads)
     d: int                # head_dim
     dtype: str            # "f32" or "bf16" for q, k, v
     gate_shift: float     # g = -softplus(N(0,1) + gate_shift)
     state_std: float      # 0 -> zero initial state
     layers: int = 1       # independent layers (distinct states) per step
     seed: int = 0
+    Hk: int = 0           # heads of q and k (0: one per value head); divides H
+
+    @property
+    def n_k(self) -> int:
+        return self.Hk or self.H
 
     @property
     def torch_dtype(self):
@@ -52,8 +57,15 @@ PREFILL_16K = Workload("prefill_b8_t16384_h32_d128_bf16", 8, 16384, 32, 128, "bf
                        seed=4)
 PREFILL_16K_D64 = PREFILL_16K.replace(name="prefill_b8_t16384_h64_d64_bf16", H=64, d=64, seed=5)
 PREFILL_16K_D256 = PREFILL_16K.replace(name="prefill_b8_t16384_h16_d256_bf16", H=16, d=256, seed=6)
+# a short run of tokens per sequence (multi-token / speculative decode)
+MULTITOKEN_B64_T4 = Workload("multitoken_b64_t4_h32_d128_bf16", 64, 4, 32, 128, "bf16", 0.0, 0.02,
+                             seed=7)
+# fewer key heads than value heads (16 q/k heads shared by 32 value heads)
+DECODE_B64_HK16 = Workload("decode_b64_h32_hk16_d128_bf16", 64, 1, 32, 128, "bf16", 0.0, 0.02,
+                           seed=8, Hk=16)
 
-ALL = [TINY, DECODE_24L, DECODE_B64, PREFILL_4K, PREFILL_16K, PREFILL_16K_D64, PREFILL_16K_D256]
+ALL = [TINY, DECODE_24L, DECODE_B64, PREFILL_4K, PREFILL_16K, PREFILL_16K_D64, PREFILL_16K_D256,
+       MULTITOKEN_B64_T4, DECODE_B64_HK16]
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -67,8 +79,8 @@ def make_inputs(w: Workload, device="cpu", layer: int = 0, B: int | None = None,
                 T: int | None = None, seed: int | None = None):
     """Draw one layer's inputs for workload ``w`` on ``device``.
 
-    Returns a dict with q, k, v (B, T, H, d) in the workload dtype, g, beta
-    (B, T, H) fp32 and state (B, H, d, d) fp32 or None.  ``B``/``T`` override
+    Returns a dict with q, k (B, T, Hk, d) and v (B, T, H, d) in the workload
+    dtype, g, beta (B, T, H) fp32 and state (B, H, d, d) fp32 or None.  ``B``/``T`` override
     the workload's sizes (same distributions), ``layer`` selects one of the
     workload's independent layers."""
     B = w.B if B is None else B
@@ -77,8 +89,9 @@ def make_inputs(w: Workload, device="cpu", layer: int = 0, B: int | None = None,
     gen = _gen(s, device)
     H, d = w.H, w.d
     shape = (B, T, H, d)
-    q = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
-    k = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+    qk_shape = (B, T, w.n_k, d)
+    q = torch.randn(qk_shape, generator=gen, device=device, dtype=torch.float32)
+    k = torch.randn(qk_shape, generator=gen, device=device, dtype=torch.float32)
     q = q / q.norm(dim=-1, keepdim=True)
     k = k / k.norm(dim=-1, keepdim=True)
     v = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)

@@ -67,16 +67,20 @@ def test_workspace_and_path_queries(L):
     assert L.gdn_workspace_bytes(1, 1, 32, 128, 1, 1) == 0          # recurrent needs none
     assert L.gdn_workspace_bytes(-1, 1, 32, 128, 1, 0) == 0         # invalid sizes -> 0
     assert L.gdn_workspace_bytes(1, 0, 32, 128, 1, 0) == 0          # no tokens -> 0
-    assert gdn.select_path(1, 128) == "recurrent"
-    assert gdn.select_path(5, 32) == "recurrent"
-    assert gdn.select_path(4096, 32) == "recurrent"
-    for d in (64, 128, 256):
-        assert gdn.select_path(63, d) == "recurrent"
-        assert gdn.select_path(64, d) == "chunked"
-        assert gdn.select_path(4096, d, "f32") == "recurrent"
-    assert L.gdn_select_path(10, 48, 1) == gdn.ERR_HEADDIM
-    assert L.gdn_select_path(-1, 128, 1) == gdn.ERR_ARG
-    assert L.gdn_select_path(10, 128, 5) == gdn.ERR_ARG
+    assert gdn.select_path(1, 1, 32, 128) == "recurrent"
+    assert gdn.select_path(1, 5, 32, 32) == "recurrent"
+    assert gdn.select_path(1, 4096, 32, 32) == "recurrent"            # no chunked d = 32
+    # measured switch points: (pairs, head_dim) -> first chunked length
+    for pairs, d, t_switch in ((32, 64, 48), (2048, 64, 48), (32, 128, 40), (128, 128, 24),
+                               (2048, 128, 24), (32, 256, 48), (256, 256, 64)):
+        B, H = pairs // 32, 32
+        assert gdn.select_path(B, t_switch - 1, H, d) == "recurrent"
+        assert gdn.select_path(B, t_switch, H, d) == "chunked"
+        assert gdn.select_path(B, 4096, H, d, "f32") == "recurrent"    # chunked is bf16 only
+    assert L.gdn_select_path(1, 10, 1, 48, 1) == gdn.ERR_HEADDIM
+    assert L.gdn_select_path(1, -1, 1, 128, 1) == gdn.ERR_ARG
+    assert L.gdn_select_path(-1, 10, 1, 128, 1) == gdn.ERR_ARG
+    assert L.gdn_select_path(1, 10, 1, 128, 5) == gdn.ERR_ARG
     # the fused chunked kernel keeps everything on chip: no workspace
     assert L.gdn_workspace_bytes(8, 16384, 32, 128, 1, 2) == 0
 
@@ -88,10 +92,11 @@ MB = 1 << 20
 
 def call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, g=BASE + 192 * MB,
          beta=BASE + 256 * MB, s_in=BASE + 320 * MB, out=BASE + 512 * MB,
-         s_out=BASE + 768 * MB, B=1, T=4, H=2, d=64, dtype=1, path=0, ws=None, ws_bytes=0):
+         s_out=BASE + 768 * MB, B=1, T=4, H=2, Hk=0, d=64, dtype=1, path=0, ws=None,
+         ws_bytes=0):
     p = lambda x: None if x is None else ctypes.c_void_p(x)
     return L.gdn_forward_ex(p(q), p(k), p(v), p(g), p(beta), p(s_in), p(out), p(s_out),
-                            B, T, H, d, dtype, path, p(ws), ws_bytes, None)
+                            B, T, H, Hk, d, dtype, path, p(ws), ws_bytes, None)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -112,6 +117,9 @@ def call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, g=BASE + 192 * MB,
     (dict(s_out=BASE + 192 * MB), gdn.ERR_ALIAS),            # state_out on g
     (dict(B=1 << 20, T=1 << 20, H=1 << 20, d=256), gdn.ERR_ARG),   # size overflow
     (dict(B=70000, H=70000, T=1), gdn.ERR_ARG),              # more (b, h) pairs than a grid row
+    (dict(Hk=-1), gdn.ERR_ARG), (dict(Hk=3), gdn.ERR_ARG),   # key heads: negative, > n_heads
+    (dict(H=6, Hk=4), gdn.ERR_ARG),                          # key heads must divide n_heads
+    (dict(H=4, Hk=2, out=BASE + 512), gdn.ERR_ALIAS),       # out inside q's (B,T,Hk,d) span
 ])
 def test_host_validation_rejects(L, kw, code):
     assert call(L, **kw) == code

@@ -271,3 +271,55 @@ def test_rejects_bad_arguments_without_launching():
     torch.cuda.synchronize()
     assert ei.value.status == gdn.ERR_ALIAS
     assert torch.equal(inp["state"], before)
+
+
+# ---------------------------------------------------------------- key heads
+
+@pytest.mark.parametrize("path", ["recurrent", "chunked"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("Hk", [1, 2, 4])
+def test_fewer_key_heads(path, d, Hk):
+    """q and k with Hk < H heads: value head i reads key head i % Hk (the
+    tiled mapping).  Lengths span several chunks and a ragged tail."""
+    H, T = 8, 150
+    w = W.Workload(f"gqa_d{d}_hk{Hk}", 2, T, H, d, "bf16", 0.0, 0.02, seed=40 + Hk)
+    inp = W.make_inputs(w, "cuda")
+    inp["q"] = inp["q"][:, :, :Hk].contiguous()
+    inp["k"] = inp["k"][:, :, :Hk].contiguous()
+    check(inp, "bf16", path, TOL_RECURRENT if path == "recurrent" else None)
+
+
+def test_fewer_key_heads_fp32_decode():
+    H, Hk = 32, 16
+    w = W.Workload("gqa_decode_f32", 4, 3, H, 128, "f32", 0.0, 0.02, seed=44)
+    inp = W.make_inputs(w, "cuda")
+    inp["q"] = inp["q"][:, :, :Hk].contiguous()
+    inp["k"] = inp["k"][:, :, :Hk].contiguous()
+    check(inp, "f32", "auto", TOL["f32"])
+
+
+def test_fewer_key_heads_rejects_non_divisor():
+    w = W.Workload("gqa_bad", 1, 4, 6, 64, "bf16", 0.0, 0.02, seed=45)
+    inp = W.make_inputs(w, "cuda")
+    with pytest.raises(ValueError):
+        gdn.forward(inp["q"][:, :, :4].contiguous(), inp["k"][:, :, :4].contiguous(), inp["v"],
+                    inp["g"], inp["beta"], inp["state"])
+
+
+@pytest.mark.parametrize("wname", [W.MULTITOKEN_B64_T4.name, W.DECODE_B64_HK16.name])
+def test_short_run_and_key_head_workloads_full_size(wname):
+    """The benchmark's multi-token (4 tokens, 64 sequences) and fewer-key-heads
+    decode workloads at full size, every output and the whole final state."""
+    w = W.BY_NAME[wname]
+    inp = W.make_inputs(w, "cuda")
+    check(inp, w.dtype, "auto", TOL_RECURRENT)
+
+
+@pytest.mark.parametrize("T", [2, 3, 7, 8, 9, 15, 16, 17, 23, 33, 63])
+@pytest.mark.parametrize("d", [32, 64, 128, 256])
+def test_multi_token_runs_recurrent(T, d):
+    """Short runs (2..63 tokens): windows of staged tokens with ragged last
+    windows, for every head_dim, against the oracle."""
+    w = W.Workload(f"short_d{d}_t{T}", 3, T, 4, d, "bf16", 0.0, 0.02, seed=60 + T)
+    inp = W.make_inputs(w, "cuda")
+    check(inp, "bf16", "recurrent", TOL_RECURRENT)
