@@ -325,6 +325,36 @@ def run_decode24(torch, gdn, W, dev, timer, args, dist, peaks):
             "config": cfg, "times_ms": times}
 
 
+def attn_bytes(w, elt):
+    """Algorithmic bytes of one decode-attention call: the cache (k, v) and q
+    read once, the mask read once, the fp32 output written once."""
+    kv = 2 * w.B * w.Hkv * w.n_kv * w.d * elt
+    qb = w.B * w.H * w.n_q * w.d * elt
+    mb = w.B * w.n_q * w.n_kv * elt if w.mask else 0
+    return kv + qb + mb + w.B * w.n_q * w.H * w.d * 4
+
+
+def run_attn(torch, gdn, W, w, dev, timer, args, dist, peaks):
+    """One decode-attention call per step (L2 flushed before each)."""
+    inp = W.make_attn_inputs(w, dev)
+    out = torch.empty((w.B, w.n_q, w.H, w.d), dtype=torch.float32, device=dev)
+
+    def fn():
+        gdn.flash_attn(inp["q"], inp["k"], inp["v"], inp["mask"], out=out)
+
+    times = timer.run(fn, args.steps, args.warmup, dist)
+    ms = dist.max(sum(times) / len(times))
+    elt = 4 if w.dtype == "f32" else 2
+    by = attn_bytes(w, elt)
+    ach = by / (ms / 1e3) / 1e9
+    del inp, out
+    return {"workload": w.name, "path": "flash_attn", "metric": "attention us/call",
+            "value": ms * 1e3, "unit": "us/call", "ms_per_step": ms, "launches_per_step": 1,
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": ach / peaks["hbm_gbs"], "traffic": load_traffic().get(w.name),
+                         "bytes_per_launch": by}}
+
+
 def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_place=True):
     inp = W.make_inputs(w, dev)
     B, T, H, d = w.B, w.T, w.H, w.d
@@ -503,6 +533,12 @@ def main():
     specs = [(W.DECODE_B64, "decode"), (W.MULTITOKEN_B64_T4, "decode"),
              (W.DECODE_B64_HK16, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
              (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
+    if args.only and args.only in W.ATTN_BY_NAME:
+        r = run_attn(torch, gdn, W, W.ATTN_BY_NAME[args.only], dev, timer, args, dist, peaks)
+        if dist.rank == 0:
+            print(json.dumps(r))
+        dist.close()
+        return
     if args.only:
         w, kind = next((w, k) for w, k in specs if w.name == args.only)
         if args.only_seqs:
@@ -521,6 +557,11 @@ def main():
     if not args.no_extra:
         for w, kind in specs:
             r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
+            launches += r["launches_per_step"] * args.steps
+            extra.append(r)
+            torch.cuda.empty_cache()
+        for w in W.ATTN_ALL:
+            r = run_attn(torch, gdn, W, w, dev, timer, args, dist, peaks)
             launches += r["launches_per_step"] * args.steps
             extra.append(r)
             torch.cuda.empty_cache()

@@ -74,11 +74,12 @@ enum gdn_status {
     GDN_ERR_TIMEOUT = -6,   /* a bounded device-side wait gave up (gdn_get_device_status) */
     GDN_ERR_WORKSPACE = -7, /* caller workspace NULL, too small or misaligned */
     GDN_ERR_NOMEM = -8,     /* stream-ordered workspace allocation failed */
-    GDN_ERR_DTYPE = -9      /* dtype not supported on the requested path (chunked: bf16 only) */
+    GDN_ERR_DTYPE = -9,     /* dtype not supported on the requested path (chunked: bf16 only) */
+    GDN_ERR_SHAPE = -10     /* shape outside the op's scope (flash_attn: 20 or more queries) */
 };
 
-/* dtype of q, k, v */
-enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1 };
+/* dtype of q, k, v (F16: decode attention only) */
+enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1, GDN_DTYPE_F16 = 2 };
 
 /* execution path; AUTO picks by n_tokens and head_dim */
 enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 };
@@ -159,6 +160,43 @@ int gdn_supports(int head_dim);
  * Returns GDN_ERR_CUDA if the synchronisation itself failed.
  */
 int gdn_get_device_status(gdn_stream_t stream);
+
+/*
+ * gdn_flash_attn -- decode attention, the flash_attn op of the model card
+ * ("marcsun13/ggml-gated-delta-net", section "flash_attn": shape table, the
+ * vector variant for fewer than 20 queries, grouped-query attention with k
+ * and v passed unexpanded, additive mask, result with tokens before heads):
+ *
+ *   out[b, i, h, :] = sum_j softmax_j(scale * q[b,h,i,:] . k[b,hk,j,:]
+ *                                     + mask[b,0,i,j]) * v[b,hk,j,:]
+ *   hk = h / (n_heads / n_heads_kv)          (grouped heads, as repeat_kv)
+ *
+ * q:    (n_seqs, n_heads, n_q, head_dim_k)        dtype
+ * k:    (n_seqs, n_heads_kv, n_kv, head_dim_k)    dtype
+ * v:    (n_seqs, n_heads_kv, n_kv, head_dim_v)    dtype
+ * mask: (n_seqs, 1, n_q, n_kv) dtype, additive (-inf masks a key), or NULL
+ * out:  (n_seqs, n_q, n_heads, head_dim_v) float32, written by the call
+ * dtype: GDN_DTYPE_F32, GDN_DTYPE_BF16 or GDN_DTYPE_F16 for q, k, v and the
+ *   mask together; arithmetic is float32 with exact upcast.
+ * scale: finite float multiplying q . k (callers usually pass
+ *   1 / sqrt(head_dim_k)).
+ * Supported: 1 <= n_q <= 19 (else GDN_ERR_SHAPE), head_dim_k == head_dim_v in
+ *   {64, 128, 256} (else GDN_ERR_HEADDIM), n_heads_kv dividing n_heads (else
+ *   GDN_ERR_ARG); any n_kv >= 0.  A query whose keys are all masked with
+ *   -inf, and every query when n_kv == 0, gets a zero output row.
+ * q, k, v, out 16-byte aligned; mask aligned to its element size; out must
+ * not overlap an input (GDN_ERR_ALIAS).  Asynchronous on `stream`; argument
+ * errors launch nothing.  Needs no workspace.
+ */
+int gdn_flash_attn(const void *q, const void *k, const void *v, const void *mask, float *out,
+                   int n_seqs, int n_heads, int n_heads_kv, int n_q, int n_kv,
+                   int head_dim_k, int head_dim_v, float scale, int dtype,
+                   gdn_stream_t stream);
+
+/* Capability query, the counterpart of supports_flash_attn(n_q, head_dim_k,
+ * head_dim_v) in the model card's "Ops" table: 1 if gdn_flash_attn serves
+ * that shape, 0 otherwise. */
+int gdn_flash_attn_supports(int n_q, int head_dim_k, int head_dim_v);
 
 /* Static English text for a status code (never NULL). */
 const char *gdn_status_string(int status);

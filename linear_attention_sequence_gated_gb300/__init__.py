@@ -27,14 +27,14 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 OK = 0
 ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NOMEM, \
-    ERR_DTYPE = -1, -2, -3, -4, -5, -6, -7, -8, -9
-DTYPE_F32, DTYPE_BF16 = 0, 1
+    ERR_DTYPE, ERR_SHAPE = -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
+DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
            "gdn_select_path", "gdn_supports", "gdn_get_device_status", "gdn_status_string",
-           "gdn_version"]
+           "gdn_version", "gdn_flash_attn", "gdn_flash_attn_supports"]
 
 _lib = None
 
@@ -72,6 +72,10 @@ def lib():
         L.gdn_status_string.argtypes = [i]
         L.gdn_status_string.restype = ctypes.c_char_p
         L.gdn_version.restype = i
+        L.gdn_flash_attn.argtypes = [vp, vp, vp, vp, fp] + [i] * 7 + [ctypes.c_float, i, vp]
+        L.gdn_flash_attn.restype = i
+        L.gdn_flash_attn_supports.argtypes = [i, i, i]
+        L.gdn_flash_attn_supports.restype = i
         _lib = L
     return _lib
 
@@ -171,3 +175,58 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
     if rc != OK:
         raise GdnError(rc, "gdn_forward_ex")
     return out, state_out
+
+
+def flash_attn_supports(n_q: int, head_dim_k: int, head_dim_v: int) -> bool:
+    """Whether ``flash_attn`` serves this shape (fewer than 20 queries, equal
+    head dims of 64, 128 or 256)."""
+    return bool(lib().gdn_flash_attn_supports(int(n_q), int(head_dim_k), int(head_dim_v)))
+
+
+def flash_attn(q, k, v, mask=None, scale=None, *, out=None, stream=None):
+    """Decode attention: out[b, i, h] = softmax_j(scale q[b,h,i] . k[b,hk,j] +
+    mask[b,0,i,j]) v[b,hk,j], hk = h // (n_heads / n_heads_kv).
+
+    q: (n_seqs, n_heads, n_q, d); k, v: (n_seqs, n_heads_kv, n_kv, d), all of
+    one dtype (fp32, bf16 or fp16); mask: (n_seqs, 1, n_q, n_kv) of the same
+    dtype, additive, or None; scale defaults to 1/sqrt(d).  Returns out
+    (n_seqs, n_q, n_heads, d) fp32.  ("marcsun13/ggml-gated-delta-net" model
+    card, section "flash_attn".)"""
+    import math
+    import torch
+    L = lib()
+    dts = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.float16: DTYPE_F16}
+    if q.dtype not in dts:
+        raise TypeError(f"q/k/v must be fp32, bf16 or fp16, got {q.dtype}")
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D")
+    B, H, n_q, dk = q.shape
+    Hkv, n_kv = k.shape[1], k.shape[2]
+    dv = v.shape[3]
+    if tuple(k.shape) != (B, Hkv, n_kv, dk) or tuple(v.shape) != (B, Hkv, n_kv, dv):
+        raise ValueError(f"k, v: expected (n_seqs, n_heads_kv, n_kv, d), got {tuple(k.shape)}, "
+                         f"{tuple(v.shape)}")
+    tensors = [q, k, v]
+    if mask is not None:
+        if tuple(mask.shape) != (B, 1, n_q, n_kv):
+            raise ValueError(f"mask: expected {(B, 1, n_q, n_kv)}, got {tuple(mask.shape)}")
+        tensors.append(mask)
+    for t in tensors:
+        if t.dtype != q.dtype:
+            raise TypeError("q, k, v and mask must share one dtype")
+    if out is None:
+        out = torch.empty((B, n_q, H, dv), dtype=torch.float32, device=q.device)
+    tensors.append(out)
+    for t in tensors:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous CUDA tensors")
+    if tuple(out.shape) != (B, n_q, H, dv) or out.dtype != torch.float32:
+        raise ValueError("out must be (n_seqs, n_q, n_heads, head_dim) fp32")
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    with torch.cuda.device(q.device):
+        rc = L.gdn_flash_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(mask), _ptr(out), B, H, Hkv, n_q,
+                              n_kv, dk, dv, float(scale), dts[q.dtype], _stream_handle(stream))
+    if rc != OK:
+        raise GdnError(rc, "gdn_flash_attn")
+    return out

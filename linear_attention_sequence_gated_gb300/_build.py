@@ -14,7 +14,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
-SOURCES = ["gdn_api.cu", "gdn_recurrent.cu", "gdn_chunked.cu"]
+SOURCES = ["gdn_api.cu", "gdn_recurrent.cu", "gdn_chunked.cu", "gdn_attn.cu"]
 HEADERS = [os.path.join(CSRC, "gdn_internal.h"), os.path.join(CSRC, "gdn_ptx.cuh"),
            os.path.join(os.path.dirname(PKG), "include", "gdn.h")]
 

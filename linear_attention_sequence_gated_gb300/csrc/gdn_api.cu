@@ -32,31 +32,12 @@ int *status_word_for_current_device() {
     return g_status_ptr[dev];
 }
 
-// Bytes spanned by a dense tensor of `n` elements of `elt` bytes; false on overflow.
-bool span_bytes(unsigned long long n, unsigned long long elt, unsigned long long *out) {
-    if (n != 0 && elt > ULLONG_MAX / n) return false;
-    *out = n * elt;
-    return *out < (1ull << 62);
-}
-
-bool mul_ok(unsigned long long a, unsigned long long b, unsigned long long *out) {
-    if (a != 0 && b > ULLONG_MAX / a) return false;
-    *out = a * b;
-    return true;
-}
-
-struct Range {
-    uintptr_t lo, hi;  // [lo, hi)
-};
-bool overlap(Range a, Range b) {
-    if (a.lo == a.hi || b.lo == b.hi) return false;
-    return a.lo < b.hi && b.lo < a.hi;
-}
-Range range_of(const void *p, unsigned long long bytes) {
-    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-    return {lo, p ? lo + (uintptr_t)bytes : lo};
-}
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+using gdn::host::aligned;
+using gdn::host::mul_ok;
+using gdn::host::overlap;
+using gdn::host::Range;
+using gdn::host::range_of;
+using gdn::host::span_bytes;
 
 // Tokens from which AUTO prefers the chunked path, measured on GB300 with
 // bf16 q/k/v (both paths timed over T = 2..128 for 32, 128, 256 and 2048
@@ -271,6 +252,7 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
         case GDN_ERR_NOMEM: return "stream-ordered workspace allocation failed";
         case GDN_ERR_DTYPE: return "dtype not supported on the requested path (chunked: bf16 only)";
+        case GDN_ERR_SHAPE: return "shape outside the op's scope (flash_attn: 20 or more queries)";
         default: return "unknown status";
     }
 }

@@ -31,4 +31,37 @@ cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
                            cudaStream_t stream);
 bool chunked_supports(int d);
 
+// Host-side argument checks shared by the C-ABI front ends.
+namespace host {
+
+// Bytes spanned by a dense tensor of `n` elements of `elt` bytes; false on overflow.
+inline bool span_bytes(unsigned long long n, unsigned long long elt, unsigned long long *out) {
+    if (n != 0 && elt > ~0ull / n) return false;
+    *out = n * elt;
+    return *out < (1ull << 62);
+}
+
+inline bool mul_ok(unsigned long long a, unsigned long long b, unsigned long long *out) {
+    if (a != 0 && b > ~0ull / a) return false;
+    *out = a * b;
+    return true;
+}
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+inline bool overlap(Range a, Range b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+inline Range range_of(const void *p, unsigned long long bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return {lo, p ? lo + (uintptr_t)bytes : lo};
+}
+inline bool aligned(const void *p, uintptr_t a) {
+    return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+}  // namespace host
+
 }  // namespace gdn

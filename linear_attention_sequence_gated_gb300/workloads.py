@@ -112,3 +112,66 @@ def to_numpy_f32(inputs):
     for key, val in inputs.items():
         out[key] = None if val is None else val.detach().float().cpu().numpy()
     return out
+
+
+# ------------------------------------------------------------------ decode attention
+
+@dataclasses.dataclass(frozen=True)
+class AttnWorkload:
+    """Decode attention: q (B, H, n_q, d); k, v (B, Hkv, n_kv, d); optional
+    additive mask (B, 1, n_q, n_kv).  q, k, v ~ N(0, 1); the mask, when
+    present, is 0 on visible keys and -inf on the last ``masked_tail`` keys
+    of each query row shifted by the query index (a causal tail, as when the
+    queries are the newest tokens of the cache), plus N(0, mask_std)."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    n_q: int
+    n_kv: int
+    d: int
+    dtype: str            # "f32", "bf16" or "f16" for q, k, v and the mask
+    mask: bool = False
+    masked_tail: int = 0
+    mask_std: float = 0.0
+    seed: int = 0
+
+    @property
+    def torch_dtype(self):
+        return {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[self.dtype]
+
+    def replace(self, **kw) -> "AttnWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+# the shape timed on the model card (section "Measured": 16 query heads over 4
+# kv heads, head_dim 256, one query) at its two cache lengths
+ATTN_KV512 = AttnWorkload("attn_b1_h16_kv4_q1_n512_d256_bf16", 1, 16, 4, 1, 512, 256, "bf16",
+                          seed=20)
+ATTN_KV141 = ATTN_KV512.replace(name="attn_b1_h16_kv4_q1_n141_d256_bf16", n_kv=141, seed=21)
+# batched decode over a long cache: the cache streams from HBM
+ATTN_B64_KV4K = AttnWorkload("attn_b64_h32_kv8_q1_n4096_d128_bf16", 64, 32, 8, 1, 4096, 128,
+                             "bf16", seed=22)
+
+ATTN_ALL = [ATTN_KV512, ATTN_KV141, ATTN_B64_KV4K]
+ATTN_BY_NAME = {w.name: w for w in ATTN_ALL}
+
+
+def make_attn_inputs(w: AttnWorkload, device="cpu", seed: int | None = None):
+    """q, k, v (and mask or None) for ``w`` on ``device``, in the workload dtype."""
+    gen = _gen((w.seed if seed is None else seed) * 1000 + 7, device)
+    f = dict(generator=gen, device=device, dtype=torch.float32)
+    q = torch.randn((w.B, w.H, w.n_q, w.d), **f)
+    k = torch.randn((w.B, w.Hkv, w.n_kv, w.d), **f)
+    v = torch.randn((w.B, w.Hkv, w.n_kv, w.d), **f)
+    mask = None
+    if w.mask:
+        mask = torch.randn((w.B, 1, w.n_q, w.n_kv), **f) * w.mask_std
+        if w.masked_tail > 0:
+            j = torch.arange(w.n_kv, device=device)[None, :]
+            i = torch.arange(w.n_q, device=device)[:, None]
+            hidden = j >= (w.n_kv - w.masked_tail + i)
+            mask = mask.masked_fill(hidden[None, None], float("-inf"))
+    dt = w.torch_dtype
+    return {"q": q.to(dt).contiguous(), "k": k.to(dt).contiguous(), "v": v.to(dt).contiguous(),
+            "mask": None if mask is None else mask.to(dt).contiguous()}

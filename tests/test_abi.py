@@ -56,7 +56,7 @@ def test_supports(L):
 
 
 def test_status_strings(L):
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = gdn.status_string(code)
         assert s and s != "unknown status"
     assert gdn.status_string(-99) == "unknown status"
@@ -153,3 +153,54 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(gdn, "_lib", None)
     with pytest.raises(RuntimeError, match="libgdn.so not found"):
         gdn.lib()
+
+
+
+# ------------------------------------------------------------ decode attention
+
+def test_flash_attn_supports(L):
+    for d in (64, 128, 256):
+        for n_q in (1, 5, 19):
+            assert gdn.flash_attn_supports(n_q, d, d)
+        assert not gdn.flash_attn_supports(20, d, d)      # the vector variant only
+        assert not gdn.flash_attn_supports(0, d, d)
+    assert not gdn.flash_attn_supports(1, 128, 64)        # unequal head dims
+    for d in (32, 48, 96, 512):
+        assert not gdn.flash_attn_supports(1, d, d)
+
+
+def attn_call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, mask=BASE + 192 * MB,
+              out=BASE + 256 * MB, B=1, H=16, Hkv=4, n_q=1, n_kv=512, dk=256, dv=256, scale=0.0625,
+              dtype=1):
+    p = lambda x: None if x is None else ctypes.c_void_p(x)
+    return L.gdn_flash_attn(p(q), p(k), p(v), p(mask), p(out), B, H, Hkv, n_q, n_kv, dk, dv,
+                            ctypes.c_float(scale), dtype, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), gdn.ERR_ARG), (dict(n_kv=-1), gdn.ERR_ARG), (dict(n_q=-1), gdn.ERR_ARG),
+    (dict(dtype=3), gdn.ERR_ARG), (dict(dk=48, dv=48), gdn.ERR_HEADDIM),
+    (dict(dk=128, dv=256), gdn.ERR_HEADDIM), (dict(n_q=20), gdn.ERR_SHAPE),
+    (dict(Hkv=3), gdn.ERR_ARG), (dict(Hkv=0), gdn.ERR_ARG), (dict(Hkv=32), gdn.ERR_ARG),
+    (dict(scale=float("inf")), gdn.ERR_ARG), (dict(scale=float("nan")), gdn.ERR_ARG),
+    (dict(q=None), gdn.ERR_ARG), (dict(out=None), gdn.ERR_ARG), (dict(k=None), gdn.ERR_ARG),
+    (dict(v=None), gdn.ERR_ARG),
+    (dict(q=BASE + 8), gdn.ERR_ALIGN), (dict(k=BASE + 64 * MB + 4), gdn.ERR_ALIGN),
+    (dict(out=BASE + 256 * MB + 8), gdn.ERR_ALIGN), (dict(mask=BASE + 192 * MB + 1), gdn.ERR_ALIGN),
+    (dict(out=BASE), gdn.ERR_ALIAS), (dict(out=BASE + 128 * MB + 4096), gdn.ERR_ALIAS),
+    (dict(out=BASE + 192 * MB), gdn.ERR_ALIAS),
+    (dict(B=1 << 20, H=1 << 20, Hkv=1 << 20, n_kv=1 << 20), gdn.ERR_ARG),
+])
+def test_flash_attn_host_validation_rejects(L, kw, code):
+    assert attn_call(L, **kw) == code
+
+
+def test_flash_attn_empty_is_a_no_op(L):
+    # no queries at all: nothing to do and no pointer needed
+    assert attn_call(L, B=0, q=None, k=None, v=None, mask=None, out=None) == gdn.OK
+    assert attn_call(L, n_q=0, q=None, k=None, v=None, mask=None, out=None) == gdn.OK
+    assert attn_call(L, H=0, Hkv=0, q=None, k=None, v=None, mask=None, out=None) == gdn.OK
+
+
+def test_gdn_entry_points_reject_f16(L):
+    assert call(L, dtype=2) == gdn.ERR_ARG
