@@ -41,6 +41,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -55,33 +57,51 @@ constexpr int C = 64;            // chunk length (tokens)
 constexpr int NT = 256;          // threads per CTA (two warpgroups)
 constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrices (16-B rows)
 
+// Shared-memory and TMEM map of the state kernel (head_dim 256).  The chunk
+// transform Z = [T; P T] arrives ready-made from the workspace (written by
+// chunk_z_kernel), so a CTA only carries BV = 64 value rows of the state.
 template <int D>
 struct Cfg {
-    static constexpr int BV = (D == 256) ? 32 : 64;       // value rows per CTA
+    static constexpr int BV = 64;                          // value rows per CTA
+    static constexpr int NVB = D / BV;                     // CTAs per (sequence, head)
     static constexpr int KT = (D + 127) / 128;            // 128-key tiles of the state update
-    static constexpr int NSLAB = (D / 64 < 2) ? 2 : D / 64;  // 64-key slabs (d=64: + a zero slab)
+    static constexpr int NSLAB = D / 64;                   // 64-key slabs of [K;Q]
     // shared memory map (bytes from a 1024-aligned base)
     static constexpr int OFF_QK = 0;                       // [K;Q]: NSLAB x (128 rows x 128 B)
     static constexpr int OFF_V = OFF_QK + NSLAB * 16384;   // V block, 64 rows
     static constexpr int OFF_Z = OFF_V + 8192;             // Z hi, Z lo: 128 rows x 128 B each
     static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
-    static constexpr int OFF_UN = OFF_S + 2 * D * 128;     // union: {A then T, P, W} | {R/U~ hi, lo}
-    static constexpr int SZ_F = 64 * FST * 4;
-    static constexpr int OFF_A = OFF_UN;
-    static constexpr int OFF_P = OFF_A + SZ_F;
-    static constexpr int OFF_W = OFF_P + SZ_F;             // 16 x 96 fp32
-    static constexpr int OFF_RU = OFF_UN;                  // R (then U~) hi, lo: 64 rows x 128 B
-    static constexpr int UN_BYTES = 2 * SZ_F + 16 * 96 * 4;
-    static constexpr int OFF_MISC = OFF_UN + UN_BYTES;     // G, beta, gamma, end-decay
+    static constexpr int OFF_RU = OFF_S + 2 * D * 128;     // R (then U~) hi, lo: 64 rows x 128 B
+    static constexpr int OFF_MISC = OFF_RU + 2 * 8192;     // G, beta, gamma, end-decay
     static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;  // + alignment slack
     // TMEM columns
-    static constexpr int COL_KQ = 0;
-    static constexpr int COL_X = 64;
-    static constexpr int COL_Y = 64 + BV;
-    static constexpr int COL_DS = 64 + 2 * BV;
+    static constexpr int COL_X = 0;
+    static constexpr int COL_Y = BV;
+    static constexpr int COL_DS = 2 * BV;
     static constexpr int TMEM_COLS = 256;
     static_assert(COL_DS + KT * BV <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM + 64 <= 232448, "shared memory (dynamic + static)");
+};
+
+// Bytes of one chunk's Z = [T; P T] in the workspace: bf16 hi then lo, each
+// 128 rows x 64 columns in the 128-byte-swizzled layout the MMA reads.
+constexpr int Z_BYTES = 2 * 16384;
+
+// Shared-memory map of chunk_z_kernel (head_dim D): [K;Q] for the K K^T /
+// Q K^T product, then (reusing the same bytes once that product is done)
+// A -> T, P, the block solve's scratch and the Z tile.
+template <int D>
+struct ZCfg {
+    static constexpr int SZ_F = 64 * FST * 4;              // one 64 x 64 fp32 matrix
+    static constexpr int OFF_QK = 0;                       // D/64 slabs x (K 8 KB | Q 8 KB)
+    static constexpr int OFF_A = 0;                        // A, then T in place
+    static constexpr int OFF_P = SZ_F;
+    static constexpr int OFF_Z = 2 * SZ_F;                 // Z hi | Z lo (W lives here during the solve)
+    static constexpr int REGION = (D / 64) * 16384 > OFF_Z + Z_BYTES ? (D / 64) * 16384
+                                                                     : OFF_Z + Z_BYTES;
+    static constexpr int OFF_MISC = REGION;                // G, beta
+    static constexpr int SMEM = OFF_MISC + 2 * 64 * 4 + 1024;
+    static_assert(16 * 96 * 4 <= Z_BYTES, "solve scratch inside the Z tile");
 };
 
 struct Bars {
@@ -218,12 +238,189 @@ __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int b
     ptx::named_sync(bar, 256);
 }
 
+// ---------------------------------------------------------------------------
+// Chunk transform for head_dim 256: Z = [T; P T] of every (sequence, head,
+// chunk), independent of the state, computed once per chunk (not once per
+// value block) into the workspace.  Persistent CTAs walk the chunks:
+//   1. TMA brings K and Q (stacked per 64-key slab), plain loads the gates;
+//   2. MMA [K;Q] K^T -> TMEM (M = 128, N = 64, K = D): K K^T and Q K^T;
+//   3. CUDA cores: A and P, T = (I + A)^-1 by 16 x 16 blocks, P T, and
+//      Z = [T; P T] as bf16 hi + lo in the swizzled tile layout;
+//   4. one bulk copy writes the 32 KB tile to the workspace.
+template <int D>
+__global__ void __launch_bounds__(NT, 3)
+chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const float *__restrict__ g, const float *__restrict__ beta,
+               uint8_t *__restrict__ zws, int T, int H, int Hk, int n_chunks, int n_tasks,
+               int *status)
+{
+    using ZC = ZCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+    __shared__ Bars bars;
+    float *sG = reinterpret_cast<float *>(sm + ZC::OFF_MISC);
+    float *sBeta = sG + 64;
+    uint8_t *sQK = sm + ZC::OFF_QK;
+    float *sA = reinterpret_cast<float *>(sm + ZC::OFF_A);
+    float *sP = reinterpret_cast<float *>(sm + ZC::OFF_P);
+    float *sW = reinterpret_cast<float *>(sm + ZC::OFF_Z);
+    uint8_t *sZhi = sm + ZC::OFF_Z, *sZlo = sm + ZC::OFF_Z + 16384;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int wg = tid >> 7;
+    const int row = tid & 127;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+
+    if (tid == 0) {
+        bars.abort = 0;
+        ptx::mbar_init(&bars.tma, 1);
+        ptx::mbar_init(&bars.mma, 1);
+        ptx::fence_mbar_init();
+        ptx::prefetch_tmap(&tm_q);
+        ptx::prefetch_tmap(&tm_k);
+    }
+    if (warp == 0) {
+        ptx::tmem_alloc(&bars.tmem_base, 64);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    volatile int *abort_flag = &bars.abort;
+    auto fail = [&]() {
+        if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
+    };
+    const uint32_t aQK = ptx::smem_u32(sQK);
+
+    uint32_t phase = 0;
+    for (int task = blockIdx.x; task < n_tasks && !*abort_flag; task += gridDim.x) {
+        const int c = task % n_chunks;
+        const int bh = task / n_chunks;
+        const int b = bh / H, h = bh - b * H;
+        const int t0 = c * C;
+        const int n = min(C, T - t0);
+
+        // 1. loads
+        if (tid == 0) {
+            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192;
+            ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
+#pragma unroll
+            for (int sl = 0; sl < D / 64; ++sl) {
+                ptx::tma_load_4d(sQK + sl * 16384, &tm_k, &bars.tma, sl * 64, h % Hk, t0, b);
+                ptx::tma_load_4d(sQK + sl * 16384 + 8192, &tm_q, &bars.tma, sl * 64, h % Hk, t0, b);
+            }
+        }
+        if (tid < 64) {
+            const int r = tid;
+            float gr = 0.f, br = 0.f;
+            if (r < n) {
+                const size_t gi = ((size_t)b * T + t0 + r) * H + h;
+                gr = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
+                br = beta[gi];
+            }
+            float sacc = gr;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+                if (lane >= o) sacc += y;
+            }
+            sG[r] = sacc;
+            sBeta[r] = br;
+        }
+        __syncthreads();
+        if (tid >= 32 && tid < 64) sG[tid] += sG[31];
+        if (!ptx::mbar_wait(&bars.tma, phase, abort_flag)) fail();
+        __syncthreads();
+        if (*abort_flag) break;
+
+        // 2. MMA: [K;Q] K^T  (M = 128, N = 64, K = D)
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t a = aQK + (kk >> 2) * 16384 + (kk & 3) * 32;
+                const uint64_t da = ptx::smem_desc(a, 16, 1024);
+                ptx::mma_bf16(tmem, da, da, idesc, kk > 0);
+            }
+            ptx::mma_commit(&bars.mma);
+        }
+        if (!ptx::mbar_wait(&bars.mma, phase, abort_flag)) fail();
+        ptx::tc_fence_after();
+        phase ^= 1;
+
+        // 3. A, P (the [K;Q] bytes are free now: the product has completed)
+        {
+            float kq[32];
+            ptx::tmem_ld16(tmem + lane_off + wg * 32, *reinterpret_cast<float(*)[16]>(kq));
+            ptx::tmem_ld16(tmem + lane_off + wg * 32 + 16, *reinterpret_cast<float(*)[16]>(kq + 16));
+            ptx::tmem_ld_wait();
+            const int r = row & 63;
+            const float Gr = sG[r];
+            if (row < 64) {
+                const float br = sBeta[r];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int i = wg * 32 + j;
+                    sP[r * FST + i] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ut_transform(sA, sW, tid, 0);                 // T in place over A; W dead afterwards
+        {
+            const int r = tid >> 2, c0 = (tid & 3) * 16;
+            float t[16], pt[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                t[e] = sA[r * FST + c0 + e];
+                pt[e] = 0.f;
+            }
+            // (P T)[r][j] = sum_{i=j}^{r} P[r][i] T[i][j]   (T[i][j] = 0 for i < j)
+            for (int i = c0; i <= r; ++i) {
+                const float p = sP[r * FST + i];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sA[i * FST + c0 + e], pt[e]);
+            }
+            store_split16(sZhi, sZlo, r, c0, t);
+            store_split16(sZhi, sZlo, 64 + r, c0, pt);
+        }
+        // 4. the tile to the workspace (one bulk copy), then the buffer is free
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            ptx::bulk_store(zws + (size_t)task * Z_BYTES, sZhi, Z_BYTES);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_read_all();
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+    }
+    if (tid == 0) ptx::bulk_wait_all();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) ptx::tmem_dealloc(tmem, 64);
+}
+
 template <int D>
 __global__ void __launch_bounds__(NT, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
                const float *__restrict__ beta, const float *state_in, float *state_out,
-               float *__restrict__ out, int T, int H, int Hk, float scale, int *status)
+               float *__restrict__ out, const uint8_t *__restrict__ zws, int T, int H, int Hk,
+               float scale, int *status)
 {
     using CF = Cfg<D>;
     constexpr int BV = CF::BV;
@@ -237,9 +434,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float *sBeta = sG + 64;
     float *sGam = sG + 128;
     float *sEnd = sG + 192;
-    float *sA = reinterpret_cast<float *>(sm + CF::OFF_A);
-    float *sP = reinterpret_cast<float *>(sm + CF::OFF_P);
-    float *sW = reinterpret_cast<float *>(sm + CF::OFF_W);
     uint8_t *sQK = sm + CF::OFF_QK;
     uint8_t *sV = sm + CF::OFF_V;
     uint8_t *sZhi = sm + CF::OFF_Z, *sZlo = sm + CF::OFF_Z + 16384;
@@ -252,10 +446,13 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int wg = tid >> 7;                 // warpgroup: which half of the value columns
     const int row = tid & 127;               // TMEM lane this thread reads
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const int bh = blockIdx.x;
+    // the value blocks of one head are neighbours in the grid, so they share
+    // their [K;Q] and Z reads through L2
+    const int bh = blockIdx.x / CF::NVB;
     const int b = bh / H, h = bh - b * H;
-    const int v0 = blockIdx.y * BV;
+    const int v0 = (blockIdx.x % CF::NVB) * BV;
     const int n_chunks = (T + C - 1) / C;
+    const uint8_t *zbh = zws + (size_t)bh * n_chunks * Z_BYTES;
 
     if (tid == 0) {
         bars.abort = 0;
@@ -270,12 +467,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::tmem_alloc(&bars.tmem_base, CF::TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    // zero, for d=64, the second key slab that pads K^T to 128 rows in the
-    // state update
-    if (D == 64)
-        for (int i = tid; i < 16384 / 16; i += NT)
-            reinterpret_cast<uint4 *>(sQK + 16384)[i] = make_uint4(0, 0, 0, 0);
-
     // ---- initial state block into registers: key = kt*128 + row, values
     //      v0 + wg*HALF + j; coalesced over keys
     float S[KT][HALF];
@@ -328,9 +519,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         const int t0 = c * C;
         const int n = min(C, T - t0);
 
-        // ---------------- 1. loads
+        // ---------------- 1. loads: [K;Q], the V block and the chunk's Z tile
         if (tid == 0) {
-            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2;
+            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2 + Z_BYTES;
             ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
 #pragma unroll
             for (int s = 0; s < D / 64; ++s) {
@@ -338,6 +529,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h % Hk, t0, b);
             }
             ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, t0, b);
+            ptx::bulk_load(sZhi, zbh + (size_t)c * Z_BYTES, Z_BYTES, &bars.tma);
         }
         if (tid < 64) {
             const int r = tid;
@@ -367,70 +559,6 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!ptx::mbar_wait(&bars.tma, (uint32_t)(c & 1), abort_flag)) fail();
         __syncthreads();
         if (*abort_flag) break;
-
-        // ---------------- 2. MMA: [K;Q] K^T  (M=128, N=64, K=D)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, false);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t a = aQK + (kk >> 2) * 16384 + (kk & 3) * 32;
-                const uint64_t da = ptx::smem_desc(a, 16, 1024);
-                ptx::mma_bf16(tmem + CF::COL_KQ, da, da, idesc, kk > 0);
-            }
-            ptx::mma_commit(&bars.mma);
-        }
-        wait_mma();
-
-        // ---------------- 3. A, P; T = (I + A)^-1; P T; Z hi / lo
-        {
-            // each thread: TMEM lane `row`, columns wg*32 .. +31
-            float kq[32];
-            ptx::tmem_ld16(tmem + lane_off + CF::COL_KQ + wg * 32, *reinterpret_cast<float(*)[16]>(kq));
-            ptx::tmem_ld16(tmem + lane_off + CF::COL_KQ + wg * 32 + 16,
-                           *reinterpret_cast<float(*)[16]>(kq + 16));
-            ptx::tmem_ld_wait();
-            const int r = row & 63;
-            const float Gr = sG[r];
-            if (row < 64) {
-                const float br = sBeta[r];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = wg * 32 + j;
-                    sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kq[j] : 0.f;
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int i = wg * 32 + j;
-                    sP[r * FST + i] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
-                }
-            }
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
-        // 3a/3b. T = (I + A)^-1 by 16x16 blocks, in place over A
-        ut_transform(sA, sW, tid, 0);
-        // 3c. Z rows: thread -> (row r = tid/4, columns 16*(tid%4) .. +15)
-        {
-            const int r = tid >> 2, c0 = (tid & 3) * 16;
-            float t[16], pt[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                t[e] = sA[r * FST + c0 + e];
-                pt[e] = 0.f;
-            }
-            // (P T)[r][j] = sum_{i=j}^{r} P[r][i] T[i][j]   (T[i][j] = 0 for i < j)
-            for (int i = c0; i <= r; ++i) {
-                const float p = sP[r * FST + i];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sA[i * FST + c0 + e], pt[e]);
-            }
-            store_split16(sZhi, sZlo, r, c0, t);
-            store_split16(sZhi, sZlo, 64 + r, c0, pt);
-        }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
 
         // ---------------- 4. MMA: [K;Q] S^T  (M=128, N=BV, K=D; S as hi + lo)
         if (tid == 0) {
@@ -1256,25 +1384,48 @@ bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
            CUDA_SUCCESS;
 }
 
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
+}
+
+// head_dim 256: the chunk transform for every chunk into the workspace, then
+// the state walk (4 CTAs per head, 64 value rows each) reading it.
 template <int D>
-cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
+cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     using CF = Cfg<D>;
+    using ZC = ZCfg<D>;
+    const int n_chunks = (p.T + C - 1) / C;
+    const long long n_tasks = (long long)p.B * p.H * n_chunks;
+    if (!workspace || ws_bytes < (size_t)n_tasks * Z_BYTES || n_tasks > INT_MAX)
+        return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
     if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
         !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, CF::BV == 64))
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, true))
         return cudaErrorInvalidValue;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(chunked_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        attr_err = cudaFuncSetAttribute(chunk_z_kernel<D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(chunked_kernel<D>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    dim3 grid((unsigned)(p.B * p.H), D / CF::BV);
-    chunked_kernel<D><<<grid, NT, CF::SMEM, stream>>>(mq, mk, mv, p.g, p.beta, p.state_in,
-                                                      p.state_out, p.out, p.T, p.H, p.Hk,
-                                                      p.scale, p.status);
+    uint8_t *zws = static_cast<uint8_t *>(workspace);
+    const long long z_grid = std::min<long long>(n_tasks, 3LL * sm_count());
+    chunk_z_kernel<D><<<(unsigned)z_grid, NT, ZC::SMEM, stream>>>(
+        mq, mk, p.g, p.beta, zws, p.T, p.H, p.Hk, n_chunks, (int)n_tasks, p.status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    chunked_kernel<D><<<(unsigned)(p.B * p.H * CF::NVB), NT, CF::SMEM, stream>>>(
+        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
+        p.status);
     return cudaGetLastError();
 }
 
@@ -1303,14 +1454,21 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
 
 bool chunked_supports(int d) { return d == 64 || d == 128 || d == 256; }
 
-size_t chunked_workspace_bytes(int, int, int, int, int) { return 0; }
+// head_dim 64 / 128 keep every chunk intermediate on chip; head_dim 256
+// keeps one 32 KB transform tile per (sequence, head, chunk) in the workspace.
+size_t chunked_workspace_bytes(int B, int T, int H, int d, int) {
+    if (d != 256 || B <= 0 || T <= 0 || H <= 0) return 0;
+    const size_t n_chunks = ((size_t)T + C - 1) / C;
+    return (size_t)B * (size_t)H * n_chunks * (size_t)Z_BYTES;
+}
 
-cudaError_t launch_chunked(const Problem &p, void *, size_t, cudaStream_t stream) {
+cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
+                           cudaStream_t stream) {
     if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
     switch (p.d) {
         case 64: return launch_ws<64>(p, stream);
         case 128: return launch_ws<128>(p, stream);
-        case 256: return launch_d<256>(p, stream);
+        case 256: return launch_d<256>(p, workspace, ws_bytes, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -81,8 +81,14 @@ def test_workspace_and_path_queries(L):
     assert L.gdn_select_path(1, -1, 1, 128, 1) == gdn.ERR_ARG
     assert L.gdn_select_path(-1, 10, 1, 128, 1) == gdn.ERR_ARG
     assert L.gdn_select_path(1, 10, 1, 128, 5) == gdn.ERR_ARG
-    # the fused chunked kernel keeps everything on chip: no workspace
+    # head_dim 64 / 128: the fused chunked kernel keeps everything on chip
     assert L.gdn_workspace_bytes(8, 16384, 32, 128, 1, 2) == 0
+    assert L.gdn_workspace_bytes(8, 16384, 64, 64, 1, 2) == 0
+    # head_dim 256: one 32 KB chunk-transform tile per (sequence, head, chunk)
+    assert L.gdn_workspace_bytes(8, 16384, 16, 256, 1, 2) == 8 * 16 * 256 * 32768
+    assert L.gdn_workspace_bytes(2, 65, 3, 256, 1, 2) == 2 * 3 * 2 * 32768
+    assert L.gdn_workspace_bytes(1, 4096, 16, 256, 1, 1) == 0      # recurrent path: none
+    assert L.gdn_workspace_bytes(1, 4096, 16, 256, 0, 2) == 0      # chunked is bf16 only
 
 
 # fake, well-aligned device addresses; every call below must fail validation
