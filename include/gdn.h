@@ -75,7 +75,8 @@ enum gdn_status {
     GDN_ERR_WORKSPACE = -7, /* caller workspace NULL, too small or misaligned */
     GDN_ERR_NOMEM = -8,     /* stream-ordered workspace allocation failed */
     GDN_ERR_DTYPE = -9,     /* dtype not supported on the requested path (chunked: bf16 only) */
-    GDN_ERR_SHAPE = -10     /* shape outside the op's scope (flash_attn: 20 or more queries) */
+    GDN_ERR_SHAPE = -10,    /* shape outside the op's scope (flash_attn: 20 or more queries) */
+    GDN_ERR_SCRATCH = -11   /* gdn_forward_noalloc: the call needs more than its fixed scratch */
 };
 
 /* dtype of q, k, v (F16: decode attention only) */
@@ -127,6 +128,34 @@ int gdn_forward_ex(const void *q, const void *k, const void *v,
                    int n_seqs, int n_tokens, int n_heads, int n_k_heads, int head_dim,
                    int dtype, int path, void *workspace, size_t workspace_bytes,
                    gdn_stream_t stream);
+
+/*
+ * gdn_forward_noalloc -- gdn_forward_ex for callers that cannot allocate
+ * device memory while they run (for example a serving framework that has
+ * reserved the whole device for its own arena, or a decode loop that must
+ * not stall on an allocation).  This entry point has no counterpart in the
+ * paper or the model card; it exists only for such callers.
+ *
+ * Same arguments and behaviour as gdn_forward_ex, without the workspace
+ * arguments.  It calls no allocation routine.  The one path that needs
+ * scratch (chunked, head_dim 256: 32 KiB per sequence, head and 64-token
+ * chunk) uses a fixed array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the
+ * library, held by every GPU that loads the library until the process exits.
+ * A call that would need more returns GDN_ERR_SCRATCH before touching the
+ * GPU; gdn_workspace_bytes() tells how much a call needs.
+ * All calls share the array: calls that may overlap on the GPU (different
+ * streams with no ordering) race on it and must not be issued that way.  Its
+ * contents carry over between calls; no call depends on them.
+ * The first call on each device that needs the array looks up its device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (64u << 20)
+int gdn_forward_noalloc(const void *q, const void *k, const void *v,
+                        const float *g, const float *beta, const float *state_in,
+                        float *out, float *state_out,
+                        int n_seqs, int n_tokens, int n_heads, int n_k_heads, int head_dim,
+                        int dtype, int path, gdn_stream_t stream);
 
 /* Bytes of device workspace gdn_forward_ex needs for these sizes, dtype and
  * path (0 when the selected path needs none).  Returns 0 on invalid sizes. */

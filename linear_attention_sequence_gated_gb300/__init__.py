@@ -27,14 +27,14 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 OK = 0
 ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE, ERR_NOMEM, \
-    ERR_DTYPE, ERR_SHAPE = -1, -2, -3, -4, -5, -6, -7, -8, -9, -10
+    ERR_DTYPE, ERR_SHAPE, ERR_SCRATCH = -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -11
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
            "gdn_select_path", "gdn_supports", "gdn_get_device_status", "gdn_status_string",
-           "gdn_version", "gdn_flash_attn", "gdn_flash_attn_supports"]
+           "gdn_version", "gdn_flash_attn", "gdn_flash_attn_supports", "gdn_forward_noalloc"]
 
 _lib = None
 
@@ -76,6 +76,8 @@ def lib():
         L.gdn_flash_attn.restype = i
         L.gdn_flash_attn_supports.argtypes = [i, i, i]
         L.gdn_flash_attn_supports.restype = i
+        L.gdn_forward_noalloc.argtypes = fwd[:11] + [i, i, i, i, vp]
+        L.gdn_forward_noalloc.restype = i
         _lib = L
     return _lib
 

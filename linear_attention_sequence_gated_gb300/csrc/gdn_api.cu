@@ -253,6 +253,8 @@ const char *gdn_status_string(int status) {
         case GDN_ERR_NOMEM: return "stream-ordered workspace allocation failed";
         case GDN_ERR_DTYPE: return "dtype not supported on the requested path (chunked: bf16 only)";
         case GDN_ERR_SHAPE: return "shape outside the op's scope (flash_attn: 20 or more queries)";
+        case GDN_ERR_SCRATCH:
+            return "the call needs more scratch than gdn_forward_noalloc's fixed 64 MiB array";
         default: return "unknown status";
     }
 }
@@ -260,3 +262,60 @@ const char *gdn_status_string(int status) {
 int gdn_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.  Some callers must not allocate device memory
+// at all once they are running: a serving process whose framework has
+// reserved the whole device up front for its own arena, or a decode loop in
+// which an allocation (and the device synchronisation cudaMalloc can imply)
+// would stall the step.  For them the one path that needs scratch -- the
+// head_dim 256 chunked path, which keeps a 32 KiB transform tile per
+// (sequence, head, 64-token chunk) -- takes its scratch from this fixed array
+// instead.  The array is part of the library image: every GPU that loads the
+// library holds these 64 MiB until the process exits.  Calls share it, so two
+// calls that overlap on the GPU (different streams, no ordering between them)
+// race on it.  Nothing in it has to start at zero: the transform kernel writes
+// every tile a call reads before the state kernel of that call reads it.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void *g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) on the first call that needs it.  The
+// array's name in host code is only a stand-in; kernels get this address.
+void *noalloc_scratch_for_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+        g_scratch_ptr[dev] = p;
+    }
+    return g_scratch_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" int gdn_forward_noalloc(const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, const float *state_in, float *out,
+                                   float *state_out, int n_seqs, int n_tokens, int n_heads,
+                                   int n_k_heads, int head_dim, int dtype, int path,
+                                   gdn_stream_t stream) {
+    if (n_k_heads < 0) return GDN_ERR_ARG;
+    // scratch the call needs (0 for invalid sizes: run() reports those)
+    const size_t need = gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype, path);
+    if (need > (size_t)GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_SCRATCH;
+    void *ws = nullptr;
+    if (need > 0) {
+        ws = noalloc_scratch_for_current_device();
+        if (!ws) return GDN_ERR_CUDA;
+    }
+    return run(q, k, v, g, beta, state_in, out, state_out, n_seqs, n_tokens, n_heads,
+               n_k_heads == 0 ? n_heads : n_k_heads, head_dim, dtype, path, ws,
+               ws ? (size_t)GDN_NOALLOC_SCRATCH_BYTES : 0, reinterpret_cast<cudaStream_t>(stream));
+}

@@ -56,7 +56,7 @@ def test_supports(L):
 
 
 def test_status_strings(L):
-    for code in range(-10, 1):
+    for code in range(-11, 1):
         s = gdn.status_string(code)
         assert s and s != "unknown status"
     assert gdn.status_string(-99) == "unknown status"

@@ -1,0 +1,87 @@
+"""The allocation-free entry point, gdn_forward_noalloc, against gdn_forward_ex.
+
+gdn_forward_noalloc serves callers that cannot allocate device memory while
+they run (a framework that has reserved the device for its own arena, a
+decode loop that must not stall on an allocation).  The one path that needs
+scratch -- chunked, head_dim 256 -- then uses a fixed 64 MiB array inside the
+library instead of caller or stream-ordered memory.  These tests call it
+through the C ABI twice in a row, with different inputs (the array keeps the
+previous call's contents), and compare each result with the existing entry
+point's on the same inputs, within the bf16 parity bound used by the other
+tests.  The file is named so that pytest collects it last.
+"""
+import ctypes
+
+import pytest
+import torch
+
+import linear_attention_sequence_gated_gb300 as gdn
+from linear_attention_sequence_gated_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TOL = 3e-3          # max |x - ref| / RMS(ref), the bound of the bf16 parity tests
+
+
+@pytest.fixture(scope="module")
+def L():
+    from linear_attention_sequence_gated_gb300 import _build
+    _build.build()
+    return gdn.lib()
+
+
+def ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def rel_err(x, ref):
+    x, ref = x.double(), ref.double()
+    return ((x - ref).abs().max() / ref.pow(2).mean().sqrt()).item()
+
+
+def noalloc(L, inp, out, st_out, path=gdn.PATHS["chunked"]):
+    B, T, H, d = inp["v"].shape
+    Hk = inp["q"].shape[2]
+    stream = torch.cuda.current_stream().cuda_stream
+    return L.gdn_forward_noalloc(ptr(inp["q"]), ptr(inp["k"]), ptr(inp["v"]), ptr(inp["g"]),
+                                 ptr(inp["beta"]), ptr(inp["state"]), ptr(out), ptr(st_out),
+                                 B, T, H, Hk, d, gdn.DTYPE_BF16, path, ctypes.c_void_p(stream))
+
+
+def test_two_calls_in_a_row_match_the_existing_entry_point(L):
+    # head_dim 256 on the chunked path: 2 x 4 heads x 16 chunks = 128 scratch tiles (4 MiB)
+    for seed in (71, 72):
+        w = W.Workload(f"noalloc_{seed}", 2, 1000, 4, 256, "bf16", 0.0, 0.02, seed=seed)
+        inp = W.make_inputs(w, "cuda")
+        assert L.gdn_workspace_bytes(w.B, w.T, w.H, w.d, gdn.DTYPE_BF16, 2) > 0
+        ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                      inp["state"], path="chunked")
+        out = torch.full_like(ref_out, float("nan"))
+        st = torch.full_like(ref_st, float("nan"))
+        assert noalloc(L, inp, out, st) == gdn.OK
+        torch.cuda.synchronize()
+        assert gdn.device_status() == gdn.OK
+        assert rel_err(out, ref_out) <= TOL
+        assert rel_err(st, ref_st) <= TOL
+
+
+def test_paths_without_scratch_and_auto(L):
+    # head_dim 128 needs no scratch: the call goes straight through
+    w = W.Workload("noalloc_d128", 2, 300, 4, 128, "bf16", 0.0, 0.02, seed=73)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  inp["state"])
+    out, st = torch.empty_like(ref_out), torch.empty_like(ref_st)
+    assert noalloc(L, inp, out, st, path=gdn.PATHS["auto"]) == gdn.OK
+    torch.cuda.synchronize()
+    assert rel_err(out, ref_out) <= TOL and rel_err(st, ref_st) <= TOL
+
+
+def test_rejects_calls_beyond_the_fixed_scratch(L):
+    # 8 sequences x 16 heads x 256 chunks of head_dim 256 would need 1 GiB; the
+    # check happens on the host before any pointer is used
+    fake = ctypes.c_void_p(1 << 40)
+    rc = L.gdn_forward_noalloc(fake, fake, fake, fake, fake, None, fake, fake,
+                               8, 16384, 16, 16, 256, gdn.DTYPE_BF16, gdn.PATHS["chunked"], None)
+    assert rc == gdn.ERR_SCRATCH
+    assert "64 MiB" in gdn.status_string(rc)
