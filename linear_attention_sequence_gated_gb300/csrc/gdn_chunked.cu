@@ -297,6 +297,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t aQK = ptx::smem_u32(sQK);
 
     uint32_t phase = 0;
+    bool tma_pending = false;                         // thread 0: a load not yet waited for
     for (int task = blockIdx.x; task < n_tasks && !*abort_flag; task += gridDim.x) {
         const int c = task % n_chunks;
         const int bh = task / n_chunks;
@@ -308,6 +309,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (tid == 0) {
             constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192;
             ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
+            tma_pending = true;
 #pragma unroll
             for (int sl = 0; sl < D / 64; ++sl) {
                 ptx::tma_load_4d(sQK + sl * 16384, &tm_k, &bars.tma, sl * 64, h % Hk, t0, b);
@@ -334,6 +336,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __syncthreads();
         if (tid >= 32 && tid < 64) sG[tid] += sG[31];
         if (!ptx::mbar_wait(&bars.tma, phase, abort_flag)) fail();
+        else if (tid == 0) tma_pending = false;
         __syncthreads();
         if (*abort_flag) break;
 
@@ -408,7 +411,13 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         __syncthreads();
         ptx::tc_fence_after();
     }
-    if (tid == 0) ptx::bulk_wait_all();
+    if (tid == 0) {
+        ptx::bulk_wait_all();
+        if (tma_pending) {                            // after an abort: let the load land
+            const volatile int never = 0;
+            ptx::mbar_wait(&bars.tma, phase, &never, 1000000000LL);
+        }
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, 64);
@@ -515,22 +524,42 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const uint32_t aQK = ptx::smem_u32(sQK);
     const size_t tok_stride = (size_t)H * D;
 
+    // Loads of chunk c (thread 0).  Each buffer is refilled for the next chunk
+    // as soon as this chunk is done with it: V after R, Z after the Z R
+    // product, [K;Q] after the state-update product; all three land on the
+    // one transaction barrier of that chunk, armed with the first issue.
+    auto load_v = [&](int cc) {
+        constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2 + Z_BYTES;
+        ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
+        ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, cc * C, b);
+    };
+    auto load_z = [&](int cc) {
+        ptx::bulk_load(sZhi, zbh + (size_t)cc * Z_BYTES, Z_BYTES, &bars.tma);
+    };
+    auto load_qk = [&](int cc) {
+#pragma unroll
+        for (int s = 0; s < D / 64; ++s) {
+            ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h % Hk, cc * C, b);
+            ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h % Hk, cc * C, b);
+        }
+    };
+    // thread 0 tracks the chunk whose loads are armed but not yet waited for
+    // (and which of its three loads were issued), to drain them on abort
+    int armed = -1, issued = 0;
+    if (tid == 0 && n_chunks > 0) {
+        load_v(0);
+        load_z(0);
+        load_qk(0);
+        armed = 0;
+        issued = 7;
+    }
+
     for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
         const int t0 = c * C;
         const int n = min(C, T - t0);
+        const bool more = c + 1 < n_chunks;
 
-        // ---------------- 1. loads: [K;Q], the V block and the chunk's Z tile
-        if (tid == 0) {
-            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2 + Z_BYTES;
-            ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
-#pragma unroll
-            for (int s = 0; s < D / 64; ++s) {
-                ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h % Hk, t0, b);
-                ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h % Hk, t0, b);
-            }
-            ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, t0, b);
-            ptx::bulk_load(sZhi, zbh + (size_t)c * Z_BYTES, Z_BYTES, &bars.tma);
-        }
+        // ---------------- 1. gates (the chunk's tiles were issued earlier)
         if (tid < 64) {
             const int r = tid;
             float gr = 0.f, br = 0.f;
@@ -557,6 +586,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             sEnd[tid] = fast_exp(sG[63] - sG[tid]);
         }
         if (!ptx::mbar_wait(&bars.tma, (uint32_t)(c & 1), abort_flag)) fail();
+        else if (tid == 0) armed = -1;
         __syncthreads();
         if (*abort_flag) break;
 
@@ -616,6 +646,11 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::fence_proxy_async_smem();
         ptx::tc_fence_before();
         __syncthreads();
+        if (tid == 0 && more) {                       // V of this chunk has been read
+            load_v(c + 1);
+            armed = c + 1;
+            issued = 1;
+        }
 
         // ---------------- 6. MMA: Z R  (M=128, N=BV, K=64; hi*hi + hi*lo + lo*hi)
         if (tid == 0) {
@@ -635,6 +670,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mma_commit(&bars.mma);
         }
         wait_mma();
+        if (tid == 0 && more) {                       // the Z R product has read Z
+            load_z(c + 1);
+            issued |= 2;
+        }
 
         // ---------------- 7. O (lanes 64-127) and U~ hi / lo (lanes 0-63)
         {
@@ -698,6 +737,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::mma_commit(&bars.mma);
         }
         wait_mma();
+        if (tid == 0 && more) {                       // both products have read [K;Q]
+            load_qk(c + 1);
+            issued |= 4;
+        }
 
         // ---------------- 9. S = gamma_C S + dS^T; S hi / lo for the next chunk
         {
@@ -743,6 +786,15 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
         }
+    }
+    // after an abort: let the copies still addressed to this CTA's shared
+    // memory land (issuing any of the armed chunk's loads not yet issued, so
+    // that its byte count can complete), within a bounded wait
+    if (tid == 0 && armed >= 0) {
+        if (!(issued & 2)) load_z(armed);
+        if (!(issued & 4)) load_qk(armed);
+        const volatile int never = 0;
+        ptx::mbar_wait(&bars.tma, (uint32_t)(armed & 1), &never, 1000000000LL);
     }
     ptx::tc_fence_before();
     __syncthreads();
