@@ -11,16 +11,19 @@
 // the kernel is bound by HBM and by latency, not by arithmetic.  Mapping on
 // sm_103a:
 //   * the R = (n_heads / n_heads_kv) * n_q rows of one kv head are cut into
-//     row groups of RG rows; one thread-block cluster of CL <= 8 CTAs serves
+//     row groups of RG rows; one thread-block cluster of CL <= 16 CTAs serves
 //     (sequence, kv head, row block), and the cluster's CL x (warps per row
-//     group) warps split the keys into contiguous ranges;
-//   * a warp streams its keys eight at a time through its own ring of
-//     shared-memory stages filled by asynchronous copies (two steps of k and v
-//     in flight while one is computed, no block barrier), lanes splitting
-//     head_dim, and keeps its own online softmax (running max, sum of exp,
-//     output slice) per row;
-//   * the eight keys' partial dot products are reduced across the warp by a
-//     transposing butterfly (about one shuffle per key and row);
+//     group) warps split the keys into contiguous ranges; CL grows when there
+//     are few (sequence, kv head) pairs to fill the GPU with;
+//   * a warp streams its keys through its own two-stage ring of shared
+//     memory filled by asynchronous copies (the next step's k and v land while
+//     this one is computed; no block barrier), and keeps its own online
+//     softmax (running max, sum of exp, output slice) per row;
+//   * scores: each lane (head_dim/64 lanes per key) reads its key's k row
+//     across the padded stage (one bank group per lane) against the CTA's
+//     q rows, which are broadcast from shared memory; P V: each lane owns
+//     head_dim/32 value columns and reads the step's probabilities as one
+//     128-bit load per key; both accumulate with packed fp32 FMAs;
 //   * at the end the warps of a CTA merge through shared memory and the CTAs
 //     of the cluster through distributed shared memory, so no partial result
 //     goes through global scratch.
@@ -41,8 +44,7 @@ namespace gdn {
 namespace attn {
 namespace {
 
-constexpr int KG = 8;           // keys per step of a warp
-constexpr int MAX_CLUSTER = 8;  // portable cluster size
+constexpr int MAX_CLUSTER = 16; // largest cluster the merge handles (non-portable size)
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src) {
     const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
@@ -129,38 +131,91 @@ __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
 
-// Geometry for head_dim D and input type Tin.  A warp keeps RG rows' query
-// slice, output slice and one step's partial dot products in registers; its
-// ring holds ST steps of KG keys of k and v.  Eight warps and three stages
-// unless that ring would not fit, then four warps and two stages.
+// Packed fp32 FMA on two lanes of a 64-bit register pair (sm_100 family):
+// d = a * b + c element by element, each rounded as fmaf rounds it.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// 8 consecutive elements of a row in shared memory, as fp32
+__device__ __forceinline__ void lds8(const float *p, float (&x)[8]) {
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    const float4 b = *reinterpret_cast<const float4 *>(p + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void lds8(const __nv_bfloat16 *p, float (&x)[8]) {
+    Slice<__nv_bfloat16, 8> s;
+    ld_slice<false>(s, p);
+    unpack(s, x);
+}
+__device__ __forceinline__ void lds8(const __half *p, float (&x)[8]) {
+    Slice<__half, 8> s;
+    ld_slice<false>(s, p);
+    unpack(s, x);
+}
+// 8 consecutive elements of q in global memory, as fp32
+template <typename Tin>
+__device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
+    if constexpr (sizeof(Tin) == 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+        Slice<Tin, 8> s;
+        ld_slice<true>(s, p);
+        unpack(s, x);
+    }
+}
+
+// Geometry for head_dim D and input type Tin.
+//   scores: KPL = D/64 lanes share a key (each a DQ = 64-element part of its
+//           row), so a step holds NKS = 32/KPL keys, one per lane group;
+//   P V:    every lane owns SL = D/32 consecutive value columns;
+//   a warp carries RG = 4 rows (query head of the group x query).
+// A warp's ring holds ST steps of NKS keys of k (rows padded by 16 bytes, so
+// that lanes reading different rows hit different banks) and v.
 template <int D, typename Tin> struct Geo {
     static constexpr int ELT = (int)sizeof(Tin);
-    static constexpr int SL = D / 32;                 // elements of a row per lane
-    static constexpr int RG = D == 256 ? 2 : 4;       // rows per warp
-    static constexpr int STEP = KG * 2 * D * ELT;     // bytes of one step: k rows, then v rows
-    static constexpr bool BIG = 8 * 3 * STEP > 200 * 1024;
-    static constexpr int NW = BIG ? 4 : 8;            // warps per CTA
-    static constexpr int ST = BIG ? 2 : 3;            // ring stages per warp
+    static constexpr int KPL = D / 64;
+    static constexpr int NKS = 32 / KPL;
+    static constexpr int DQ = D / KPL;
+    static constexpr int SL = D / 32;
+    static constexpr int RG = 4;
+    static constexpr int KST = D * ELT + 16;
+    static constexpr int VST = D * ELT;
+    static constexpr int STEP = NKS * (KST + VST);
+    static constexpr int NW = ELT == 4 ? 4 : 8;       // warps per CTA
+    static constexpr int ST = 2;                      // ring stages per warp
     static constexpr int NTHR = NW * 32;
     static constexpr int RING = NW * ST * STEP;
     // after the key loop the ring is reused for the merge buffers
     static constexpr int WO = 0;                                  // [NW][RG][D] fp32
     static constexpr int CO = WO + NW * RG * D * 4;               // [NW*RG][D] fp32
-    static constexpr int SMEM = RING > CO + NW * RG * D * 4 ? RING : CO + NW * RG * D * 4;
+    static constexpr int MERGE = CO + NW * RG * D * 4;
+    static constexpr int QOFF = RING > MERGE ? RING : MERGE;      // the CTA's q rows, fp32
+    static constexpr int SMEM = QOFF + NW * RG * D * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory");
-    static constexpr int MIN_CTAS = SMEM <= 110 * 1024 ? 2 : 1;   // CTAs an SM should hold
+    static_assert(KST % 16 == 0 && STEP % 16 == 0 && QOFF % 16 == 0, "alignment");
 };
 
 // Small per-CTA state outside the ring.
-template <int NW, int RG>
+template <int NW, int RG, int NKS>
 struct SmallSmem {
     float wm[NW][RG], wl[NW][RG];                     // each warp's partial max, sum per row
     float cm[NW * RG], cl[NW * RG];                   // the CTA's partial per local row
-    float p[NW][RG][KG];                              // a step's probabilities, per warp
+    float p[NW][NKS][RG];                             // a step's probabilities, [key][row]
 };
 
 template <int D, typename Tin>
-__global__ void __launch_bounds__(Geo<D, Tin>::NTHR, Geo<D, Tin>::MIN_CTAS)
+__global__ void __launch_bounds__(Geo<D, Tin>::NTHR, 1)
 attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const Tin *__restrict__ mask,
                    float *__restrict__ out, int H, int Hkv, int n_q, int n_kv, int n_rb, int n_rgc,
@@ -168,11 +223,12 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 {
     using G = Geo<D, Tin>;
     constexpr int SL = G::SL, RG = G::RG, NW = G::NW, ST = G::ST, NTHR = G::NTHR;
-    constexpr int NWARP = NW;
+    constexpr int NKS = G::NKS, DQ = G::DQ;
     extern __shared__ __align__(16) uint8_t ring[];
-    __shared__ SmallSmem<NW, RG> sm;
+    __shared__ __align__(16) SmallSmem<NW, RG, NKS> sm;
     float (*wo)[RG][D] = reinterpret_cast<float (*)[RG][D]>(ring + G::WO);
     float (*co)[D] = reinterpret_cast<float (*)[D]>(ring + G::CO);
+    float *sQ = reinterpret_cast<float *>(ring + G::QOFF);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     uint32_t rank_u;
@@ -184,64 +240,41 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const int b = bhk / Hkv, hk = bhk - b * Hkv;
     const int rep = H / Hkv;
     const int R = rep * n_q;                          // rows (query head, query) of this kv head
-    const int n_ksc = NWARP / n_rgc;                  // warps per row group in a CTA
+    const int n_ksc = NW / n_rgc;                     // warps per row group in a CTA
     const int rgc = warp % n_rgc;                     // this warp's row group in the CTA
     const int ksw = warp / n_rgc;                     // this warp's key split in the CTA
     const int rows_cta = n_rgc * RG;
-    const int r0 = rb * rows_cta + rgc * RG;          // first row of this warp
+    const int rbase = rb * rows_cta;
+    const int r0 = rbase + rgc * RG;                  // first row of this warp
     const int nr = max(0, min(RG, R - r0));
 
-    // key range of this warp: split s of S = CL * n_ksc, in steps of KG
+    // key range of this warp: split s of S = CL * n_ksc, in steps of NKS keys
     const int S = CL * n_ksc;
     const int s = rank * n_ksc + ksw;
-    const int n_steps_all = (n_kv + KG - 1) / KG;
+    const int n_steps_all = (n_kv + NKS - 1) / NKS;
     const int sps = (n_steps_all + S - 1) / S;
-    const int kb = min(n_kv, s * sps * KG);
-    const int ke = min(n_kv, kb + sps * KG);
-
-    // this lane's slice of the warp's rows of q, scaled, fp32
-    float qv[RG][SL];
-#pragma unroll
-    for (int r = 0; r < RG; ++r) {
-        if (r < nr) {
-            const int rg = r0 + r;                    // head hk*rep + rg / n_q, query rg % n_q
-            Slice<Tin, SL> raw;
-            ld_slice<true>(raw, q + ((size_t)(b * H + hk * rep) * n_q + rg) * D + lane * SL);
-            unpack(raw, qv[r]);
-#pragma unroll
-            for (int e = 0; e < SL; ++e) qv[r][e] *= scale;
-        } else {
-#pragma unroll
-            for (int e = 0; e < SL; ++e) qv[r][e] = 0.f;
-        }
-    }
-    float m[RG], l[RG], acc[RG][SL];
-#pragma unroll
-    for (int r = 0; r < RG; ++r) {
-        m[r] = -INFINITY;
-        l[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < SL; ++e) acc[r][e] = 0.f;
-    }
+    const int kb = min(n_kv, s * sps * NKS);
+    const int ke = min(n_kv, kb + sps * NKS);
+    const int n_steps = nr > 0 ? (ke - kb + NKS - 1) / NKS : 0;
 
     const Tin *kg = k + (size_t)(b * Hkv + hk) * n_kv * D;
     const Tin *vg = v + (size_t)(b * Hkv + hk) * n_kv * D;
     uint8_t *wring = ring + warp * ST * G::STEP;
-    const int n_steps = nr > 0 ? (ke - kb + KG - 1) / KG : 0;
-    // stage `st` <- keys kb + KG*step .. (k rows, then v rows); rows past the
-    // range are not copied (their scores are masked, their v rows skipped)
+    // stage `st` <- keys kb + NKS*step ..: k rows (padded), then v rows; rows
+    // past the range are not copied (their scores are masked, their v rows skipped)
     auto issue = [&](int step, int st) {
         if (step < n_steps) {
-            const int j0 = kb + step * KG;
-            const int nk = min(KG, ke - j0);
+            const int j0 = kb + step * NKS;
+            const int nk = min(NKS, ke - j0);
             constexpr int CPR = D * G::ELT / 16;      // 16-byte copies per row
-            uint8_t *dst = wring + st * G::STEP;
-            for (int c = lane; c < KG * CPR; c += 32) {
+            uint8_t *dk = wring + st * G::STEP;
+            uint8_t *dv = dk + NKS * G::KST;
+            for (int c = lane; c < NKS * CPR; c += 32) {
                 const int g = c / CPR, x = c - g * CPR;
                 if (g < nk) {
-                    cp_async16(dst + g * D * G::ELT + x * 16,
+                    cp_async16(dk + g * G::KST + x * 16,
                                reinterpret_cast<const uint8_t *>(kg + (size_t)(j0 + g) * D) + x * 16);
-                    cp_async16(dst + (KG + g) * D * G::ELT + x * 16,
+                    cp_async16(dv + g * G::VST + x * 16,
                                reinterpret_cast<const uint8_t *>(vg + (size_t)(j0 + g) * D) + x * 16);
                 }
             }
@@ -251,107 +284,137 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int i = 0; i < ST - 1; ++i) issue(i, i);
 
+    // the CTA's rows of q, scaled, fp32 (rows past R: zeros); rows rbase + lr
+    // are consecutive in q: head hk*rep + row / n_q, query row % n_q
+    for (int i = tid; i < rows_cta * (D / 8); i += NTHR) {
+        const int lr = i / (D / 8), c = i - lr * (D / 8);
+        const int rg = rbase + lr;
+        float x[8];
+        if (rg < R) {
+            ldg8(q + ((size_t)(b * H + hk * rep) * n_q + rg) * D + c * 8, x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
+        float4 *dst = reinterpret_cast<float4 *>(sQ + lr * D + c * 8);
+        dst[0] = make_float4(scale * x[0], scale * x[1], scale * x[2], scale * x[3]);
+        dst[1] = make_float4(scale * x[4], scale * x[5], scale * x[6], scale * x[7]);
+    }
+    __syncthreads();
+
+    float m[RG], l[RG];
+    float2 acc[RG][SL / 2];
+#pragma unroll
+    for (int r = 0; r < RG; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int e = 0; e < SL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
+    }
+    const int key = lane % NKS, part = lane / NKS;    // score pass: this lane's key and row part
+    const float *qw = sQ + (rgc * RG) * D + part * DQ;
+
     for (int step = 0; step < n_steps; ++step) {
         cp_async_wait<ST - 2>();                      // this step's copies (own lane) landed
         __syncwarp();                                 // ... and every lane's
-        const int j0 = kb + step * KG;
-        const int nk = min(KG, ke - j0);
-        const Tin *sk = reinterpret_cast<const Tin *>(wring + (step % ST) * G::STEP);
-        const Tin *sv = sk + KG * D;
-        Slice<Tin, SL> kr[KG];
+        // refill the stage the previous step used (every lane passed the
+        // __syncwarp after reading it) while this step is computed
+        issue(step + ST - 1, (step + ST - 1) % ST);
+        const int j0 = kb + step * NKS;
+        const int nk = min(NKS, ke - j0);
+        const uint8_t *sk = wring + (step % ST) * G::STEP;
+        const Tin *sv = reinterpret_cast<const Tin *>(sk + NKS * G::KST);
+
+        // ---- scores: q . k over this lane's part of its key's row
+        float2 a2[RG];
 #pragma unroll
-        for (int g = 0; g < KG; ++g) ld_slice<false>(kr[g], sk + g * D + lane * SL);
-        // partial dot products of this lane's slice: part[r][g]
-        float part[RG][KG];
-#pragma unroll
-        for (int g = 0; g < KG; ++g) {
-            float kx[SL];
-            unpack(kr[g], kx);
+        for (int r = 0; r < RG; ++r) a2[r] = make_float2(0.f, 0.f);
+        const Tin *krow = reinterpret_cast<const Tin *>(sk + key * G::KST) + part * DQ;
+#pragma unroll 4
+        for (int c = 0; c < DQ / 8; ++c) {
+            float kx[8];
+            lds8(krow + c * 8, kx);
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
-                float a = 0.f;
+                float qx[8];
+                lds8(qw + r * D + c * 8, qx);
 #pragma unroll
-                for (int e = 0; e < SL; ++e) a = fmaf(qv[r][e], kx[e], a);
-                part[r][g] = a;
+                for (int e = 0; e < 8; e += 2)
+                    a2[r] = ffma2(make_float2(qx[e], qx[e + 1]), make_float2(kx[e], kx[e + 1]),
+                                  a2[r]);
             }
         }
-        // transposing butterfly: after the xor-16/8/4 steps lane holds the sum
-        // over its 8-lane class for key kidx; xor-2/1 finish the sum over all 32
+        // ---- online softmax over the step's keys, all RG rows side by side
+        //      (rows past the warp's valid rows are masked out, not branched
+        //      around, so each reduction level issues RG independent shuffles)
+        float sc[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) sc[r] = a2[r].x + a2[r].y;
+#pragma unroll
+        for (int off = NKS; off < 32; off <<= 1)
+#pragma unroll
+            for (int r = 0; r < RG; ++r) sc[r] += __shfl_xor_sync(0xffffffffu, sc[r], off);
 #pragma unroll
         for (int r = 0; r < RG; ++r) {
-            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-            float h4[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                // keys i (bit 2 of key = 0 half) vs i + 4: keep own half
-                const float keep = b4 ? part[r][i + 4] : part[r][i];
-                const float send = b4 ? part[r][i] : part[r][i + 4];
-                h4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-            float h2[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const float keep = b3 ? h4[i + 2] : h4[i];
-                const float send = b3 ? h4[i] : h4[i + 2];
-                h2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            float h1;
-            {
-                const float keep = b2 ? h2[1] : h2[0];
-                const float send = b2 ? h2[0] : h2[1];
-                h1 = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-            }
-            h1 += __shfl_xor_sync(0xffffffffu, h1, 2);
-            h1 += __shfl_xor_sync(0xffffffffu, h1, 1);
-            // h1 is the score of key (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0)
-            const int key = (b4 ? 4 : 0) + (b3 ? 2 : 0) + (b2 ? 1 : 0);
-            float sc = h1;
-            if (key < nk) {
+            if (r < nr && key < nk) {
                 if (mask) {
                     const int i = (r0 + r) % n_q;
-                    sc += to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]);
+                    sc[r] += to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]);
                 }
             } else {
-                sc = -INFINITY;
+                sc[r] = -INFINITY;
             }
-            float gm = sc;
-            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 4));
-            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 8));
-            gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 16));
-            const float m_new = fmaxf(m[r], gm);
-            const bool none = (m_new == -INFINITY);
-            const float p = none ? 0.f : expf(sc - m_new);
-            float ps = p;
-            ps += __shfl_xor_sync(0xffffffffu, ps, 4);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-            ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-            const float c = none ? 1.f : expf(m[r] - m_new);
-            m[r] = m_new;
-            l[r] = fmaf(l[r], c, ps);
-#pragma unroll
-            for (int e = 0; e < SL; ++e) acc[r][e] *= c;
-            if ((lane & 3) == 0) sm.p[warp][r][key] = p;
         }
+        float gm[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) gm[r] = sc[r];
+#pragma unroll
+        for (int off = 1; off < NKS; off <<= 1)
+#pragma unroll
+            for (int r = 0; r < RG; ++r) gm[r] = fmaxf(gm[r], __shfl_xor_sync(0xffffffffu, gm[r], off));
+        float pv[RG], ps[RG], cf[RG];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            const float m_new = fmaxf(m[r], gm[r]);
+            const bool none = (m_new == -INFINITY);
+            pv[r] = none ? 0.f : expf(sc[r] - m_new);
+            cf[r] = none ? 1.f : expf(m[r] - m_new);
+            m[r] = m_new;
+            ps[r] = pv[r];
+        }
+#pragma unroll
+        for (int off = 1; off < NKS; off <<= 1)
+#pragma unroll
+            for (int r = 0; r < RG; ++r) ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], off);
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            l[r] = fmaf(l[r], cf[r], ps[r]);
+#pragma unroll
+            for (int e = 0; e < SL / 2; ++e)
+                acc[r][e] = make_float2(acc[r][e].x * cf[r], acc[r][e].y * cf[r]);
+        }
+        static_assert(RG == 4, "one 128-bit store of the probabilities per key");
+        if (part == 0)
+            *reinterpret_cast<float4 *>(&sm.p[warp][key][0]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
         __syncwarp();
-        // P V on this lane's slice (keys past the range are skipped: their
-        // stage rows hold stale data)
+        // ---- P V on this lane's value columns (keys past the range skipped:
+        //      their stage rows hold stale data)
+#pragma unroll 2
+        for (int g = 0; g < nk; ++g) {
+            Slice<Tin, SL> vr;
+            ld_slice<false>(vr, sv + g * D + lane * SL);
+            float vx[SL];
+            unpack(vr, vx);
+            const float4 p4 = *reinterpret_cast<const float4 *>(&sm.p[warp][g][0]);
+            const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
 #pragma unroll
-        for (int g = 0; g < KG; ++g) {
-            if (g < nk) {
-                Slice<Tin, SL> vr;
-                ld_slice<false>(vr, sv + g * D + lane * SL);
-                float vx[SL];
-                unpack(vr, vx);
+            for (int r = 0; r < RG; ++r)
 #pragma unroll
-                for (int r = 0; r < RG; ++r) {
-                    const float p = sm.p[warp][r][g];
-#pragma unroll
-                    for (int e = 0; e < SL; ++e) acc[r][e] = fmaf(p, vx[e], acc[r][e]);
-                }
-            }
+                for (int e = 0; e < SL / 2; ++e)
+                    acc[r][e] = ffma2(make_float2(pr[r], pr[r]), make_float2(vx[2 * e], vx[2 * e + 1]),
+                                      acc[r][e]);
         }
         __syncwarp();                                 // stage and probabilities consumed
-        issue(step + ST - 1, (step + ST - 1) % ST);
     }
     cp_async_wait<0>();
     __syncthreads();                                  // every warp is done with the ring
@@ -361,18 +424,20 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     for (int r = 0; r < RG; ++r) {
         if (lane == 0) { sm.wm[warp][r] = m[r]; sm.wl[warp][r] = l[r]; }
 #pragma unroll
-        for (int e = 0; e < SL; ++e) wo[warp][r][lane * SL + e] = acc[r][e];
+        for (int e = 0; e < SL / 2; ++e) {
+            wo[warp][r][lane * SL + 2 * e] = acc[r][e].x;
+            wo[warp][r][lane * SL + 2 * e + 1] = acc[r][e].y;
+        }
     }
     __syncthreads();
-    // CTA partial for local row lr = rgc * RG + r: merge warps ksw' * n_rgc + rgc
     for (int it = tid; it < rows_cta * D; it += NTHR) {
         const int lr = it / D, col = it - lr * D;
         const int g = lr / RG, r = lr - g * RG;
         float M = -INFINITY;
-        for (int w = g; w < NWARP; w += n_rgc) M = fmaxf(M, sm.wm[w][r]);
+        for (int w = g; w < NW; w += n_rgc) M = fmaxf(M, sm.wm[w][r]);
         float L = 0.f, o = 0.f;
         if (M != -INFINITY) {
-            for (int w = g; w < NWARP; w += n_rgc) {
+            for (int w = g; w < NW; w += n_rgc) {
                 const float mw = sm.wm[w][r];
                 if (mw != -INFINITY) {
                     const float wt = expf(mw - M);
@@ -386,7 +451,6 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
     // ---- merge the CTAs of the cluster (same rows, different keys)
     cluster_sync();
-    const int rbase = rb * rows_cta;
     const int nr_cta = max(0, min(rows_cta, R - rbase));
     for (int it = rank * NTHR + tid; it < nr_cta * D; it += CL * NTHR) {
         const int lr = it / D, col = it - lr * D;
@@ -422,32 +486,64 @@ struct AttnProblem {
     float scale;
 };
 
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
+}
+
 template <int D, typename Tin>
 cudaError_t launch(const AttnProblem &p, cudaStream_t stream) {
     using G = Geo<D, Tin>;
     constexpr int RG = G::RG, NWARP = G::NW;
     const int rep = p.H / p.Hkv;
     const long long R = (long long)rep * p.n_q;
-    // row groups per CTA: enough for the rows, a power of two dividing 8
+    // row groups per CTA: enough for the rows, a power of two dividing the warps
     int n_rgc = 1;
     while (n_rgc < NWARP && (long long)n_rgc * RG < R) n_rgc *= 2;
     const int n_ksc = NWARP / n_rgc;
     const int n_rb = (int)((R + (long long)n_rgc * RG - 1) / ((long long)n_rgc * RG));
-    // CTAs per cluster: as many as give every warp at least one step of keys
-    // (a short cache is latency-bound: spread it over as many SMs as allowed)
-    const long long per_cta = (long long)n_ksc * KG;
-    const long long want = (p.n_kv + per_cta - 1) / per_cta;
-    const int CL = (int)(want < 1 ? 1 : (want > MAX_CLUSTER ? MAX_CLUSTER : want));
-    const long long blocks = (long long)p.B * p.Hkv * n_rb * CL;
-    if (blocks > INT_MAX) return cudaErrorInvalidValue;
-    cudaLaunchConfig_t cfg = {};
+    // one-time set-up: shared memory size, clusters beyond the portable 8, and
+    // the largest cluster this kernel can actually be given
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int max_cl = 8;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(attn_decode_kernel<D, Tin>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+        if (attr_err != cudaSuccess) return;
+        if (cudaFuncSetAttribute(attn_decode_kernel<D, Tin>,
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+            cudaLaunchConfig_t q = {};
+            q.gridDim = dim3(MAX_CLUSTER);
+            q.blockDim = dim3(G::NTHR);
+            q.dynamicSmemBytes = G::SMEM;
+            int n = 0;
+            if (cudaOccupancyMaxPotentialClusterSize(&n, attn_decode_kernel<D, Tin>, &q) ==
+                    cudaSuccess && n >= 8)
+                max_cl = n < MAX_CLUSTER ? n : MAX_CLUSTER;
+        }
+        (void)cudaGetLastError();                    // a refused query leaves the portable 8
     });
     if (attr_err != cudaSuccess) return attr_err;
+    // CTAs per cluster: enough clusters x CTAs for about four waves of the GPU
+    // (one CTA per SM; a partial last wave then costs little), but no more
+    // CTAs than give every warp one step of keys.  A short or single-sequence
+    // cache is spread over many SMs; a large batch keeps few CTAs per
+    // (sequence, kv head, row block) and long key ranges per warp.
+    const long long units = (long long)p.B * p.Hkv * n_rb;
+    const long long fill = (4LL * device_sm_count() + units - 1) / units;
+    const long long per_cta = (long long)n_ksc * G::NKS;
+    const long long by_keys = (p.n_kv + per_cta - 1) / per_cta;
+    long long cl = fill < by_keys ? fill : by_keys;
+    if (cl > max_cl) cl = max_cl;
+    if (cl < 1) cl = 1;
+    const int CL = (int)cl;
+    const long long blocks = units * CL;
+    if (blocks > INT_MAX) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(G::NTHR);
     cfg.dynamicSmemBytes = G::SMEM;
