@@ -59,6 +59,14 @@ __device__ __forceinline__ float load_scalar(const __nv_bfloat16 *p) {
     return __bfloat162float(__ldg(p));
 }
 
+// Warm L2 with `bytes` (a multiple of 16, 16-byte aligned) at `p`.  Only a
+// hint: nothing is read into the program, so it may be issued before the
+// previous grid has finished; L2 is the point of coherence, so lines that
+// grid still writes are simply updated there.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 template <int D, int L, int R, typename Tin>
 struct TokenInputs {
     static constexpr int NV = D / (4 * L);
@@ -84,7 +92,12 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
     // Launched with programmatic stream serialization: this grid may be
     // scheduled while the previous kernel on the stream is still running.
-    // Nothing is read before the previous grid has completed and flushed.
+    // Nothing is read before the previous grid has completed and flushed; the
+    // block's state rows (one contiguous run of RB rows) are only prefetched
+    // into L2 meanwhile, so their HBM latency overlaps the previous kernel.
+    if (threadIdx.x == 0 && state_in)
+        prefetch_l2(state_in + (size_t)blockIdx.x * D * D + (size_t)blockIdx.y * RB * D,
+                    RB * D * (uint32_t)sizeof(float));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -268,6 +281,9 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     using Win = TokenWindow<D, RB, Tin, WT>;
     __shared__ Win win[2];
 
+    if (threadIdx.x == 0 && state_in)                       // as in recurrent_kernel
+        prefetch_l2(state_in + (size_t)blockIdx.x * D * D + (size_t)blockIdx.y * RB * D,
+                    RB * D * (uint32_t)sizeof(float));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
