@@ -120,22 +120,12 @@ __device__ __forceinline__ float fast_exp(float x) {
 }
 
 // Store 16 consecutive fp32 values as bf16 hi / lo into two 128-B-swizzled
-// tiles at (row, col0 .. col0+15); col0 is a multiple of 8.
+// tiles at (row, col0 .. col0+15); col0 is a multiple of 8.  hi keeps the top
+// 16 bits of each value, lo = bf16_rn(x - hi): ~16 significant bits together.
 __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile, int row, int col0,
                                               const float (&x)[16]) {
-#pragma unroll
-    for (int c = 0; c < 16; c += 8) {
-        uint32_t h[8], l[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ptx::split_bf16(x[c + e], h[e], l[e]);
-        const uint4 hv = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                                    h[6] | (h[7] << 16));
-        const uint4 lv = make_uint4(l[0] | (l[1] << 16), l[2] | (l[3] << 16), l[4] | (l[5] << 16),
-                                    l[6] | (l[7] << 16));
-        const uint32_t off = ptx::sw128_offset(row, col0 + c);
-        *reinterpret_cast<uint4 *>(hi_tile + off) = hv;
-        *reinterpret_cast<uint4 *>(lo_tile + off) = lv;
-    }
+    ptx::store_split8(hi_tile, lo_tile, row, col0, *reinterpret_cast<const float(*)[8]>(x));
+    ptx::store_split8(hi_tile, lo_tile, row, col0 + 8, *reinterpret_cast<const float(*)[8]>(x + 8));
 }
 
 // T = (I + A)^-1 for a strictly lower triangular 64x64 A stored in full
@@ -554,19 +544,34 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         issued = 7;
     }
 
+    // g and beta of the next chunk, one token per thread (threads 0-63):
+    // loaded a chunk ahead so that their latency is hidden behind the chunk
+    float gnext = 0.f, bnext = 0.f;
+    if (tid < 64 && tid < T) {
+        const size_t gi = ((size_t)b * T + tid) * H + h;
+        gnext = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
+        bnext = beta[gi];
+    }
+
     for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
         const int t0 = c * C;
         const int n = min(C, T - t0);
         const bool more = c + 1 < n_chunks;
 
-        // ---------------- 1. gates (the chunk's tiles were issued earlier)
+        // ---------------- 1. gates (the chunk's tiles were issued earlier; its
+        //                  g and beta were loaded into registers one chunk ahead)
         if (tid < 64) {
             const int r = tid;
-            float gr = 0.f, br = 0.f;
-            if (r < n) {
-                const size_t gi = ((size_t)b * T + t0 + r) * H + h;
-                gr = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
-                br = beta[gi];
+            const float gr = gnext, br = bnext;
+            if (more) {
+                const int rn = min(C, T - (t0 + C));
+                gnext = 0.f;
+                bnext = 0.f;
+                if (r < rn) {
+                    const size_t gi = ((size_t)b * T + t0 + C + r) * H + h;
+                    gnext = fmaxf(g[gi], -30.f);
+                    bnext = beta[gi];
+                }
             }
             // inclusive scan of g over the chunk (two warps)
             float sacc = gr;
@@ -625,16 +630,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 for (int j = 0; j < HALF; j += 16) {
                     float rr[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int vc = wg * HALF + j + e;
-                        float vv;
-                        if (BV == 64)
-                            vv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                sV + ptx::sw128_offset(r, vc)));
-                        else
-                            vv = __bfloat162float(
-                                reinterpret_cast<const __nv_bfloat16 *>(sV)[r * BV + vc]);
-                        rr[e] = fmaf(br, vv, -bg * x[j + e]);
+                    for (int e8 = 0; e8 < 16; e8 += 8) {
+                        // 8 values of row r: one 16-byte chunk of the swizzled V tile
+                        const uint4 raw = *reinterpret_cast<const uint4 *>(
+                            sV + ptx::sw128_offset(r, wg * HALF + j + e8));
+                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float vv = __uint_as_float(
+                                (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+                            rr[e8 + e] = fmaf(br, vv, -bg * x[j + e8 + e]);
+                        }
                     }
                     store_split16(sRhi, sRlo, r, wg * HALF + j, rr);
                 }
