@@ -72,8 +72,8 @@ struct Cfg {
     static constexpr int OFF_Z = OFF_V + 8192;             // Z hi, Z lo: 128 rows x 128 B each
     static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
     static constexpr int OFF_RU = OFF_S + 2 * D * 128;     // R (then U~) hi, lo: 64 rows x 128 B
-    static constexpr int OFF_MISC = OFF_RU + 2 * 8192;     // G, beta, gamma, end-decay
-    static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;  // + alignment slack
+    static constexpr int OFF_MISC = OFF_RU + 2 * 8192;     // 2 gate sets: G, beta, gamma, end-decay
+    static constexpr int SMEM = OFF_MISC + 2 * 4 * 64 * 4 + 1024;  // + alignment slack
     // TMEM columns
     static constexpr int COL_X = 0;
     static constexpr int COL_Y = BV;
@@ -429,10 +429,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
     __shared__ Bars bars;
-    float *sG = reinterpret_cast<float *>(sm + CF::OFF_MISC);
-    float *sBeta = sG + 64;
-    float *sGam = sG + 128;
-    float *sEnd = sG + 192;
+    float *gsets = reinterpret_cast<float *>(sm + CF::OFF_MISC);   // set i: gsets + 256 i
     uint8_t *sQK = sm + CF::OFF_QK;
     uint8_t *sV = sm + CF::OFF_V;
     uint8_t *sZhi = sm + CF::OFF_Z, *sZlo = sm + CF::OFF_Z + 16384;
@@ -544,52 +541,57 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         issued = 7;
     }
 
-    // g and beta of the next chunk, one token per thread (threads 0-63):
-    // loaded a chunk ahead so that their latency is hidden behind the chunk
+    // Gates: warps 2 and 3 (threads 64-127, TMEM lanes 64-127, idle while the
+    // other warps build R) scan the next chunk's g into the other of two gate
+    // sets during step 5, from g and beta they loaded one chunk earlier; the
+    // set of chunk 0 is built here.  Set layout: G (in-chunk running sum of g,
+    // each clamped at -30: exp(-30) ~ 1e-13, a reset stays a reset), beta,
+    // gamma = exp(G), end-decay = exp(G_63 - G).
+    const bool gate_thread = tid >= 64 && tid < 128;
+    const int gr_ = tid - 64;                          // token of the chunk (gate threads)
     float gnext = 0.f, bnext = 0.f;
-    if (tid < 64 && tid < T) {
-        const size_t gi = ((size_t)b * T + tid) * H + h;
-        gnext = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
-        bnext = beta[gi];
+    auto load_gates = [&](int cc) {                   // g, beta of chunk cc into gnext / bnext
+        gnext = 0.f;
+        bnext = 0.f;
+        if (cc * C + gr_ < T) {
+            const size_t gi = ((size_t)b * T + cc * C + gr_) * H + h;
+            gnext = fmaxf(g[gi], -30.f);
+            bnext = beta[gi];
+        }
+    };
+    auto scan_gates = [&](float *set) {               // gate threads only
+        float sacc = gnext;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+            if (lane >= o) sacc += y;
+        }
+        set[gr_] = sacc;
+        set[64 + gr_] = bnext;
+        ptx::named_sync(3, 64);
+        if (gr_ >= 32) set[gr_] = sacc + set[31];
+        ptx::named_sync(3, 64);
+        set[128 + gr_] = fast_exp(set[gr_]);
+        set[192 + gr_] = fast_exp(set[63] - set[gr_]);
+    };
+    if (gate_thread && n_chunks > 0) {
+        load_gates(0);
+        scan_gates(gsets);
+        if (n_chunks > 1) load_gates(1);
     }
+    __syncthreads();
 
     for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
         const int t0 = c * C;
         const int n = min(C, T - t0);
         const bool more = c + 1 < n_chunks;
+        float *sG = gsets + (c & 1) * 256;            // this chunk's gate set
+        float *sBeta = sG + 64;
+        float *sGam = sG + 128;
+        float *sEnd = sG + 192;
+        (void)sG;
 
-        // ---------------- 1. gates (the chunk's tiles were issued earlier; its
-        //                  g and beta were loaded into registers one chunk ahead)
-        if (tid < 64) {
-            const int r = tid;
-            const float gr = gnext, br = bnext;
-            if (more) {
-                const int rn = min(C, T - (t0 + C));
-                gnext = 0.f;
-                bnext = 0.f;
-                if (r < rn) {
-                    const size_t gi = ((size_t)b * T + t0 + C + r) * H + h;
-                    gnext = fmaxf(g[gi], -30.f);
-                    bnext = beta[gi];
-                }
-            }
-            // inclusive scan of g over the chunk (two warps)
-            float sacc = gr;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, sacc, o);
-                if (lane >= o) sacc += y;
-            }
-            sG[r] = sacc;       // warp 1 adds warp 0's total below
-            sBeta[r] = br;
-        }
-        __syncthreads();
-        if (tid >= 32 && tid < 64) sG[tid] += sG[31];
-        __syncthreads();
-        if (tid < 64) {
-            sGam[tid] = fast_exp(sG[tid]);
-            sEnd[tid] = fast_exp(sG[63] - sG[tid]);
-        }
+        // ---------------- 1. wait for the chunk's tiles (issued earlier)
         if (!ptx::mbar_wait(&bars.tma, (uint32_t)(c & 1), abort_flag)) fail();
         else if (tid == 0) armed = -1;
         __syncthreads();
@@ -647,6 +649,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             } else {
 #pragma unroll
                 for (int j = 0; j < HALF; ++j) xq[j] = x[j];
+                if (gate_thread && more) {            // the next chunk's gates
+                    scan_gates(gsets + ((c + 1) & 1) * 256);
+                    if (c + 2 < n_chunks) load_gates(c + 2);
+                }
             }
         }
         ptx::fence_proxy_async_smem();
