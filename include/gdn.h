@@ -227,6 +227,18 @@ int gdn_flash_attn(const void *q, const void *k, const void *v, const void *mask
  * that shape, 0 otherwise. */
 int gdn_flash_attn_supports(int n_q, int head_dim_k, int head_dim_v);
 
+/*
+ * gdn_selftest_wait_timeout -- exercises the library's failure path on the
+ * GPU without faulting it: enqueues on `stream` one small kernel whose
+ * bounded wait (on a barrier nothing ever completes) gives up after about
+ * 0.1 ms and records GDN_ERR_TIMEOUT in the device status word, the same way
+ * the chunked kernels report a wait that gives up.  The kernel then returns
+ * normally and the context stays usable; a following
+ * gdn_get_device_status() returns GDN_ERR_TIMEOUT and clears it.  A
+ * diagnostic with no counterpart in the pages.  Returns GDN_OK once enqueued.
+ */
+int gdn_selftest_wait_timeout(gdn_stream_t stream);
+
 /* Static English text for a status code (never NULL). */
 const char *gdn_status_string(int status);
 

@@ -34,7 +34,8 @@ PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
            "gdn_select_path", "gdn_supports", "gdn_get_device_status", "gdn_status_string",
-           "gdn_version", "gdn_flash_attn", "gdn_flash_attn_supports", "gdn_forward_noalloc"]
+           "gdn_version", "gdn_flash_attn", "gdn_flash_attn_supports", "gdn_forward_noalloc",
+           "gdn_selftest_wait_timeout"]
 
 _lib = None
 
@@ -78,6 +79,8 @@ def lib():
         L.gdn_flash_attn_supports.restype = i
         L.gdn_forward_noalloc.argtypes = fwd[:11] + [i, i, i, i, vp]
         L.gdn_forward_noalloc.restype = i
+        L.gdn_selftest_wait_timeout.argtypes = [vp]
+        L.gdn_selftest_wait_timeout.restype = i
         _lib = L
     return _lib
 

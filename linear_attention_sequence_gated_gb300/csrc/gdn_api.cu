@@ -261,6 +261,14 @@ const char *gdn_status_string(int status) {
 
 int gdn_version(void) { return 100; }
 
+int gdn_selftest_wait_timeout(gdn_stream_t stream) {
+    int *status = status_word_for_current_device();
+    if (!status) return GDN_ERR_CUDA;
+    return gdn::launch_wait_selftest(status, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? GDN_OK
+               : GDN_ERR_CUDA;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------

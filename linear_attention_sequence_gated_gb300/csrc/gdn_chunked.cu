@@ -1514,7 +1514,31 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Self-test of the bounded waits: one CTA waits on an mbarrier that nothing
+// ever arrives at, for at most `budget` SM clock cycles, and records
+// GDN_ERR_TIMEOUT in the status word exactly as the chunked kernels do when
+// one of their waits gives up.  The kernel then returns normally.
+__global__ void wait_selftest_kernel(int *status, long long budget) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        ptx::mbar_init(&bar, 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (!ptx::mbar_wait(&bar, 0, &abort_flag, budget)) {
+        if (atomicExch(&abort_flag, 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
+    }
+    __syncthreads();
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(int *status, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(status, 200000LL);
+    return cudaGetLastError();
+}
 
 bool chunked_supports(int d) { return d == 64 || d == 128 || d == 256; }
 

@@ -30,6 +30,8 @@ size_t chunked_workspace_bytes(int B, int T, int H, int d, int dtype);
 cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
                            cudaStream_t stream);
 bool chunked_supports(int d);
+// One CTA whose bounded wait gives up and records GDN_ERR_TIMEOUT (self-test).
+cudaError_t launch_wait_selftest(int *status, cudaStream_t stream);
 
 // Host-side argument checks shared by the C-ABI front ends.
 namespace host {

@@ -11,6 +11,8 @@ model card (section "Measured": 32 value heads x head_dim 128, one token per
 step, 24 layers) plus batched decode and long prefill; see
 linear_attention_sequence_gated_gb300/workloads.py for the distributions.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -323,3 +325,19 @@ def test_multi_token_runs_recurrent(T, d):
     w = W.Workload(f"short_d{d}_t{T}", 3, T, 4, d, "bf16", 0.0, 0.02, seed=60 + T)
     inp = W.make_inputs(w, "cuda")
     check(inp, "bf16", "recurrent", TOL_RECURRENT)
+
+
+# ---------------------------------------------------------------- failure path
+
+def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
+    """A wait that gives up (a barrier nothing completes, bounded to ~0.1 ms)
+    reports GDN_ERR_TIMEOUT through the device status word, which the query
+    clears; the next call runs normally."""
+    L = gdn.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    assert gdn.device_status() == gdn.OK
+    assert L.gdn_selftest_wait_timeout(ctypes.c_void_p(stream)) == gdn.OK
+    assert gdn.device_status() == gdn.ERR_TIMEOUT
+    assert gdn.device_status() == gdn.OK                 # read and cleared
+    w = W.Workload("after_timeout", 1, 100, 2, 128, "bf16", 0.0, 0.02, seed=90)
+    check(W.make_inputs(w, "cuda"), "bf16", "chunked")
