@@ -322,7 +322,16 @@ def run_decode24(torch, gdn, W, dev, timer, args, dist, peaks):
            "layers": L, "io_dtype": "bf16", "state_dtype": "f32",
            "l2": "flushed (512 MB write) before every timed step", "graph": True}
     return {"value": us_step, "ms": ms, "roofline": roof, "e2e": e2e, "launches": launches,
-            "config": cfg, "times_ms": times}
+            "config": cfg, "times_ms": times, "spread": spread(times)}
+
+
+def spread(times_ms, scale=1e3, unit="us"):
+    """Median, minimum and maximum of the timed repetitions (in `unit`)."""
+    xs = sorted(times_ms)
+    n = len(xs)
+    med = xs[n // 2] if n % 2 else 0.5 * (xs[n // 2 - 1] + xs[n // 2])
+    return {"median": med * scale, "min": xs[0] * scale, "max": xs[-1] * scale, "unit": unit,
+            "n": n}
 
 
 def attn_bytes(w, elt):
@@ -350,6 +359,7 @@ def run_attn(torch, gdn, W, w, dev, timer, args, dist, peaks):
     del inp, out
     return {"workload": w.name, "path": "flash_attn", "metric": "attention us/call",
             "value": ms * 1e3, "unit": "us/call", "ms_per_step": ms, "launches_per_step": 1,
+            "spread": spread(times),
             "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": ach / peaks["hbm_gbs"], "traffic": load_traffic().get(w.name),
                          "bytes_per_launch": by}}
@@ -376,7 +386,7 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
         raise RuntimeError(f"device status after {w.name}")
     ms = dist.max(sum(times) / len(times))
     in_b = 2 if w.dtype == "bf16" else 4
-    res = {"workload": w.name, "path": path, "ms_per_step": ms,
+    res = {"workload": w.name, "path": path, "ms_per_step": ms, "spread": spread(times),
            "launches_per_step": launches_per_call(path, d)}
     if kind == "decode":
         bytes_launch = run_bytes(B, T, H, w.n_k, d, in_b)
@@ -591,7 +601,7 @@ def main():
                         "beta sigmoid(N(0,1)), g -softplus(N(0,1)), state N(0,0.02))",
                 "config": head["config"], "roofline": head["roofline"], "cpu_baseline": cpu,
                 "e2e": head["e2e"], "gpu_launches": launches, "clocks": clocks.summary(),
-                "peaks_source": peaks["source"], "workloads": extra}
+                "spread": head["spread"], "peaks_source": peaks["source"], "workloads": extra}
         print(json.dumps(line))
     dist.close()
 
