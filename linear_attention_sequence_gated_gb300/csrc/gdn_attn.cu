@@ -209,8 +209,10 @@ template <int D, typename Tin> struct Geo {
 // Small per-CTA state outside the ring.
 template <int NW, int RG, int NKS>
 struct SmallSmem {
-    float wm[NW][RG], wl[NW][RG];                     // each warp's partial max, sum per row
+    float wm[NW][RG], wl[NW][RG];                     // each warp's partial max (then weight), sum
     float cm[NW * RG], cl[NW * RG];                   // the CTA's partial per local row
+    float pw[NW * RG][MAX_CLUSTER];                   // cluster merge: weight of each CTA per row
+    float pl[NW * RG];                                // cluster merge: total sum of exp per row
     float p[NW][NKS][RG];                             // a step's probabilities, [key][row]
 };
 
@@ -419,7 +421,9 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     cp_async_wait<0>();
     __syncthreads();                                  // every warp is done with the ring
 
-    // ---- merge the warps of this CTA (same row group, different keys)
+    // ---- merge the warps of this CTA (same row group, different keys).  The
+    //      weights exp(m_w - M) depend only on the row: one thread per row
+    //      computes them (in place of the maxima) and the row's M and L.
 #pragma unroll
     for (int r = 0; r < RG; ++r) {
         if (lane == 0) { sm.wm[warp][r] = m[r]; sm.wl[warp][r] = l[r]; }
@@ -430,48 +434,62 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         }
     }
     __syncthreads();
+    if (tid < rows_cta) {                             // local row lr = tid: group g, row r
+        const int g = tid / RG, r = tid - g * RG;
+        float M = -INFINITY;
+        for (int w = g; w < NW; w += n_rgc) M = fmaxf(M, sm.wm[w][r]);
+        float L = 0.f;
+        for (int w = g; w < NW; w += n_rgc) {
+            const float mw = sm.wm[w][r];
+            const float wt = (M == -INFINITY || mw == -INFINITY) ? 0.f : expf(mw - M);
+            L = fmaf(wt, sm.wl[w][r], L);
+            sm.wm[w][r] = wt;                         // each warp belongs to one row group
+        }
+        sm.cm[tid] = M;
+        sm.cl[tid] = L;
+    }
+    __syncthreads();
     for (int it = tid; it < rows_cta * D; it += NTHR) {
         const int lr = it / D, col = it - lr * D;
         const int g = lr / RG, r = lr - g * RG;
-        float M = -INFINITY;
-        for (int w = g; w < NW; w += n_rgc) M = fmaxf(M, sm.wm[w][r]);
-        float L = 0.f, o = 0.f;
-        if (M != -INFINITY) {
-            for (int w = g; w < NW; w += n_rgc) {
-                const float mw = sm.wm[w][r];
-                if (mw != -INFINITY) {
-                    const float wt = expf(mw - M);
-                    L = fmaf(wt, sm.wl[w][r], L);
-                    o = fmaf(wt, wo[w][r][col], o);
-                }
-            }
-        }
+        float o = 0.f;
+        for (int w = g; w < NW; w += n_rgc) o = fmaf(sm.wm[w][r], wo[w][r][col], o);
         co[lr][col] = o;
-        if (col == 0) { sm.cm[lr] = M; sm.cl[lr] = L; }
     }
-    // ---- merge the CTAs of the cluster (same rows, different keys)
+    // ---- merge the CTAs of the cluster (same rows, different keys): per row,
+    //      each CTA's weight once, then the weighted sum per column
     cluster_sync();
     const int nr_cta = max(0, min(rows_cta, R - rbase));
-    for (int it = rank * NTHR + tid; it < nr_cta * D; it += CL * NTHR) {
-        const int lr = it / D, col = it - lr * D;
+    if (tid < nr_cta) {
         float mk[MAX_CLUSTER];
         float M = -INFINITY;
 #pragma unroll
         for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
-            mk[pr] = pr < CL ? ld_peer(peer_addr(&sm.cm[lr], pr)) : -INFINITY;
+            mk[pr] = pr < CL ? ld_peer(peer_addr(&sm.cm[tid], pr)) : -INFINITY;
             M = fmaxf(M, mk[pr]);
         }
-        float L = 0.f, o = 0.f;
-        if (M != -INFINITY) {
+        float L = 0.f;
 #pragma unroll
-            for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
-                if (pr < CL && mk[pr] != -INFINITY) {
-                    const float wt = expf(mk[pr] - M);
-                    L = fmaf(wt, ld_peer(peer_addr(&sm.cl[lr], pr)), L);
-                    o = fmaf(wt, ld_peer(peer_addr(&co[lr][col], pr)), o);
-                }
+        for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
+            float wt = 0.f;
+            if (pr < CL && M != -INFINITY && mk[pr] != -INFINITY) {
+                wt = expf(mk[pr] - M);
+                L = fmaf(wt, ld_peer(peer_addr(&sm.cl[tid], pr)), L);
             }
+            sm.pw[tid][pr] = wt;
         }
+        sm.pl[tid] = L;
+    }
+    __syncthreads();
+    for (int it = rank * NTHR + tid; it < nr_cta * D; it += CL * NTHR) {
+        const int lr = it / D, col = it - lr * D;
+        float o = 0.f;
+#pragma unroll
+        for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
+            const float wt = sm.pw[lr][pr];
+            if (pr < CL && wt != 0.f) o = fmaf(wt, ld_peer(peer_addr(&co[lr][col], pr)), o);
+        }
+        const float L = sm.pl[lr];
         const int rg = rbase + lr;
         const int h = hk * rep + rg / n_q, i = rg % n_q;
         out[(((size_t)b * n_q + i) * H + h) * D + col] = (L > 0.f) ? o / L : 0.f;
