@@ -89,8 +89,9 @@ enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 
  * gdn_forward -- the op with float32 q, k, v.
  * q, k, v: (n_seqs, n_tokens, n_heads, head_dim) float32.  Other arguments as
  * described above.  Uses the AUTO path; if that path needs a workspace it is
- * taken from cudaMallocAsync on `stream` and released on `stream` (stream
- * ordered, no host synchronisation).
+ * allocated and released in stream order on `stream` (no host
+ * synchronisation) from a memory pool the library keeps per device, which
+ * holds up to 1 GiB reserved between calls.
  */
 int gdn_forward(const float *q, const float *k, const float *v,
                 const float *g, const float *beta, const float *state_in,
@@ -118,7 +119,9 @@ int gdn_forward_bf16(const void *q, const void *k, const void *v,
  * workspace: caller-owned device buffer of at least
  *   gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype, path)
  *   bytes, 256-byte aligned; or NULL, in which case the call allocates and
- *   frees it stream-ordered on `stream` (cudaMallocAsync / cudaFreeAsync).
+ *   frees it stream-ordered on `stream` from the library's per-device memory
+ *   pool (cudaMallocFromPoolAsync / cudaFreeAsync; up to 1 GiB stays
+ *   reserved in the pool between calls).
  * The workspace contents on entry are ignored; on return they are garbage.
  * Two calls in flight at once must not share a workspace.
  */
@@ -168,8 +171,8 @@ size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
  * least T_switch tokens, everything else runs the recurrent path.  T_switch
  * was measured on GB300 and depends on head_dim and on the number of
  * (sequence, head) pairs P = n_seqs * n_heads:
- *   head_dim 64: 48;  128: 40 (P < 128) or 24 (P >= 128);
- *   256: 48 (P < 128) or 64 (P >= 128). */
+ *   head_dim 64: 48 (P < 1024) or 64;  128: 56 (P < 128) or 24;
+ *   256: 32 (P < 128) or 24. */
 int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype);
 
 /*

@@ -32,6 +32,36 @@ int *status_word_for_current_device() {
     return g_status_ptr[dev];
 }
 
+// Stream-ordered workspace allocations (when the caller passes none) come
+// from one library-owned memory pool per device that keeps up to
+// kPoolKeepBytes reserved across calls, so that a call does not map fresh
+// device memory each time.  Each call still gets its own allocation, freed in
+// stream order, so calls on different streams never share a workspace.
+constexpr unsigned long long kPoolKeepBytes = 1ull << 30;
+cudaMemPool_t g_pool[kMaxDevices] = {};
+std::mutex g_pool_mu;
+
+cudaMemPool_t pool_for_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    if (!g_pool[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool = nullptr;
+        if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+        unsigned long long keep = kPoolKeepBytes;
+        if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return nullptr;
+        }
+        g_pool[dev] = pool;
+    }
+    return g_pool[dev];
+}
+
 using gdn::host::aligned;
 using gdn::host::mul_ok;
 using gdn::host::overlap;
@@ -49,9 +79,9 @@ using gdn::host::span_bytes;
 int chunked_min_tokens(long long pairs, int head_dim) {
     const bool many = pairs >= 128;
     switch (head_dim) {
-        case 64: return 48;
-        case 128: return many ? 24 : 40;
-        case 256: return many ? 64 : 48;
+        case 64: return pairs >= 1024 ? 64 : 48;
+        case 128: return many ? 24 : 56;
+        case 256: return many ? 24 : 32;
         default: return INT_MAX;
     }
 }
@@ -165,7 +195,9 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
     void *ws = workspace;
     bool owned = false;
     if (need > 0 && !ws) {
-        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) return GDN_ERR_NOMEM;
+        cudaMemPool_t pool = pool_for_current_device();
+        if (!pool) return GDN_ERR_CUDA;
+        if (cudaMallocFromPoolAsync(&ws, need, pool, stream) != cudaSuccess) return GDN_ERR_NOMEM;
         owned = true;
     }
     const cudaError_t e = gdn::launch_chunked(p, ws, need, stream);

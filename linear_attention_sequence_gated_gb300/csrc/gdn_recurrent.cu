@@ -67,6 +67,27 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
+// Packed fp32 arithmetic on element pairs (sm_100 family): each element is
+// rounded exactly as the scalar fmaf / multiplication rounds it.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 template <int D, int L, int R, typename Tin>
 struct TokenInputs {
     static constexpr int NV = D / (4 * L);
@@ -376,19 +397,22 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 unpack4(lds_raw4(&W_.q[j][(jv * L + sub) * 4]), qv[jv]);
                 unpack4(lds_raw4(&W_.k[j][(jv * L + sub) * 4]), kv[jv]);
             }
+            // S k and S q on this lane's slice, element pairs in packed FMAs
             float pk[R], pq[R];
 #pragma unroll
-            for (int u = 0; u < R; ++u) { pk[u] = 0.f; pq[u] = 0.f; }
+            for (int u = 0; u < R; ++u) {
+                float2 ak = make_float2(0.f, 0.f), aq = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int jv = 0; jv < NV; ++jv) {
+                for (int jv = 0; jv < NV; ++jv) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-#pragma unroll
-                    for (int u = 0; u < R; ++u) {
-                        pk[u] = fmaf(s[u][jv][e], kv[jv][e], pk[u]);
-                        pq[u] = fmaf(s[u][jv][e], qv[jv][e], pq[u]);
+                    for (int e = 0; e < 4; e += 2) {
+                        const float2 sv = make_float2(s[u][jv][e], s[u][jv][e + 1]);
+                        ak = ffma2(sv, make_float2(kv[jv][e], kv[jv][e + 1]), ak);
+                        aq = ffma2(sv, make_float2(qv[jv][e], qv[jv][e + 1]), aq);
                     }
                 }
+                pk[u] = ak.x + ak.y;
+                pq[u] = aq.x + aq.y;
             }
 #pragma unroll
             for (int off = L / 2; off > 0; off >>= 1) {
@@ -406,11 +430,17 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             for (int u = 0; u < R; ++u) {
                 const float vv = lds_scalar(&W_.v[j][lrow0 + u * RU]);
                 const float delta = bt * (vv - alpha * pk[u]);
+                const float2 a2 = make_float2(alpha, alpha), d2 = make_float2(delta, delta);
 #pragma unroll
                 for (int jv = 0; jv < NV; ++jv)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        s[u][jv][e] = fmaf(alpha, s[u][jv][e], delta * kv[jv][e]);
+                    for (int e = 0; e < 4; e += 2) {
+                        // s <- alpha s + delta k, as the scalar fmaf(alpha, s, delta * k)
+                        const float2 dk = fmul2(d2, make_float2(kv[jv][e], kv[jv][e + 1]));
+                        const float2 sn = ffma2(a2, make_float2(s[u][jv][e], s[u][jv][e + 1]), dk);
+                        s[u][jv][e] = sn.x;
+                        s[u][jv][e + 1] = sn.y;
+                    }
                 const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
                 if (sub == 0) op[o + row0 + u * RU] = ov;
             }
