@@ -89,18 +89,24 @@ constexpr int Z_BYTES = 2 * 16384;
 
 // Shared-memory map of chunk_z_kernel (head_dim D): [K;Q] for the K K^T /
 // Q K^T product, then (reusing the same bytes once that product is done)
-// A -> T, P, the block solve's scratch and the Z tile.
+// A -> T (fp32), P as bf16 hi / lo tiles, and the Z tile.  The P T product
+// reads 128 A rows from P hi: rows 0-63 are P hi, 64-127 are P lo; its third
+// term reads 128 rows from P lo, whose rows 64-127 fall on the Z tile (those
+// products land in TMEM lanes that are never read).
 template <int D>
 struct ZCfg {
     static constexpr int SZ_F = 64 * FST * 4;              // one 64 x 64 fp32 matrix
     static constexpr int OFF_QK = 0;                       // D/64 slabs x (K 8 KB | Q 8 KB)
     static constexpr int OFF_A = 0;                        // A, then T in place
-    static constexpr int OFF_P = SZ_F;
-    static constexpr int OFF_Z = 2 * SZ_F;                 // Z hi | Z lo (W lives here during the solve)
+    static constexpr int OFF_PHI = 18432;                  // P hi: 64 rows x 128 B (swizzled)
+    static constexpr int OFF_PLO = OFF_PHI + 8192;         // P lo
+    static constexpr int OFF_Z = OFF_PLO + 8192;           // Z hi | Z lo (W lives here during the solve)
     static constexpr int REGION = (D / 64) * 16384 > OFF_Z + Z_BYTES ? (D / 64) * 16384
                                                                      : OFF_Z + Z_BYTES;
     static constexpr int OFF_MISC = REGION;                // G, beta
     static constexpr int SMEM = OFF_MISC + 2 * 64 * 4 + 1024;
+    static_assert(SZ_F <= OFF_PHI, "A / T below the P tiles");
+    static_assert(OFF_PHI % 1024 == 0 && OFF_Z % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
     static_assert(16 * 96 * 4 <= Z_BYTES, "solve scratch inside the Z tile");
 };
 
@@ -253,7 +259,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     float *sBeta = sG + 64;
     uint8_t *sQK = sm + ZC::OFF_QK;
     float *sA = reinterpret_cast<float *>(sm + ZC::OFF_A);
-    float *sP = reinterpret_cast<float *>(sm + ZC::OFF_P);
+    uint8_t *sPhi = sm + ZC::OFF_PHI, *sPlo = sm + ZC::OFF_PLO;
     float *sW = reinterpret_cast<float *>(sm + ZC::OFF_Z);
     uint8_t *sZhi = sm + ZC::OFF_Z, *sZlo = sm + ZC::OFF_Z + 16384;
 
@@ -286,7 +292,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     };
     const uint32_t aQK = ptx::smem_u32(sQK);
 
-    uint32_t phase = 0;
+    uint32_t phase = 0, mma_phase = 0;                // TMA and MMA barrier phases
     bool tma_pending = false;                         // thread 0: a load not yet waited for
     for (int task = blockIdx.x; task < n_tasks && !*abort_flag; task += gridDim.x) {
         const int c = task % n_chunks;
@@ -342,9 +348,10 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             ptx::mma_commit(&bars.mma);
         }
-        if (!ptx::mbar_wait(&bars.mma, phase, abort_flag)) fail();
+        if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
         ptx::tc_fence_after();
         phase ^= 1;
+        mma_phase ^= 1;
 
         // 3. A, P (the [K;Q] bytes are free now: the product has completed)
         {
@@ -362,35 +369,59 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kq[j] : 0.f;
                 }
             } else {
+                float pv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int i = wg * 32 + j;
-                    sP[r * FST + i] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                    pv[j] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
                 }
+                store_split16(sPhi, sPlo, r, wg * 32, *reinterpret_cast<float(*)[16]>(pv));
+                store_split16(sPhi, sPlo, r, wg * 32 + 16, *reinterpret_cast<float(*)[16]>(pv + 16));
             }
         }
         ptx::tc_fence_before();
         __syncthreads();
         ut_transform(sA, sW, tid, 0);                 // T in place over A; W dead afterwards
-        {
+        {                                             // T as hi / lo into Z rows 0-63
             const int r = tid >> 2, c0 = (tid & 3) * 16;
-            float t[16], pt[16];
+            float t[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                t[e] = sA[r * FST + c0 + e];
-                pt[e] = 0.f;
-            }
-            // (P T)[r][j] = sum_{i=j}^{r} P[r][i] T[i][j]   (T[i][j] = 0 for i < j)
-            for (int i = c0; i <= r; ++i) {
-                const float p = sP[r * FST + i];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) pt[e] = fmaf(p, sA[i * FST + c0 + e], pt[e]);
-            }
+            for (int e = 0; e < 16; ++e) t[e] = sA[r * FST + c0 + e];
             store_split16(sZhi, sZlo, r, c0, t);
-            store_split16(sZhi, sZlo, 64 + r, c0, pt);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        // P T on the tensor cores: A = [P hi; P lo] (128 rows), B = T rows
+        // (MN-major), three terms P hi T hi + P hi T lo + P lo T hi summed in
+        // TMEM lanes 0-63
+        if (tid == 0) {
+            ptx::tc_fence_after();
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, true);
+            const uint32_t aP[3] = {ptx::smem_u32(sPhi), ptx::smem_u32(sPhi), ptx::smem_u32(sPlo)};
+            const uint32_t bT[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZlo), ptx::smem_u32(sZhi)};
+#pragma unroll
+            for (int part = 0; part < 3; ++part)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::mma_bf16(tmem, ptx::smem_desc(aP[part] + kk * 32, 16, 1024),
+                                  ptx::smem_desc(bT[part] + kk * 2048, 8192, 1024), idesc,
+                                  part > 0 || kk > 0);
+            ptx::mma_commit(&bars.mma);
+        }
+        if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
+        ptx::tc_fence_after();
+        mma_phase ^= 1;
+        if ((warp & 3) < 2) {                         // P T rows -> Z rows 64-127
+            float pt[32];
+            ptx::tmem_ld16(tmem + lane_off + wg * 32, *reinterpret_cast<float(*)[16]>(pt));
+            ptx::tmem_ld16(tmem + lane_off + wg * 32 + 16, *reinterpret_cast<float(*)[16]>(pt + 16));
+            ptx::tmem_ld_wait();
+            store_split16(sZhi, sZlo, 64 + row, wg * 32, *reinterpret_cast<float(*)[16]>(pt));
+            store_split16(sZhi, sZlo, 64 + row, wg * 32 + 16, *reinterpret_cast<float(*)[16]>(pt + 16));
         }
         // 4. the tile to the workspace (one bulk copy), then the buffer is free
         ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
         __syncthreads();
         if (tid == 0) {
             ptx::bulk_store(zws + (size_t)task * Z_BYTES, sZhi, Z_BYTES);
