@@ -1573,10 +1573,21 @@ cudaError_t launch_wait_selftest(int *status, cudaStream_t stream) {
 
 bool chunked_supports(int d) { return d == 64 || d == 128 || d == 256; }
 
-// head_dim 64 / 128 keep every chunk intermediate on chip; head_dim 256
-// keeps one 32 KB transform tile per (sequence, head, chunk) in the workspace.
+// Below this many (sequence, head) pairs, head_dim 128 runs the two-kernel
+// path (chunk transforms into the workspace, then a state walk with two
+// value blocks per head): the fused kernel's one CTA per pair would leave
+// most SMs idle.  Measured at 4096 tokens: 32 pairs 431 -> 325 us, 64 pairs
+// 431 -> 394 us, 128 pairs 435 -> 764 us (fused -> two-kernel).
+constexpr long long kD128SplitMaxPairs = 80;
+
+bool d128_split(int B, int H) { return (long long)B * H < kD128SplitMaxPairs; }
+
+// head_dim 64 (and 128 with many pairs) keep every chunk intermediate on
+// chip; head_dim 256 (and 128 with few pairs) keep one 32 KB transform tile
+// per (sequence, head, chunk) in the workspace.
 size_t chunked_workspace_bytes(int B, int T, int H, int d, int) {
-    if (d != 256 || B <= 0 || T <= 0 || H <= 0) return 0;
+    if (B <= 0 || T <= 0 || H <= 0) return 0;
+    if (d != 256 && !(d == 128 && d128_split(B, H))) return 0;
     const size_t n_chunks = ((size_t)T + C - 1) / C;
     return (size_t)B * (size_t)H * n_chunks * (size_t)Z_BYTES;
 }
@@ -1586,7 +1597,9 @@ cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
     if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
     switch (p.d) {
         case 64: return launch_ws<64>(p, stream);
-        case 128: return launch_ws<128>(p, stream);
+        case 128:
+            return d128_split(p.B, p.H) ? launch_d<128>(p, workspace, ws_bytes, stream)
+                                        : launch_ws<128>(p, stream);
         case 256: return launch_d<256>(p, workspace, ws_bytes, stream);
         default: return cudaErrorInvalidValue;
     }

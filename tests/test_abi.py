@@ -81,8 +81,11 @@ def test_workspace_and_path_queries(L):
     assert L.gdn_select_path(1, -1, 1, 128, 1) == gdn.ERR_ARG
     assert L.gdn_select_path(-1, 10, 1, 128, 1) == gdn.ERR_ARG
     assert L.gdn_select_path(1, 10, 1, 128, 5) == gdn.ERR_ARG
-    # head_dim 64 / 128: the fused chunked kernel keeps everything on chip
+    # head_dim 64 / 128 with many (sequence, head) pairs: the fused chunked kernel keeps
+    # everything on chip; head_dim 128 with fewer than 80 pairs keeps transform tiles
     assert L.gdn_workspace_bytes(8, 16384, 32, 128, 1, 2) == 0
+    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2) == 32 * 64 * 32768
+    assert L.gdn_workspace_bytes(2, 4096, 40, 128, 1, 2) == 0            # 80 pairs: fused
     assert L.gdn_workspace_bytes(8, 16384, 64, 64, 1, 2) == 0
     # head_dim 256: one 32 KB chunk-transform tile per (sequence, head, chunk)
     assert L.gdn_workspace_bytes(8, 16384, 16, 256, 1, 2) == 8 * 16 * 256 * 32768
