@@ -134,44 +134,71 @@ __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile
     ptx::store_split8(hi_tile, lo_tile, row, col0 + 8, *reinterpret_cast<const float(*)[8]>(x + 8));
 }
 
-// T = (I + A)^-1 for a strictly lower triangular 64x64 A stored in full
-// (zeros on and above the diagonal, row stride FST), in place, on 256
-// threads t = 0..255 sharing hardware barrier `bar`, with 16x16 blocks:
-//   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks (column substitution)
-//   2. X_i = T_ii A[i, :i] for i = 1..3, all at once (into W, 16 x 96 fp32)
-//   3. T[i, :i] = -X_i T[:i, :i] for i = 1, 2, 3 in turn
-// which is block forward substitution: (I + A)_ii T_ij + sum_k A_ik T_kj = 0.
-// Each thread of steps 2 and 3 owns one row and four consecutive columns, so
-// every 128-bit shared-memory load feeds four FMAs.  The result is T in full
-// (zeros above the diagonal); entered and left with the matrix visible to all.
-template <int BI>
-__device__ __forceinline__ void ut_solve_row(float *sAT, const float *sW, int t) {
-    // T[BI, :BI] = -X_BI T[:BI, :BI]; X_BI lives at W columns 16 (BI-1) BI / 2 ...
-    constexpr int NQ = 4 * BI;
-    constexpr int XOFF = 8 * (BI - 1) * BI;          // 0, 16, 48: start column of X_BI in W
-    if (t < 16 * NQ) {
-        const int r = t / NQ, q = t % NQ;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float *xrow = sW + r * 96 + XOFF;
-#pragma unroll 4
-        for (int k4 = 0; k4 < BI * 16; k4 += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(xrow + k4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 tq = *reinterpret_cast<const float4 *>(sAT + (k4 + e) * FST + 4 * q);
-                acc.x = fmaf(av[e], tq.x, acc.x);
-                acc.y = fmaf(av[e], tq.y, acc.y);
-                acc.z = fmaf(av[e], tq.z, acc.z);
-                acc.w = fmaf(av[e], tq.w, acc.w);
-            }
-        }
-        *reinterpret_cast<float4 *>(sAT + (BI * 16 + r) * FST + 4 * q) =
-            make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-    }
+// Warp-level bf16 MMA, m16n8k16, fp32 accumulate in place: d += a b.
+// Fragments (lane = 4 g + c): a0 = A[g][2c..2c+1], a1 = A[g+8][2c..2c+1],
+// a2 = A[g][2c+8..2c+9], a3 = A[g+8][2c+8..2c+9]; b0 = B[2c..2c+1][g],
+// b1 = B[2c+8..2c+9][g]; d0, d1 = D[g][2c..2c+1], d2, d3 = D[g+8][2c..2c+1];
+// the element with the lower index in the low half of each 32-bit word.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// A fragment of the 16 x 16 fp32 block at `base` (row stride ld), as bf16
+// hi / lo words (~16 significant bits together).
+__device__ __forceinline__ void frag_a(const float *base, int ld, int lane, uint32_t (&hi)[4],
+                                       uint32_t (&lo)[4]) {
+    const int g = lane >> 2, c = lane & 3;
+    const float2 v0 = *reinterpret_cast<const float2 *>(base + g * ld + 2 * c);
+    const float2 v1 = *reinterpret_cast<const float2 *>(base + (g + 8) * ld + 2 * c);
+    const float2 v2 = *reinterpret_cast<const float2 *>(base + g * ld + 2 * c + 8);
+    const float2 v3 = *reinterpret_cast<const float2 *>(base + (g + 8) * ld + 2 * c + 8);
+    ptx::split_pair(v0.x, v0.y, hi[0], lo[0]);
+    ptx::split_pair(v1.x, v1.y, hi[1], lo[1]);
+    ptx::split_pair(v2.x, v2.y, hi[2], lo[2]);
+    ptx::split_pair(v3.x, v3.y, hi[3], lo[3]);
+}
+
+// B fragment of the 16 x 8 fp32 block at `base` (B[k][n] at base[k * ld + n]).
+__device__ __forceinline__ void frag_b(const float *base, int ld, int lane, uint32_t (&hi)[2],
+                                       uint32_t (&lo)[2]) {
+    const int g = lane >> 2, c = lane & 3;
+    const float x0 = base[(2 * c) * ld + g], x1 = base[(2 * c + 1) * ld + g];
+    const float x2 = base[(2 * c + 8) * ld + g], x3 = base[(2 * c + 9) * ld + g];
+    ptx::split_pair(x0, x1, hi[0], lo[0]);
+    ptx::split_pair(x2, x3, hi[1], lo[1]);
+}
+
+// d += A B for split operands: A hi B hi + A hi B lo + A lo B hi.
+__device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], const uint32_t (&al)[4],
+                                     const uint32_t (&bh)[2], const uint32_t (&bl)[2]) {
+    mma16816(d, ah, bh);
+    mma16816(d, ah, bl);
+    mma16816(d, al, bh);
+}
+
+// T = (I + A)^-1 for a strictly lower triangular 64x64 A stored in full
+// (zeros on and above the diagonal, row stride FST), in place, on 256
+// threads t = 0..255 (8 warps) sharing hardware barrier `bar`, with 16x16
+// blocks:
+//   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks (column
+//      substitution on CUDA cores, one column per thread)
+//   2. X_i = T_ii A[i, :i] for i = 1..3, all at once (into W, 16 x 96 fp32):
+//      twelve 16 x 8 tiles, warp-level MMAs
+//   3. T[i, :i] = -X_i T[:i, :i] for i = 1, 2, 3 in turn (2i tiles each)
+// which is block forward substitution: (I + A)_ii T_ij + sum_k A_ik T_kj = 0.
+// Every product is a 16-row block, too small for a 128-row tensor-memory
+// MMA, so the warps use register-operand MMAs on bf16 hi / lo splits
+// (three terms, ~16 significant bits, fp32 accumulation).  The result is T
+// in full (zeros above the diagonal); entered and left with the matrix
+// visible to all participants.
 __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int bar) {
+    constexpr int LW = 96;                            // row stride of W
+    const int warp = t >> 5, lane = t & 31;
+    const int g = lane >> 2, c = lane & 3;
     // 1. diagonal blocks
     float x[16];
     const int blk = t >> 4, j = t & 15;
@@ -200,38 +227,39 @@ __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int b
         for (int r = 0; r < 16; ++r) Tb[r * FST + j] = x[r];
     }
     ptx::named_sync(bar, 256);
-    // 2. X_i = T_ii A[i, :i]: 16 rows x 96 columns (X_1 | X_2 | X_3), thread
-    //    (r, q) -> row r, columns 4q .. 4q+3 for q < 24 (384 items, 256 threads)
-    for (int it = t; it < 16 * 24; it += 256) {
-        const int r = it / 24, q = it % 24;
-        const int bi = q < 4 ? 1 : (q < 12 ? 2 : 3);        // X_bi holds columns [16(bi-1)bi/2, ...)
-        const int col = 4 * q - 8 * (bi - 1) * bi;          // column within A[bi, :bi]
-        const float *trow = sAT + (bi * 16 + r) * FST + bi * 16;   // T_ii row r (zero above)
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int m4 = 0; m4 < 16; m4 += 4) {
-            const float4 tv = *reinterpret_cast<const float4 *>(trow + m4);
-            const float tvv[4] = {tv.x, tv.y, tv.z, tv.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float4 a = *reinterpret_cast<const float4 *>(
-                    sAT + (bi * 16 + m4 + e) * FST + col);
-                acc.x = fmaf(tvv[e], a.x, acc.x);
-                acc.y = fmaf(tvv[e], a.y, acc.y);
-                acc.z = fmaf(tvv[e], a.z, acc.z);
-                acc.w = fmaf(tvv[e], a.w, acc.w);
-            }
-        }
-        *reinterpret_cast<float4 *>(sW + r * 96 + 4 * q) = acc;
+    // 2. X_i = T_ii A[i, :i]: tile q (12 of them) -> block row i, columns n0 .. n0+7
+    for (int q = warp; q < 12; q += 8) {
+        const int i = q < 2 ? 1 : (q < 6 ? 2 : 3);
+        const int n0 = 8 * (q - (i == 1 ? 0 : (i == 2 ? 2 : 6)));
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        frag_a(sAT + (16 * i) * FST + 16 * i, FST, lane, ah, al);      // T_ii
+        frag_b(sAT + (16 * i) * FST + n0, FST, lane, bh, bl);           // A[i, n0 ..]
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma3(d, ah, al, bh, bl);
+        float *w = sW + 8 * (i - 1) * i + n0 + 2 * c;                   // X_i at column 16 (i-1) i / 2
+        *reinterpret_cast<float2 *>(w + g * LW) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(w + (g + 8) * LW) = make_float2(d[2], d[3]);
     }
     ptx::named_sync(bar, 256);
-    // 3. block rows in turn (each needs the rows above it)
-    ut_solve_row<1>(sAT, sW, t);
-    ptx::named_sync(bar, 256);
-    ut_solve_row<2>(sAT, sW, t);
-    ptx::named_sync(bar, 256);
-    ut_solve_row<3>(sAT, sW, t);
-    ptx::named_sync(bar, 256);
+    // 3. block rows in turn (each needs the rows above it): T[i, n0 .. n0+7]
+    //    = -sum over 16-wide k blocks of X_i[:, k] T[k, n0 ..]
+#pragma unroll
+    for (int i = 1; i <= 3; ++i) {
+        if (warp < 2 * i) {
+            const int n0 = 8 * warp;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int ks = 0; ks < i; ++ks) {
+                uint32_t ah[4], al[4], bh[2], bl[2];
+                frag_a(sW + 8 * (i - 1) * i + 16 * ks, LW, lane, ah, al);   // X_i, k block ks
+                frag_b(sAT + (16 * ks) * FST + n0, FST, lane, bh, bl);     // T[ks block, n0 ..]
+                mma3(d, ah, al, bh, bl);
+            }
+            float *o = sAT + (16 * i) * FST + n0 + 2 * c;
+            *reinterpret_cast<float2 *>(o + g * FST) = make_float2(-d[0], -d[1]);
+            *reinterpret_cast<float2 *>(o + (g + 8) * FST) = make_float2(-d[2], -d[3]);
+        }
+        ptx::named_sync(bar, 256);
+    }
 }
 
 // ---------------------------------------------------------------------------
