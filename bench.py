@@ -387,7 +387,7 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     ms = dist.max(sum(times) / len(times))
     in_b = 2 if w.dtype == "bf16" else 4
     res = {"workload": w.name, "path": path, "ms_per_step": ms, "spread": spread(times),
-           "launches_per_step": launches_per_call(path, d)}
+           "launches_per_step": launches_per_call(path, nws)}
     if kind == "decode":
         bytes_launch = run_bytes(B, T, H, w.n_k, d, in_b)
         achieved = bytes_launch / (ms / 1e3) / 1e9
@@ -425,10 +425,11 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     return res
 
 
-def launches_per_call(path, d):
-    """Kernels one call launches: the chunked path at head_dim 256 runs the
-    chunk-transform kernel and then the state kernel; every other path one."""
-    return 2 if (path == "chunked" and d == 256) else 1
+def launches_per_call(path, workspace_bytes):
+    """Kernels one call launches.  A chunked call that needs a workspace
+    (head_dim 256, and head_dim 128 with few (sequence, head) pairs) runs the
+    chunk-transform kernel and then the state kernel; every other call one."""
+    return 2 if (path == "chunked" and workspace_bytes > 0) else 1
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -19,20 +19,31 @@
 // ggml-gated-delta-net" model card, section "Ops": one dispatch per run of
 // steps, state [value][key], 1/sqrt(head_dim) output scale, log-domain gate.
 //
-// GB300 mapping.  One CTA owns one (sequence, head) and a block of BV value
-// rows of the state (rows are independent), and walks the chunks in order:
-//   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile), the
-//      V block, and plain loads bring g, beta.
+// GB300 mapping.  The chunk transform Z = [T; P T] (128 x 64) depends on
+// K, Q and the gates only; the state walk needs Z and the state.  Three
+// kernels share the steps below:
+//   - chunked_d128_kernel (head_dim 64 and 128): one CTA per (sequence,
+//     head) holds the whole state in TMEM, value rows on lanes, and runs
+//     two warp-specialised streams: 8 warps build Z one chunk ahead, 8 warps
+//     walk the state.
+//   - chunk_z_kernel + chunked_kernel (head_dim 256, and head_dim 128 with
+//     few (sequence, head) pairs): persistent CTAs write every chunk's Z to
+//     a workspace; the state walk then runs one CTA per block of 64 value
+//     rows, keys on lanes, the fp32 state in registers.
+// Per chunk:
+//   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile) and
+//      V; plain loads bring g, beta.
 //   2. MMA  [K;Q] K^T -> TMEM (M=128, N=64): K K^T and Q K^T in one tile.
-//   3. CUDA cores: A and P from it, T = (I + A)^-1 by 16x16 blocks, P T; the
+//   3. A and P from it; T = (I + A)^-1 by 16x16 blocks (diagonal blocks on
+//      CUDA cores, block products on warp-level MMAs); MMA  P T; the
 //      stacked Z = [T; P T] is written as bf16 hi + lo (two bf16 terms).
 //   4. MMA  [K;Q] S0^T -> TMEM: both K S0^T (for R) and Q S0^T (for O).
 //   5. R = beta V - beta gamma K S0^T, written as bf16 hi + lo.
 //   6. MMA  Z R -> TMEM: rows 0-63 are U = T R, rows 64-127 are P T R = P U.
 //   7. O = gamma Q S0^T + P U, scaled, to global; U scaled by
 //      exp(G_{C-1} - G_r) and written as bf16 hi + lo.
-//   8. MMA  K^T U~ -> TMEM: the transposed state increment, keys on lanes.
-//   9. S = gamma_{C-1} S + dS^T in fp32 registers; bf16 hi + lo for step 4.
+//   8. MMA  U~^T K (or K^T U~) -> TMEM: the state increment.
+//   9. S = gamma_{C-1} S + dS in fp32; bf16 hi + lo for step 4.
 // Only raw bf16 inputs enter an MMA unsplit; every derived operand (S, Z,
 // R, U~) is carried as two bf16 terms so that products keep ~16 mantissa
 // bits, and all accumulation is fp32 in TMEM.  Waits on mbarriers are
@@ -268,7 +279,7 @@ __device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int b
 // value block) into the workspace.  Persistent CTAs walk the chunks:
 //   1. TMA brings K and Q (stacked per 64-key slab), plain loads the gates;
 //   2. MMA [K;Q] K^T -> TMEM (M = 128, N = 64, K = D): K K^T and Q K^T;
-//   3. CUDA cores: A and P, T = (I + A)^-1 by 16 x 16 blocks, P T, and
+//   3. A and P, T = (I + A)^-1 by 16 x 16 blocks, MMA [P hi; P lo] T, and
 //      Z = [T; P T] as bf16 hi + lo in the swizzled tile layout;
 //   4. one bulk copy writes the 32 KB tile to the workspace.
 template <int D>
