@@ -434,8 +434,9 @@ def launches_per_call(path, workspace_bytes):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_decode24_us(W, min_seconds):
-    """The float64 C oracle, as it stands, on the 24-layer decode step."""
+def oracle_decode24_us(W, min_seconds, n_threads=0):
+    """The float64 C oracle, as it stands, on the 24-layer decode step
+    (n_threads 0: every OpenMP thread)."""
     import numpy as np
     import oracle
     oracle.build()
@@ -445,13 +446,14 @@ def oracle_decode24_us(W, min_seconds):
     t0 = time.perf_counter()
     while True:
         for x in layers:
-            oracle.recurrent_c(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"])
+            oracle.recurrent_c(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"],
+                               n_threads=n_threads)
         steps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds:
             break
     _ = np
-    return el / steps * 1e6, steps, oracle.max_threads()
+    return el / steps * 1e6, steps, (n_threads or oracle.max_threads())
 
 
 def oracle_prefill_tokens_per_s(W, w, seconds_hint=3.0):
@@ -584,9 +586,12 @@ def main():
     cpu = None
     if dist.rank == 0:
         us, n, cores = oracle_decode24_us(W, args.oracle_seconds)
+        us1, n1, _ = oracle_decode24_us(W, max(1.0, args.oracle_seconds / 4), n_threads=1)
         cpu = {"value": us, "unit": "us/step", "cores": cores, "kind": "oracle",
                "sample": f"{n} repeats of the full 24-layer decode step (float64 C, OpenMP over "
-                         f"(seq, head) pairs)"}
+                         f"(seq, head) pairs)",
+               "one_core": {"value": us1, "unit": "us/step", "cores": 1,
+                            "sample": f"{n1} repeats of the same step on one thread"}}
         for r in extra:
             if r["metric"] == "prefill tokens/s" and r["workload"] in (W.PREFILL_4K.name,
                                                                       W.PREFILL_16K.name):
