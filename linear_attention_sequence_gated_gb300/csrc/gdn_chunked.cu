@@ -193,20 +193,98 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], con
 
 // T = (I + A)^-1 for a strictly lower triangular 64x64 A stored in full
 // (zeros on and above the diagonal, row stride FST), in place, on 256
-// threads t = 0..255 (8 warps) sharing hardware barrier `bar`, with 16x16
-// blocks:
+// threads t = 0..255 (8 warps) sharing hardware barrier `bar`, with two
+// 32x32 diagonal blocks:
+//   1. T_00 = (I + A_00)^-1 and T_11 = (I + A_11)^-1 by column substitution
+//      on CUDA cores, one column per thread (warp 0: block 0, warp 1:
+//      block 1; every lane of a warp reads the same row of A, a broadcast)
+//   2. X = T_11 A_10 (32x32, into W): eight 16 x 8 tiles, warp-level MMAs
+//   3. T_10 = -X T_00: eight tiles, warp-level MMAs
+// which is block forward substitution: A_10 T_00 + (I + A_11) T_10 = 0.
+// The products are 16-row blocks, too small for a 128-row tensor-memory
+// MMA, so the warps use register-operand MMAs on bf16 hi / lo splits (three
+// terms, ~16 significant bits, fp32 accumulation).  The result is T in full
+// (zeros above the diagonal); entered and left with the matrix visible to
+// all participants.
+__device__ __forceinline__ void ut_transform32(float *sAT, float *sW, int t, int bar) {
+    constexpr int LW = 40;                            // row stride of W (32 x 32 fp32)
+    const int warp = t >> 5, lane = t & 31;
+    const int g = lane >> 2, c = lane & 3;
+    // 1. diagonal blocks: x = column j of T_bb, x[r] = -sum_{i<r} A[r][i] x[i]
+    //    below the diagonal (four partial sums per row)
+    float x[32];
+    const int blk = t >> 5, j = t & 31;
+    if (t < 64) {
+        const float *Ab = sAT + (blk * 32) * FST + blk * 32;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i4 = 0; i4 < 32; i4 += 4) {
+                if (i4 < r) {
+                    const float4 a = *reinterpret_cast<const float4 *>(Ab + r * FST + i4);
+                    acc[0] = fmaf(a.x, x[i4], acc[0]);
+                    if (i4 + 1 < r) acc[1] = fmaf(a.y, x[i4 + 1], acc[1]);
+                    if (i4 + 2 < r) acc[2] = fmaf(a.z, x[i4 + 2], acc[2]);
+                    if (i4 + 3 < r) acc[3] = fmaf(a.w, x[i4 + 3], acc[3]);
+                }
+            }
+            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            x[r] = (r == j) ? 1.f : ((r > j) ? -sum : 0.f);
+        }
+    }
+    ptx::named_sync(bar, 256);
+    if (t < 64) {
+        float *Tb = sAT + (blk * 32) * FST + blk * 32;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) Tb[r * FST + j] = x[r];
+    }
+    ptx::named_sync(bar, 256);
+    // 2. X = T_11 A_10: warp -> rows 16 m0 .. +15, columns 8 n0 .. +7
+    const int m0 = (warp >> 2) * 16, n0 = (warp & 3) * 8;
+    {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 32; ks += 16) {
+            uint32_t ah[4], al[4], bh[2], bl[2];
+            frag_a(sAT + (32 + m0) * FST + 32 + ks, FST, lane, ah, al);    // T_11 rows, k block
+            frag_b(sAT + (32 + ks) * FST + n0, FST, lane, bh, bl);         // A_10 k rows, n cols
+            mma3(d, ah, al, bh, bl);
+        }
+        float *w = sW + m0 * LW + n0 + 2 * c;
+        *reinterpret_cast<float2 *>(w + g * LW) = make_float2(d[0], d[1]);
+        *reinterpret_cast<float2 *>(w + (g + 8) * LW) = make_float2(d[2], d[3]);
+    }
+    ptx::named_sync(bar, 256);
+    // 3. T_10 = -X T_00 over A_10's place
+    {
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 32; ks += 16) {
+            uint32_t ah[4], al[4], bh[2], bl[2];
+            frag_a(sW + m0 * LW + ks, LW, lane, ah, al);                   // X rows, k block
+            frag_b(sAT + ks * FST + n0, FST, lane, bh, bl);                // T_00 k rows, n cols
+            mma3(d, ah, al, bh, bl);
+        }
+        float *o = sAT + (32 + m0) * FST + n0 + 2 * c;
+        *reinterpret_cast<float2 *>(o + g * FST) = make_float2(-d[0], -d[1]);
+        *reinterpret_cast<float2 *>(o + (g + 8) * FST) = make_float2(-d[2], -d[3]);
+    }
+    ptx::named_sync(bar, 256);
+}
+
+// The same T = (I + A)^-1 with four 16x16 diagonal blocks: shorter
+// column substitutions, two more rounds of MMAs.  Same operands, threads and
+// result as ut_transform32:
 //   1. T_ii = (I + A_ii)^-1 for the four diagonal blocks (column
 //      substitution on CUDA cores, one column per thread)
 //   2. X_i = T_ii A[i, :i] for i = 1..3, all at once (into W, 16 x 96 fp32):
 //      twelve 16 x 8 tiles, warp-level MMAs
 //   3. T[i, :i] = -X_i T[:i, :i] for i = 1, 2, 3 in turn (2i tiles each)
 // which is block forward substitution: (I + A)_ii T_ij + sum_k A_ik T_kj = 0.
-// Every product is a 16-row block, too small for a 128-row tensor-memory
-// MMA, so the warps use register-operand MMAs on bf16 hi / lo splits
-// (three terms, ~16 significant bits, fp32 accumulation).  The result is T
-// in full (zeros above the diagonal); entered and left with the matrix
-// visible to all participants.
-__device__ __forceinline__ void ut_transform(float *sAT, float *sW, int t, int bar) {
+// Measured faster than ut_transform32 where the transform stream limits the
+// chunk (head_dim 64), slower at head_dim 128.
+__device__ __forceinline__ void ut_transform16(float *sAT, float *sW, int t, int bar) {
     constexpr int LW = 96;                            // row stride of W
     const int warp = t >> 5, lane = t & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -420,7 +498,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         ptx::tc_fence_before();
         __syncthreads();
-        ut_transform(sA, sW, tid, 0);                 // T in place over A; W dead afterwards
+        ut_transform32(sA, sW, tid, 0);               // T in place over A; W dead afterwards
         {                                             // T as hi / lo into Z rows 0-63
             const int r = tid >> 2, c0 = (tid & 3) * 16;
             float t[16];
@@ -899,8 +977,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 //     R^T  = beta V^T - beta gamma (K S^T)^T                   (CUDA cores)
 //     [U^T | (P U)^T] = R^T Z^T    (one N = 128 product, B = Z rows)
 //     S   += (diag(exp(G_C - G)) U)^T K   (S pre-scaled by gamma_C; B = K MN-major)
-//     O    = (gamma Q S^T + P U) / sqrt(d): staged in shared memory, one TMA
-//            store per chunk
+//     O    = (gamma Q S^T + P U) / sqrt(d): staged in shared memory (at
+//            head_dim 128 in the chunk's Z buffer, while the S product
+//            runs), one TMA store per chunk
 // The streams hand over through mbarriers: TMA stage full, V full, gates
 // ready (4 sets), Z ready / Z free (2 buffers), and each stream's MMA
 // completions.  For head_dim 64 the same code runs with TMEM lanes 64-127
@@ -916,11 +995,11 @@ constexpr int OFF_V = 65536;            // V of one chunk (2 boxes x 64 rows x 1
 constexpr int OFF_Z = 81920;            // 2 buffers x {Z hi, Z lo} (128 rows x 128 B each)
 constexpr int OFF_PP = 147456;          // P hi (rows 0-63) | P lo (rows 64-127)
 constexpr int OFF_AT = 163840;          // A, then T in place: fp32 64 x FST
-constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 96 fp32
+constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 96 or 32 x 40 fp32
 constexpr int OFF_RT = 187392;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
 constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-decay}
 constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
-static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT, "scratch overlaps R^T");
+static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT && 16 * 96 >= 32 * 40, "scratch overlaps R^T");
 static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
 static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
 // TMEM columns
@@ -938,7 +1017,8 @@ struct Shared {
     uint64_t qk_full[2];   // TMA: [K;Q] of the chunk in the stage has landed
     uint64_t v_full;       // TMA: V of the chunk has landed
     uint64_t z_ready[2];   // transform stream: Z = [T; P T] of the chunk is in its buffer
-    uint64_t z_free[2];    // state stream MMA: the last reads of a Z buffer have completed
+    uint64_t z_free[2];    // state stream: the Z R product (and, at head_dim 128, the O
+                           // store that reuses the buffer) have finished reading it
     uint64_t g_ready[4];   // transform stream: the chunk's gate set is written
     uint64_t mma_s, mma_z; // each stream's MMA completions
     uint32_t tmem_base;
@@ -1022,6 +1102,14 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     float *__restrict__ out, int T, int H, int Hk, float scale,
                     int *status)
 {
+    // Where O is staged.  head_dim 128: in the chunk's Z buffer, so that it
+    // overlaps the S product, which still reads the R^T / U~^T buffer; the
+    // buffer then returns to the transform stream only after the O store has
+    // read it.  head_dim 64, where the transform stream limits the chunk: in
+    // the R^T buffer after the S product, so that Z buffers return as soon as
+    // the Z R product has read them.  (Measured: each choice is the faster
+    // one at its head_dim.)
+    constexpr bool kOInZ = (D == 128);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -1188,7 +1276,8 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::named_sync(BAR_Z, NS);
 
             // T = (I + A)^-1 in place
-            ut_transform(sAT, sW, t, BAR_Z);
+            if constexpr (D == 128) ut_transform32(sAT, sW, t, BAR_Z);
+            else ut_transform16(sAT, sW, t, BAR_Z);
 
             // T as hi / lo into rows 0-63 of this chunk's Z buffer, once the
             // state stream has finished with the chunk that used it before
@@ -1265,6 +1354,36 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
         ptx::tc_fence_before();
         ptx::named_sync(BAR_S, NS);
+
+        // O of a chunk into `stage` (32 KB or 16 KB, 1024-aligned) and out by
+        // one TMA store; TMEM columns read: X^T's Q half and (P U)^T
+        auto o_epilogue = [&](uint8_t *stage, const float *sGam, int t0) {
+            ptx::tc_fence_after();
+            if (vrow) {
+                const int v = row;
+                float *ot = reinterpret_cast<float *>(stage);
+#pragma unroll 1
+                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
+                    float xq[16], pu[16], gm[16];
+                    ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
+                    ptx::tmem_ld16(tl + C_PU + jc, pu);
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
+                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
+                    }
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) ot[(jc + j) * D + v] = fmaf(gm[j], xq[j], pu[j]) * scale;
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_sync(BAR_S, NS);
+            if (t == 0 && !*abort_flag) {
+                ptx::tma_store_4d(&tm_o, stage, 0, h, t0, b);
+                ptx::bulk_commit_group();
+            }
+        };
 
         for (int c = 0; c < n_chunks; ++c) {
             const int st = c & 1;
@@ -1346,7 +1465,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                                       ptx::smem_desc(bZ[part] + kk * 32, 16, 1024), idesc,
                                       part > 0 || kk > 0);
                 ptx::mma_commit(&sh.mma_s);
-                ptx::mma_commit(&sh.z_free[st]);
+                if constexpr (!kOInZ) ptx::mma_commit(&sh.z_free[st]);
             }
             wait(&sh.mma_s, mma_phase);
             mma_phase ^= 1;
@@ -1389,36 +1508,18 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 ptx::mma_commit(&sh.mma_s);
             }
 
-            wait(&sh.mma_s, mma_phase);
-            mma_phase ^= 1;
-            ptx::tc_fence_after();
-
-            // O = (gamma Q S^T + P U) / sqrt(d): staged as a [token][value] fp32
-            // tile in the R^T buffer (free now), written by one TMA store that
-            // clips tokens past T
-            if (vrow) {
-                const int v = row;
-                float *ot = reinterpret_cast<float *>(sRhi);
-#pragma unroll 1
-                for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
-                    float xq[16], pu[16], gm[16];
-                    ptx::tmem_ld16(tl + C_X + 64 + jc, xq);
-                    ptx::tmem_ld16(tl + C_PU + jc, pu);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
-                        gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
-                    }
-                    ptx::tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) ot[(jc + j) * D + v] = fmaf(gm[j], xq[j], pu[j]) * scale;
-                }
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_sync(BAR_S, NS);
-            if (t == 0 && !*abort_flag) {
-                ptx::tma_store_4d(&tm_o, sRhi, 0, h, t0, b);
-                ptx::bulk_commit_group();
+            // O = (gamma Q S^T + P U) / sqrt(d), staged as a [token][value]
+            // fp32 tile and written by one TMA store that clips tokens past T
+            if constexpr (kOInZ) {
+                o_epilogue(sZhi, sGam, t0);   // while the S product runs (it writes only S)
+                wait(&sh.mma_s, mma_phase);
+                mma_phase ^= 1;
+                ptx::tc_fence_after();
+            } else {
+                wait(&sh.mma_s, mma_phase);
+                mma_phase ^= 1;
+                ptx::tc_fence_after();
+                o_epilogue(sRhi, sGam, t0);   // the S product has finished reading U~
             }
             // this stage is free: bring chunk c + 2 into it
             if (t == 0 && c + 2 < n_chunks && !*abort_flag) issue_qk(c + 2);
@@ -1448,7 +1549,10 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             if (!last && vrow) ptx::tmem_st_wait();
-            if (t == 0) ptx::bulk_wait_read_all();   // the O tile has left the R^T buffer
+            if (t == 0) {
+                ptx::bulk_wait_read_all();               // the O tile has left its buffer
+                if constexpr (kOInZ) ptx::mbar_arrive(&sh.z_free[st]);
+            }
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
         }
