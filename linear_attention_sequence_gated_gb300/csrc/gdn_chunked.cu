@@ -1358,7 +1358,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         // O of a chunk into `stage` (32 KB or 16 KB, 1024-aligned) and out by
         // one TMA store; TMEM columns read: X^T's Q half and (P U)^T
         auto o_epilogue = [&](uint8_t *stage, const float *sGam, int t0) {
-            ptx::tc_fence_after();
+            if constexpr (kOInZ) ptx::tc_fence_after();   // else done after the S wait
             if (vrow) {
                 const int v = row;
                 float *ot = reinterpret_cast<float *>(stage);
