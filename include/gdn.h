@@ -140,10 +140,11 @@ int gdn_forward_ex(const void *q, const void *k, const void *v,
  * paper or the model card; it exists only for such callers.
  *
  * Same arguments and behaviour as gdn_forward_ex, without the workspace
- * arguments.  It calls no allocation routine.  The one path that needs
- * scratch (chunked, head_dim 256: 32 KiB per sequence, head and 64-token
- * chunk) uses a fixed array of GDN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the
- * library, held by every GPU that loads the library until the process exits.
+ * arguments.  It calls no allocation routine.  The chunked calls that need
+ * scratch (head_dim 256, and head_dim 128 with fewer than 80 (sequence, head)
+ * pairs: 32 KiB per sequence, head and 64-token chunk) use a fixed array of
+ * GDN_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library, held by every GPU
+ * that loads the library until the process exits.
  * A call that would need more returns GDN_ERR_SCRATCH before touching the
  * GPU; gdn_workspace_bytes() tells how much a call needs.
  * All calls share the array: calls that may overlap on the GPU (different
@@ -161,7 +162,10 @@ int gdn_forward_noalloc(const void *q, const void *k, const void *v,
                         int dtype, int path, gdn_stream_t stream);
 
 /* Bytes of device workspace gdn_forward_ex needs for these sizes, dtype and
- * path (0 when the selected path needs none).  Returns 0 on invalid sizes. */
+ * path (0 when the selected path needs none).  Only chunked calls need one:
+ * head_dim 256, and head_dim 128 with fewer than 80 (sequence, head) pairs,
+ * which run a chunk-transform kernel and a state kernel; 32 KiB per
+ * sequence, head and 64-token chunk.  Returns 0 on invalid sizes. */
 size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
                            int dtype, int path);
 

@@ -308,10 +308,10 @@ int gdn_selftest_wait_timeout(gdn_stream_t stream) {
 // at all once they are running: a serving process whose framework has
 // reserved the whole device up front for its own arena, or a decode loop in
 // which an allocation (and the device synchronisation cudaMalloc can imply)
-// would stall the step.  For them the one path that needs scratch -- the
-// head_dim 256 chunked path, which keeps a 32 KiB transform tile per
-// (sequence, head, 64-token chunk) -- takes its scratch from this fixed array
-// instead.  The array is part of the library image: every GPU that loads the
+// would stall the step.  For them the chunked calls that need scratch --
+// head_dim 256, and head_dim 128 with few (sequence, head) pairs, which keep
+// a 32 KiB transform tile per (sequence, head, 64-token chunk) -- take it
+// from this fixed array instead.  The array is part of the library image: every GPU that loads the
 // library holds these 64 MiB until the process exits.  Calls share it, so two
 // calls that overlap on the GPU (different streams, no ordering between them)
 // race on it.  Nothing in it has to start at zero: the transform kernel writes

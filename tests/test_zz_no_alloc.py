@@ -2,9 +2,10 @@
 
 gdn_forward_noalloc serves callers that cannot allocate device memory while
 they run (a framework that has reserved the device for its own arena, a
-decode loop that must not stall on an allocation).  The one path that needs
-scratch -- chunked, head_dim 256 -- then uses a fixed 64 MiB array inside the
-library instead of caller or stream-ordered memory.  These tests call it
+decode loop that must not stall on an allocation).  The chunked calls that
+need scratch -- head_dim 256, and head_dim 128 with few (sequence, head)
+pairs -- then use a fixed 64 MiB array inside the library instead of caller
+or stream-ordered memory.  These tests call it
 through the C ABI twice in a row, with different inputs (the array keeps the
 previous call's contents), and compare each result with the existing entry
 point's on the same inputs, within the bf16 parity bound used by the other
@@ -65,16 +66,21 @@ def test_two_calls_in_a_row_match_the_existing_entry_point(L):
         assert rel_err(st, ref_st) <= TOL
 
 
-def test_paths_without_scratch_and_auto(L):
-    # head_dim 128 needs no scratch: the call goes straight through
-    w = W.Workload("noalloc_d128", 2, 300, 4, 128, "bf16", 0.0, 0.02, seed=73)
-    inp = W.make_inputs(w, "cuda")
-    ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
-                                  inp["state"])
-    out, st = torch.empty_like(ref_out), torch.empty_like(ref_st)
-    assert noalloc(L, inp, out, st, path=gdn.PATHS["auto"]) == gdn.OK
-    torch.cuda.synchronize()
-    assert rel_err(out, ref_out) <= TOL and rel_err(st, ref_st) <= TOL
+def test_head_dim_128_with_and_without_scratch_and_auto(L):
+    # 8 (sequence, head) pairs: the two-kernel path, which takes scratch;
+    # 96 pairs: the one-kernel path, which needs none and goes straight through
+    for H, seed in ((4, 73), (48, 74)):
+        w = W.Workload(f"noalloc_d128_h{H}", 2, 300, H, 128, "bf16", 0.0, 0.02, seed=seed)
+        need = L.gdn_workspace_bytes(w.B, w.T, w.H, w.d, gdn.DTYPE_BF16, gdn.PATHS["auto"])
+        assert (need > 0) == (w.B * w.H < 80)
+        inp = W.make_inputs(w, "cuda")
+        ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                      inp["state"])
+        out, st = torch.empty_like(ref_out), torch.empty_like(ref_st)
+        assert noalloc(L, inp, out, st, path=gdn.PATHS["auto"]) == gdn.OK
+        torch.cuda.synchronize()
+        assert gdn.device_status() == gdn.OK
+        assert rel_err(out, ref_out) <= TOL and rel_err(st, ref_st) <= TOL
 
 
 def test_rejects_calls_beyond_the_fixed_scratch(L):
