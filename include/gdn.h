@@ -175,7 +175,7 @@ size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim,
  * least T_switch tokens, everything else runs the recurrent path.  T_switch
  * was measured on GB300 and depends on head_dim and on the number of
  * (sequence, head) pairs P = n_seqs * n_heads:
- *   head_dim 64: 48 (P < 1024) or 64;  128: 56 (P < 128) or 24;
+ *   head_dim 64: 48 (P < 1024) or 64;  128: 72 (P < 48), 44 (P < 80) or 24;
  *   256: 32 (P < 128) or 24. */
 int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype);
 

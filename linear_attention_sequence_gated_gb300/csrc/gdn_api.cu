@@ -80,7 +80,9 @@ int chunked_min_tokens(long long pairs, int head_dim) {
     const bool many = pairs >= 128;
     switch (head_dim) {
         case 64: return pairs >= 1024 ? 64 : 48;
-        case 128: return many ? 24 : 56;
+        // fewer than 80 pairs run the two-kernel chunked path (a fixed cost of
+        // two launches and a transform pass), 80 or more the one-kernel path
+        case 128: return pairs >= 80 ? 24 : (pairs >= 48 ? 44 : 72);
         case 256: return many ? 24 : 32;
         default: return INT_MAX;
     }

@@ -71,8 +71,9 @@ def test_workspace_and_path_queries(L):
     assert gdn.select_path(1, 5, 32, 32) == "recurrent"
     assert gdn.select_path(1, 4096, 32, 32) == "recurrent"            # no chunked d = 32
     # measured switch points: (pairs, head_dim) -> first chunked length
-    for pairs, d, t_switch in ((32, 64, 48), (256, 64, 48), (2048, 64, 64), (32, 128, 56),
-                               (128, 128, 24), (2048, 128, 24), (32, 256, 32), (256, 256, 24)):
+    for pairs, d, t_switch in ((32, 64, 48), (256, 64, 48), (2048, 64, 64), (32, 128, 72),
+                               (64, 128, 44), (96, 128, 24), (128, 128, 24), (2048, 128, 24),
+                               (32, 256, 32), (256, 256, 24)):
         B, H = pairs // 32, 32
         assert gdn.select_path(B, t_switch - 1, H, d) == "recurrent"
         assert gdn.select_path(B, t_switch, H, d) == "chunked"
