@@ -156,6 +156,42 @@ def test_head_dims_dtypes_lengths(d, dtype, T):
         assert e_out <= tol and e_st <= tol, (path, e_out, e_st)
 
 
+# At head_dim 128 the chunked path has two kernels: one CTA per (sequence,
+# head) pair when there are at least 80 pairs, a chunk-transform pass plus a
+# state walk on value-row blocks below that.  The small cases above (6 pairs)
+# take the second; these take the first, with ragged tails and fewer key heads.
+ONE_KERNEL_D128_PAIRS = 80
+
+
+@pytest.mark.parametrize("T", [1, 7, 63, 64, 65, 200, 1000])
+def test_head_dim_128_one_kernel_chunked_path(T):
+    w = W.Workload("d128_many_pairs", 2, T, 48, 128, "bf16", 0.0, 0.02, seed=78)
+    assert w.B * w.H >= ONE_KERNEL_D128_PAIRS
+    assert gdn.workspace_bytes(w.B, w.T, w.H, w.d, "bf16", "chunked") == 0
+    check(W.make_inputs(w, "cuda"), "bf16", "chunked")
+
+
+def test_head_dim_128_one_kernel_chunked_path_key_heads_and_carry():
+    """Fewer key heads (48 value heads over 12) on the one-kernel path, and
+    one call against two calls split off a chunk boundary."""
+    w = W.Workload("d128_many_pairs_gqa", 2, 200, 48, 128, "bf16", 0.0, 0.02, seed=79)
+    inp = W.make_inputs(w, "cuda")
+    inp["q"] = inp["q"][:, :, :12].contiguous()
+    inp["k"] = inp["k"][:, :, :12].contiguous()
+    ref_out, ref_st = run_oracle(inp)
+    out, st = run_gpu(inp, "chunked")
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+    t1 = 100
+    a = {key: (val[:, :t1].contiguous() if key != "state" else val) for key, val in inp.items()}
+    b = {key: (val[:, t1:].contiguous() if key != "state" else None) for key, val in inp.items()}
+    oa, sa = run_gpu(a, "chunked")
+    b["state"] = sa
+    ob, sb = run_gpu(b, "chunked")
+    e_out, e_st = errs(torch.cat([oa, ob], dim=1), sb, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+
+
 @pytest.mark.parametrize("shift", [-2.0, 2.0, 6.0])
 def test_gate_regimes(shift):
     """Slow (alpha ~ 0.88), fast (~0.12) and near-total (~0.002) decay."""
