@@ -166,6 +166,8 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
     for t in tensors:
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on one CUDA device")
     if tuple(out.shape) != (B, T, H, d) or out.dtype != torch.float32:
         raise ValueError("out must be (n_seqs, n_tokens, n_heads, head_dim) fp32")
     if tuple(state_out.shape) != (B, H, d, d) or state_out.dtype != torch.float32:
@@ -225,6 +227,8 @@ def flash_attn(q, k, v, mask=None, scale=None, *, out=None, stream=None):
     for t in tensors:
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError("all tensors must be contiguous CUDA tensors")
+        if t.device != q.device:
+            raise ValueError("all tensors must be on one CUDA device")
     if tuple(out.shape) != (B, n_q, H, dv) or out.dtype != torch.float32:
         raise ValueError("out must be (n_seqs, n_q, n_heads, head_dim) fp32")
     if scale is None:
