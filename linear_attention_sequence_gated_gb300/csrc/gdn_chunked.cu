@@ -34,8 +34,8 @@
 //   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile) and
 //      V; plain loads bring g, beta.
 //   2. MMA  [K;Q] K^T -> TMEM (M=128, N=64): K K^T and Q K^T in one tile.
-//   3. A and P from it; T = (I + A)^-1 by 16x16 blocks (diagonal blocks on
-//      CUDA cores, block products on warp-level MMAs); MMA  P T; the
+//   3. A and P from it; T = (I + A)^-1 by 32x32 or 16x16 blocks (diagonal
+//      blocks on CUDA cores, block products on warp-level MMAs); MMA  P T; the
 //      stacked Z = [T; P T] is written as bf16 hi + lo (two bf16 terms).
 //   4. MMA  [K;Q] S0^T -> TMEM: both K S0^T (for R) and Q S0^T (for O).
 //   5. R = beta V - beta gamma K S0^T, written as bf16 hi + lo.
@@ -68,7 +68,8 @@ constexpr int C = 64;            // chunk length (tokens)
 constexpr int NT = 256;          // threads per CTA (two warpgroups)
 constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrices (16-B rows)
 
-// Shared-memory and TMEM map of the state kernel (head_dim 256).  The chunk
+// Shared-memory and TMEM map of the state kernel (head_dim 256, and 128 with
+// few pairs).  The chunk
 // transform Z = [T; P T] arrives ready-made from the workspace (written by
 // chunk_z_kernel), so a CTA only carries BV = 64 value rows of the state.
 template <int D>
@@ -352,12 +353,13 @@ __device__ __forceinline__ void ut_transform16(float *sAT, float *sW, int t, int
 }
 
 // ---------------------------------------------------------------------------
-// Chunk transform for head_dim 256: Z = [T; P T] of every (sequence, head,
-// chunk), independent of the state, computed once per chunk (not once per
-// value block) into the workspace.  Persistent CTAs walk the chunks:
+// Chunk transform for head_dim 256, and for head_dim 128 with few (sequence,
+// head) pairs: Z = [T; P T] of every (sequence, head, chunk), independent of
+// the state, computed once per chunk (not once per value block) into the
+// workspace.  Persistent CTAs walk the chunks:
 //   1. TMA brings K and Q (stacked per 64-key slab), plain loads the gates;
 //   2. MMA [K;Q] K^T -> TMEM (M = 128, N = 64, K = D): K K^T and Q K^T;
-//   3. A and P, T = (I + A)^-1 by 16 x 16 blocks, MMA [P hi; P lo] T, and
+//   3. A and P, T = (I + A)^-1 by 32 x 32 blocks, MMA [P hi; P lo] T, and
 //      Z = [T; P T] as bf16 hi + lo in the swizzled tile layout;
 //   4. one bulk copy writes the 32 KB tile to the workspace.
 template <int D>
@@ -1630,8 +1632,9 @@ int sm_count() {
     return n;
 }
 
-// head_dim 256: the chunk transform for every chunk into the workspace, then
-// the state walk (4 CTAs per head, 64 value rows each) reading it.
+// head_dim 256, and head_dim 128 with few pairs: the chunk transform for
+// every chunk into the workspace, then the state walk (D / 64 CTAs per head,
+// 64 value rows each) reading it.
 template <int D>
 cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     using CF = Cfg<D>;
