@@ -425,6 +425,57 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     return res
 
 
+def run_decode_steady(torch, gdn, W, w, dev, args, dist, peaks, n_bufs=4):
+    """Batched decode in steady state: K back-to-back calls between one pair
+    of events, each updating in place one of `n_bufs` state buffers in turn
+    (each larger than L2), with no flush in between.  Every call's state
+    write-back then lands inside the timed window, as it does in a decode
+    loop where step n + 1 pays for step n's writes."""
+    B, T, H, d = w.B, w.T, w.H, w.d
+    inp = W.make_inputs(w, dev)
+    states = [inp["state"].clone() for _ in range(n_bufs)]
+    out = torch.empty((B, T, H, d), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    calls = max(args.steps, 4 * n_bufs)
+
+    def call(i):
+        st = states[i % n_bufs]
+        gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st, out=out,
+                    state_out=st, path="recurrent")
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, n_bufs)):
+            call(i)
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(calls):
+            call(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+    if gdn.device_status() != gdn.OK:
+        raise RuntimeError(f"device status after {w.name} (steady state)")
+    ms = dist.max(a.elapsed_time(b) / calls)
+    by = run_bytes(B, T, H, w.n_k, d, 2 if w.dtype == "bf16" else 4)
+    ach = by / (ms / 1e3) / 1e9
+    del inp, states, out
+    return {"workload": w.name + "_steady", "path": "recurrent", "metric": "decode us/step",
+            "value": ms * 1e3, "unit": "us/step", "ms_per_step": ms, "launches_per_step": 1,
+            "launches_timed": calls,
+            "how": f"{calls} back-to-back in-place calls over {n_bufs} rotating state buffers "
+                   "(128 MiB each), one pair of CUDA events, no L2 flush: each call's state "
+                   "write-back lands inside the window",
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": ach / peaks["hbm_gbs"], "traffic": None,
+                         "bytes_per_launch": by,
+                         "note": "algorithmic bytes; in steady state the DRAM bytes per call "
+                                 "equal them (state read + written back once)"}}
+
+
 def launches_per_call(path, workspace_bytes):
     """Kernels one call launches.  A chunked call that needs a workspace
     (head_dim 256, and head_dim 128 with few (sequence, head) pairs) runs the
@@ -478,6 +529,48 @@ def oracle_prefill_tokens_per_s(W, w, seconds_hint=3.0):
     return {"value": token_heads_per_s / w.H, "unit": "tokens/s", "cores": nthr, "kind": "oracle",
             "sample": f"{pairs} (seq, head) pairs x {T} tokens, {reps} repeats, scaled to "
                       f"{w.H} heads"}
+
+
+def oracle_decode_us(W, w, seconds_hint=2.0):
+    """The float64 C oracle on a whole decode / short-run workload (every
+    (sequence, head) pair), repeated for about `seconds_hint` seconds."""
+    import oracle
+    oracle.build()
+    x = W.to_numpy_f32(W.make_inputs(w, "cpu"))
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.recurrent_c(x["q"], x["k"], x["v"], x["g"], x["beta"], x["state"])
+        reps += 1
+        if time.perf_counter() - t0 >= seconds_hint:
+            break
+    el = time.perf_counter() - t0
+    return {"value": el / reps * 1e6, "unit": "us/step", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"the whole workload ({w.B * w.H} (seq, head) pairs x {w.T} token(s)), "
+                      f"{reps} repeats"}
+
+
+def oracle_attn_us(W, w, seconds_hint=2.0):
+    """The float64 numpy attention oracle on a bounded sample of a decode
+    attention workload (whole sequences), scaled to one call."""
+    from oracle.attn import attention
+    nb = 1 if w.B > 1 else w.B
+    x = W.make_attn_inputs(w.replace(B=nb), "cpu")
+    f64 = lambda t: None if t is None else t.double().numpy()
+    q, k, v, m = f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["mask"])
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        attention(q, k, v, m)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds_hint:
+            break
+    el = time.perf_counter() - t0
+    return {"value": el / reps * 1e6 * (w.B / nb), "unit": "us/call", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{nb} of {w.B} sequence(s), {reps} repeats, scaled to the whole call "
+                      "(numpy float64, one Python thread)"}
 
 
 # ------------------------------------------------------------------ main
@@ -546,11 +639,19 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     timer = Timer(torch, stream, flush)
 
-    specs = [(W.DECODE_B64, "decode"), (W.MULTITOKEN_B64_T4, "decode"),
-             (W.DECODE_B64_HK16, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill"),
-             (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill")]
+    # the entries with a stated target (batched decode, the 4k and 8 x 16k
+    # head_dim-128 prefills) come last in "workloads"
+    specs = [(W.MULTITOKEN_B64_T4, "decode"), (W.DECODE_B64_HK16, "decode"),
+             (W.PREFILL_16K_D64, "prefill"), (W.PREFILL_16K_D256, "prefill"),
+             (W.DECODE_B64, "decode"), (W.PREFILL_4K, "prefill"), (W.PREFILL_16K, "prefill")]
     if args.only and args.only in W.ATTN_BY_NAME:
         r = run_attn(torch, gdn, W, W.ATTN_BY_NAME[args.only], dev, timer, args, dist, peaks)
+        if dist.rank == 0:
+            print(json.dumps(r))
+        dist.close()
+        return
+    if args.only and args.only == W.DECODE_B64.name + "_steady":
+        r = run_decode_steady(torch, gdn, W, W.DECODE_B64, dev, args, dist, peaks)
         if dist.rank == 0:
             print(json.dumps(r))
         dist.close()
@@ -571,16 +672,21 @@ def main():
     extra = []
     launches = head["launches"]
     if not args.no_extra:
-        for w, kind in specs:
-            r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
-            launches += r["launches_per_step"] * args.steps
-            extra.append(r)
-            torch.cuda.empty_cache()
         for w in W.ATTN_ALL:
             r = run_attn(torch, gdn, W, w, dev, timer, args, dist, peaks)
             launches += r["launches_per_step"] * args.steps
             extra.append(r)
             torch.cuda.empty_cache()
+        for w, kind in specs:
+            r = run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind)
+            launches += r["launches_per_step"] * args.steps
+            extra.append(r)
+            torch.cuda.empty_cache()
+            if w is W.DECODE_B64:
+                r = run_decode_steady(torch, gdn, W, w, dev, args, dist, peaks)
+                launches += r["launches_timed"]
+                extra.append(r)
+                torch.cuda.empty_cache()
     clocks.stop()
 
     cpu = None
@@ -592,10 +698,18 @@ def main():
                          f"(seq, head) pairs)",
                "one_core": {"value": us1, "unit": "us/step", "cores": 1,
                             "sample": f"{n1} repeats of the same step on one thread"}}
+        cpu_decode = {}
         for r in extra:
-            if r["metric"] == "prefill tokens/s" and r["workload"] in (W.PREFILL_4K.name,
-                                                                      W.PREFILL_16K.name):
-                r["cpu_baseline"] = oracle_prefill_tokens_per_s(W, W.BY_NAME[r["workload"]])
+            name = r["workload"]
+            if r["metric"] == "prefill tokens/s":
+                r["cpu_baseline"] = oracle_prefill_tokens_per_s(W, W.BY_NAME[name])
+            elif r["metric"] == "decode us/step":
+                base = name[:-len("_steady")] if name.endswith("_steady") else name
+                if base not in cpu_decode:
+                    cpu_decode[base] = oracle_decode_us(W, W.BY_NAME[base])
+                r["cpu_baseline"] = cpu_decode[base]
+            elif r["path"] == "flash_attn":
+                r["cpu_baseline"] = oracle_attn_us(W, W.ATTN_BY_NAME[name])
 
     if dist.rank == 0:
         us = head["value"]

@@ -184,8 +184,10 @@ int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dty
  * supports_gated_delta_net(head_dim) ("Ops" table and the note that the
  * head dim must be asked, not assumed).  Returns a bit mask: bit 0 (1) =
  * the recurrent path supports head_dim, bit 1 (2) = the chunked path does
- * (for bf16 q/k/v).  0 means unsupported.  Supported: 32 (recurrent only),
- * 64, 128, 256 (both).
+ * (for bf16 q/k/v).  0 means unsupported.  Supported: 32 and 96 (recurrent
+ * only), 64, 128, 256 (both).  The model card's shape note says upstream
+ * covers a state row with 32 threads, so its head_dim is a multiple of 32 up
+ * to 128; every such width is served here, and 256 as well.
  */
 int gdn_supports(int head_dim);
 
@@ -216,8 +218,10 @@ int gdn_get_device_status(gdn_stream_t stream);
  *   mask together; arithmetic is float32 with exact upcast.
  * scale: finite float multiplying q . k (callers usually pass
  *   1 / sqrt(head_dim_k)).
- * Supported: 1 <= n_q <= 19 (else GDN_ERR_SHAPE), head_dim_k == head_dim_v in
- *   {64, 128, 256} (else GDN_ERR_HEADDIM), n_heads_kv dividing n_heads (else
+ * Supported: 1 <= n_q <= 19 (else GDN_ERR_SHAPE), head_dim_k and head_dim_v
+ *   each in {64, 128, 256}, equal or not (the model card's capability query
+ *   takes the two widths separately; else GDN_ERR_HEADDIM), n_heads_kv
+ *   dividing n_heads (else
  *   GDN_ERR_ARG); any n_kv >= 0.  A query whose keys are all masked with
  *   -inf, and every query when n_kv == 0, gets a zero output row.
  * q, k, v, out 16-byte aligned; mask aligned to its element size; out must

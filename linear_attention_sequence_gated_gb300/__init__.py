@@ -185,8 +185,8 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
 
 
 def flash_attn_supports(n_q: int, head_dim_k: int, head_dim_v: int) -> bool:
-    """Whether ``flash_attn`` serves this shape (fewer than 20 queries, equal
-    head dims of 64, 128 or 256)."""
+    """Whether ``flash_attn`` serves this shape (fewer than 20 queries; key and
+    value head dims each 64, 128 or 256, equal or not)."""
     return bool(lib().gdn_flash_attn_supports(int(n_q), int(head_dim_k), int(head_dim_v)))
 
 
@@ -194,10 +194,10 @@ def flash_attn(q, k, v, mask=None, scale=None, *, out=None, stream=None):
     """Decode attention: out[b, i, h] = softmax_j(scale q[b,h,i] . k[b,hk,j] +
     mask[b,0,i,j]) v[b,hk,j], hk = h // (n_heads / n_heads_kv).
 
-    q: (n_seqs, n_heads, n_q, d); k, v: (n_seqs, n_heads_kv, n_kv, d), all of
-    one dtype (fp32, bf16 or fp16); mask: (n_seqs, 1, n_q, n_kv) of the same
-    dtype, additive, or None; scale defaults to 1/sqrt(d).  Returns out
-    (n_seqs, n_q, n_heads, d) fp32.  ("marcsun13/ggml-gated-delta-net" model
+    q: (n_seqs, n_heads, n_q, dk); k: (n_seqs, n_heads_kv, n_kv, dk); v:
+    (n_seqs, n_heads_kv, n_kv, dv), all of one dtype (fp32, bf16 or fp16);
+    mask: (n_seqs, 1, n_q, n_kv) of the same dtype, additive, or None; scale
+    defaults to 1/sqrt(dk).  Returns out (n_seqs, n_q, n_heads, dv) fp32.  ("marcsun13/ggml-gated-delta-net" model
     card, section "flash_attn".)"""
     import math
     import torch
@@ -211,7 +211,7 @@ def flash_attn(q, k, v, mask=None, scale=None, *, out=None, stream=None):
     Hkv, n_kv = k.shape[1], k.shape[2]
     dv = v.shape[3]
     if tuple(k.shape) != (B, Hkv, n_kv, dk) or tuple(v.shape) != (B, Hkv, n_kv, dv):
-        raise ValueError(f"k, v: expected (n_seqs, n_heads_kv, n_kv, d), got {tuple(k.shape)}, "
+        raise ValueError(f"k, v: expected (n_seqs, n_heads_kv, n_kv, dk / dv), got {tuple(k.shape)}, "
                          f"{tuple(v.shape)}")
     tensors = [q, k, v]
     if mask is not None:
@@ -230,7 +230,7 @@ def flash_attn(q, k, v, mask=None, scale=None, *, out=None, stream=None):
         if t.device != q.device:
             raise ValueError("all tensors must be on one CUDA device")
     if tuple(out.shape) != (B, n_q, H, dv) or out.dtype != torch.float32:
-        raise ValueError("out must be (n_seqs, n_q, n_heads, head_dim) fp32")
+        raise ValueError("out must be (n_seqs, n_q, n_heads, dv) fp32")
     if scale is None:
         scale = 1.0 / math.sqrt(dk)
     with torch.cuda.device(q.device):

@@ -16,7 +16,7 @@ namespace {
 // here when a wait gives up.  One per device that loads the library.
 __device__ int g_device_status = 0;
 
-constexpr int kMaxDevices = 64;
+using gdn::kMaxDevices;
 int *g_status_ptr[kMaxDevices] = {};
 std::mutex g_status_mu;
 
@@ -257,7 +257,8 @@ int gdn_select_path(int n_seqs, int n_tokens, int n_heads, int head_dim, int dty
 
 int gdn_supports(int head_dim) {
     int caps = 0;
-    if (head_dim == 32 || head_dim == 64 || head_dim == 128 || head_dim == 256) caps |= 1;
+    if (head_dim == 32 || head_dim == 64 || head_dim == 96 || head_dim == 128 || head_dim == 256)
+        caps |= 1;
     if (gdn::chunked_supports(head_dim)) caps |= 2;
     return caps;
 }

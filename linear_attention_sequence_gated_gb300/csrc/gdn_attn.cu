@@ -175,35 +175,37 @@ __device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
     }
 }
 
-// Geometry for head_dim D and input type Tin.
-//   scores: KPL = D/64 lanes share a key (each a DQ = 64-element part of its
-//           row), so a step holds NKS = 32/KPL keys, one per lane group;
-//   P V:    every lane owns SL = D/32 consecutive value columns;
+// Geometry for key / query width DK, value width DV and input type Tin.
+//   scores: KPL = max(DK, DV)/64 lanes share a key (each a DQ = DK/KPL-element
+//           part of its row), so a step holds NKS = 32/KPL keys, one per lane
+//           group (wide value rows keep the step, and the ring, small);
+//   P V:    every lane owns SL = DV/32 consecutive value columns;
 //   a warp carries RG = 4 rows (query head of the group x query).
 // A warp's ring holds ST steps of NKS keys of k (rows padded by 16 bytes, so
 // that lanes reading different rows hit different banks) and v.
-template <int D, typename Tin> struct Geo {
+template <int DK, int DV, typename Tin> struct Geo {
     static constexpr int ELT = (int)sizeof(Tin);
-    static constexpr int KPL = D / 64;
+    static constexpr int KPL = (DK > DV ? DK : DV) / 64;
     static constexpr int NKS = 32 / KPL;
-    static constexpr int DQ = D / KPL;
-    static constexpr int SL = D / 32;
+    static constexpr int DQ = DK / KPL;
+    static constexpr int SL = DV / 32;
     static constexpr int RG = 4;
-    static constexpr int KST = D * ELT + 16;
-    static constexpr int VST = D * ELT;
+    static constexpr int KST = DK * ELT + 16;
+    static constexpr int VST = DV * ELT;
     static constexpr int STEP = NKS * (KST + VST);
     static constexpr int NW = ELT == 4 ? 4 : 8;       // warps per CTA
     static constexpr int ST = 2;                      // ring stages per warp
     static constexpr int NTHR = NW * 32;
     static constexpr int RING = NW * ST * STEP;
     // after the key loop the ring is reused for the merge buffers
-    static constexpr int WO = 0;                                  // [NW][RG][D] fp32
-    static constexpr int CO = WO + NW * RG * D * 4;               // [NW*RG][D] fp32
-    static constexpr int MERGE = CO + NW * RG * D * 4;
+    static constexpr int WO = 0;                                  // [NW][RG][DV] fp32
+    static constexpr int CO = WO + NW * RG * DV * 4;              // [NW*RG][DV] fp32
+    static constexpr int MERGE = CO + NW * RG * DV * 4;
     static constexpr int QOFF = RING > MERGE ? RING : MERGE;      // the CTA's q rows, fp32
-    static constexpr int SMEM = QOFF + NW * RG * D * 4;
+    static constexpr int SMEM = QOFF + NW * RG * DK * 4;
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST % 16 == 0 && STEP % 16 == 0 && QOFF % 16 == 0, "alignment");
+    static_assert(DQ % 8 == 0 && KPL * NKS == 32, "score split");
 };
 
 // Small per-CTA state outside the ring.
@@ -216,20 +218,20 @@ struct SmallSmem {
     float p[NW][NKS][RG];                             // a step's probabilities, [key][row]
 };
 
-template <int D, typename Tin>
-__global__ void __launch_bounds__(Geo<D, Tin>::NTHR, 1)
+template <int DK, int DV, typename Tin>
+__global__ void __launch_bounds__(Geo<DK, DV, Tin>::NTHR, 1)
 attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                    const Tin *__restrict__ v, const Tin *__restrict__ mask,
                    float *__restrict__ out, int H, int Hkv, int n_q, int n_kv, int n_rb, int n_rgc,
                    int CL, float scale)
 {
-    using G = Geo<D, Tin>;
+    using G = Geo<DK, DV, Tin>;
     constexpr int SL = G::SL, RG = G::RG, NW = G::NW, ST = G::ST, NTHR = G::NTHR;
     constexpr int NKS = G::NKS, DQ = G::DQ;
     extern __shared__ __align__(16) uint8_t ring[];
     __shared__ __align__(16) SmallSmem<NW, RG, NKS> sm;
-    float (*wo)[RG][D] = reinterpret_cast<float (*)[RG][D]>(ring + G::WO);
-    float (*co)[D] = reinterpret_cast<float (*)[D]>(ring + G::CO);
+    float (*wo)[RG][DV] = reinterpret_cast<float (*)[RG][DV]>(ring + G::WO);
+    float (*co)[DV] = reinterpret_cast<float (*)[DV]>(ring + G::CO);
     float *sQ = reinterpret_cast<float *>(ring + G::QOFF);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -259,8 +261,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const int ke = min(n_kv, kb + sps * NKS);
     const int n_steps = nr > 0 ? (ke - kb + NKS - 1) / NKS : 0;
 
-    const Tin *kg = k + (size_t)(b * Hkv + hk) * n_kv * D;
-    const Tin *vg = v + (size_t)(b * Hkv + hk) * n_kv * D;
+    const Tin *kg = k + (size_t)(b * Hkv + hk) * n_kv * DK;
+    const Tin *vg = v + (size_t)(b * Hkv + hk) * n_kv * DV;
     uint8_t *wring = ring + warp * ST * G::STEP;
     // stage `st` <- keys kb + NKS*step ..: k rows (padded), then v rows; rows
     // past the range are not copied (their scores are masked, their v rows skipped)
@@ -268,17 +270,21 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         if (step < n_steps) {
             const int j0 = kb + step * NKS;
             const int nk = min(NKS, ke - j0);
-            constexpr int CPR = D * G::ELT / 16;      // 16-byte copies per row
+            constexpr int CPK = DK * G::ELT / 16;     // 16-byte copies per k row
+            constexpr int CPV = DV * G::ELT / 16;     // ... per v row
             uint8_t *dk = wring + st * G::STEP;
             uint8_t *dv = dk + NKS * G::KST;
-            for (int c = lane; c < NKS * CPR; c += 32) {
-                const int g = c / CPR, x = c - g * CPR;
-                if (g < nk) {
+            for (int c = lane; c < NKS * CPK; c += 32) {
+                const int g = c / CPK, x = c - g * CPK;
+                if (g < nk)
                     cp_async16(dk + g * G::KST + x * 16,
-                               reinterpret_cast<const uint8_t *>(kg + (size_t)(j0 + g) * D) + x * 16);
+                               reinterpret_cast<const uint8_t *>(kg + (size_t)(j0 + g) * DK) + x * 16);
+            }
+            for (int c = lane; c < NKS * CPV; c += 32) {
+                const int g = c / CPV, x = c - g * CPV;
+                if (g < nk)
                     cp_async16(dv + g * G::VST + x * 16,
-                               reinterpret_cast<const uint8_t *>(vg + (size_t)(j0 + g) * D) + x * 16);
-                }
+                               reinterpret_cast<const uint8_t *>(vg + (size_t)(j0 + g) * DV) + x * 16);
             }
         }
         cp_async_commit();
@@ -288,17 +294,17 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
     // the CTA's rows of q, scaled, fp32 (rows past R: zeros); rows rbase + lr
     // are consecutive in q: head hk*rep + row / n_q, query row % n_q
-    for (int i = tid; i < rows_cta * (D / 8); i += NTHR) {
-        const int lr = i / (D / 8), c = i - lr * (D / 8);
+    for (int i = tid; i < rows_cta * (DK / 8); i += NTHR) {
+        const int lr = i / (DK / 8), c = i - lr * (DK / 8);
         const int rg = rbase + lr;
         float x[8];
         if (rg < R) {
-            ldg8(q + ((size_t)(b * H + hk * rep) * n_q + rg) * D + c * 8, x);
+            ldg8(q + ((size_t)(b * H + hk * rep) * n_q + rg) * DK + c * 8, x);
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
-        float4 *dst = reinterpret_cast<float4 *>(sQ + lr * D + c * 8);
+        float4 *dst = reinterpret_cast<float4 *>(sQ + lr * DK + c * 8);
         dst[0] = make_float4(scale * x[0], scale * x[1], scale * x[2], scale * x[3]);
         dst[1] = make_float4(scale * x[4], scale * x[5], scale * x[6], scale * x[7]);
     }
@@ -314,7 +320,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         for (int e = 0; e < SL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
     }
     const int key = lane % NKS, part = lane / NKS;    // score pass: this lane's key and row part
-    const float *qw = sQ + (rgc * RG) * D + part * DQ;
+    const float *qw = sQ + (rgc * RG) * DK + part * DQ;
 
     for (int step = 0; step < n_steps; ++step) {
         cp_async_wait<ST - 2>();                      // this step's copies (own lane) landed
@@ -339,7 +345,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
                 float qx[8];
-                lds8(qw + r * D + c * 8, qx);
+                lds8(qw + r * DK + c * 8, qx);
 #pragma unroll
                 for (int e = 0; e < 8; e += 2)
                     a2[r] = ffma2(make_float2(qx[e], qx[e + 1]), make_float2(kx[e], kx[e + 1]),
@@ -404,7 +410,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll 2
         for (int g = 0; g < nk; ++g) {
             Slice<Tin, SL> vr;
-            ld_slice<false>(vr, sv + g * D + lane * SL);
+            ld_slice<false>(vr, sv + g * DV + lane * SL);
             float vx[SL];
             unpack(vr, vx);
             const float4 p4 = *reinterpret_cast<const float4 *>(&sm.p[warp][g][0]);
@@ -449,8 +455,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         sm.cl[tid] = L;
     }
     __syncthreads();
-    for (int it = tid; it < rows_cta * D; it += NTHR) {
-        const int lr = it / D, col = it - lr * D;
+    for (int it = tid; it < rows_cta * DV; it += NTHR) {
+        const int lr = it / DV, col = it - lr * DV;
         const int g = lr / RG, r = lr - g * RG;
         float o = 0.f;
         for (int w = g; w < NW; w += n_rgc) o = fmaf(sm.wm[w][r], wo[w][r][col], o);
@@ -481,8 +487,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         sm.pl[tid] = L;
     }
     __syncthreads();
-    for (int it = rank * NTHR + tid; it < nr_cta * D; it += CL * NTHR) {
-        const int lr = it / D, col = it - lr * D;
+    for (int it = rank * NTHR + tid; it < nr_cta * DV; it += CL * NTHR) {
+        const int lr = it / DV, col = it - lr * DV;
         float o = 0.f;
 #pragma unroll
         for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
@@ -492,7 +498,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         const float L = sm.pl[lr];
         const int rg = rbase + lr;
         const int h = hk * rep + rg / n_q, i = rg % n_q;
-        out[(((size_t)b * n_q + i) * H + h) * D + col] = (L > 0.f) ? o / L : 0.f;
+        out[(((size_t)b * n_q + i) * H + h) * DV + col] = (L > 0.f) ? o / L : 0.f;
     }
     cluster_sync();                                   // peers are done reading this CTA
 }
@@ -500,21 +506,13 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 struct AttnProblem {
     const void *q, *k, *v, *mask;
     float *out;
-    int B, H, Hkv, n_q, n_kv, d;
+    int B, H, Hkv, n_q, n_kv, dk, dv;
     float scale;
 };
 
-int device_sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 1;
-    return n;
-}
-
-template <int D, typename Tin>
+template <int DK, int DV, typename Tin>
 cudaError_t launch(const AttnProblem &p, cudaStream_t stream) {
-    using G = Geo<D, Tin>;
+    using G = Geo<DK, DV, Tin>;
     constexpr int RG = G::RG, NWARP = G::NW;
     const int rep = p.H / p.Hkv;
     const long long R = (long long)rep * p.n_q;
@@ -523,36 +521,39 @@ cudaError_t launch(const AttnProblem &p, cudaStream_t stream) {
     while (n_rgc < NWARP && (long long)n_rgc * RG < R) n_rgc *= 2;
     const int n_ksc = NWARP / n_rgc;
     const int n_rb = (int)((R + (long long)n_rgc * RG - 1) / ((long long)n_rgc * RG));
-    // one-time set-up: shared memory size, clusters beyond the portable 8, and
-    // the largest cluster this kernel can actually be given
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    static int max_cl = 8;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(attn_decode_kernel<D, Tin>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
-        if (attr_err != cudaSuccess) return;
-        if (cudaFuncSetAttribute(attn_decode_kernel<D, Tin>,
+    // one-time set-up per device: shared memory size, clusters beyond the
+    // portable 8, and the largest cluster this kernel can actually be given
+    static PerDeviceOnce setup;
+    static int max_cl_of[kMaxDevices];
+    const cudaError_t attr_err = setup.run([] {
+        const int dev = current_device();
+        max_cl_of[dev] = 8;
+        cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<DK, DV, Tin>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, G::SMEM);
+        if (e != cudaSuccess) return e;
+        if (cudaFuncSetAttribute(attn_decode_kernel<DK, DV, Tin>,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
             cudaLaunchConfig_t q = {};
             q.gridDim = dim3(MAX_CLUSTER);
             q.blockDim = dim3(G::NTHR);
             q.dynamicSmemBytes = G::SMEM;
             int n = 0;
-            if (cudaOccupancyMaxPotentialClusterSize(&n, attn_decode_kernel<D, Tin>, &q) ==
+            if (cudaOccupancyMaxPotentialClusterSize(&n, attn_decode_kernel<DK, DV, Tin>, &q) ==
                     cudaSuccess && n >= 8)
-                max_cl = n < MAX_CLUSTER ? n : MAX_CLUSTER;
+                max_cl_of[dev] = n < MAX_CLUSTER ? n : MAX_CLUSTER;
         }
         (void)cudaGetLastError();                    // a refused query leaves the portable 8
+        return cudaSuccess;
     });
     if (attr_err != cudaSuccess) return attr_err;
+    const int max_cl = max_cl_of[current_device()];
     // CTAs per cluster: enough clusters x CTAs for about four waves of the GPU
     // (one CTA per SM; a partial last wave then costs little), but no more
     // CTAs than give every warp one step of keys.  A short or single-sequence
     // cache is spread over many SMs; a large batch keeps few CTAs per
     // (sequence, kv head, row block) and long key ranges per warp.
     const long long units = (long long)p.B * p.Hkv * n_rb;
-    const long long fill = (4LL * device_sm_count() + units - 1) / units;
+    const long long fill = (4LL * current_sm_count() + units - 1) / units;
     const long long per_cta = (long long)n_ksc * G::NKS;
     const long long by_keys = (p.n_kv + per_cta - 1) / per_cta;
     long long cl = fill < by_keys ? fill : by_keys;
@@ -573,25 +574,37 @@ cudaError_t launch(const AttnProblem &p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<D, Tin>, static_cast<const Tin *>(p.q),
+    return cudaLaunchKernelEx(&cfg, attn_decode_kernel<DK, DV, Tin>, static_cast<const Tin *>(p.q),
                               static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v),
                               static_cast<const Tin *>(p.mask), p.out, p.H, p.Hkv, p.n_q, p.n_kv,
                               n_rb, n_rgc, CL, p.scale);
 }
 
+template <int DK, typename Tin>
+cudaError_t launch_dv(const AttnProblem &p, cudaStream_t stream) {
+    switch (p.dv) {
+        case 64: return launch<DK, 64, Tin>(p, stream);
+        case 128: return launch<DK, 128, Tin>(p, stream);
+        case 256: return launch<DK, 256, Tin>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename Tin>
 cudaError_t launch_dtype(const AttnProblem &p, cudaStream_t stream) {
-    switch (p.d) {
-        case 64: return launch<64, Tin>(p, stream);
-        case 128: return launch<128, Tin>(p, stream);
-        case 256: return launch<256, Tin>(p, stream);
+    switch (p.dk) {
+        case 64: return launch_dv<64, Tin>(p, stream);
+        case 128: return launch_dv<128, Tin>(p, stream);
+        case 256: return launch_dv<256, Tin>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 constexpr int kMaxQueries = 19;   // the vector (decode) variant: fewer than 20 queries
 
-bool head_dims_ok(int dk, int dv) { return dk == dv && (dk == 64 || dk == 128 || dk == 256); }
+// key / query and value widths are independent: each of 64, 128 or 256
+bool head_dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+bool head_dims_ok(int dk, int dv) { return head_dim_ok(dk) && head_dim_ok(dv); }
 
 }  // namespace
 }  // namespace attn
@@ -616,8 +629,9 @@ int gdn_flash_attn(const void *q, const void *k, const void *v, const void *mask
     if (n_heads > 0 && (n_heads_kv < 1 || n_heads % n_heads_kv != 0)) return GDN_ERR_ARG;
     if (!std::isfinite(scale)) return GDN_ERR_ARG;
     const unsigned long long elt = dtype == GDN_DTYPE_F32 ? 4 : 2;
-    const unsigned long long d = (unsigned long long)head_dim_k;
-    unsigned long long nq_rows, kv_rows, mask_n, q_bytes, kv_bytes, mask_bytes, out_bytes;
+    const unsigned long long dk = (unsigned long long)head_dim_k;
+    const unsigned long long dv = (unsigned long long)head_dim_v;
+    unsigned long long nq_rows, kv_rows, mask_n, q_bytes, k_bytes, v_bytes, mask_bytes, out_bytes;
     if (!mul_ok((unsigned long long)n_seqs * (unsigned long long)n_heads, (unsigned long long)n_q,
                 &nq_rows) ||
         !mul_ok((unsigned long long)n_seqs * (unsigned long long)n_heads_kv,
@@ -625,10 +639,12 @@ int gdn_flash_attn(const void *q, const void *k, const void *v, const void *mask
         !mul_ok((unsigned long long)n_seqs * (unsigned long long)n_q, (unsigned long long)n_kv,
                 &mask_n))
         return GDN_ERR_ARG;
-    unsigned long long nq_elems, kv_elems;
-    if (!mul_ok(nq_rows, d, &nq_elems) || !mul_ok(kv_rows, d, &kv_elems) ||
-        !span_bytes(nq_elems, elt, &q_bytes) || !span_bytes(kv_elems, elt, &kv_bytes) ||
-        !span_bytes(mask_n, elt, &mask_bytes) || !span_bytes(nq_elems, 4, &out_bytes))
+    unsigned long long q_elems, out_elems, k_elems, v_elems;
+    if (!mul_ok(nq_rows, dk, &q_elems) || !mul_ok(nq_rows, dv, &out_elems) ||
+        !mul_ok(kv_rows, dk, &k_elems) || !mul_ok(kv_rows, dv, &v_elems) ||
+        !span_bytes(q_elems, elt, &q_bytes) || !span_bytes(k_elems, elt, &k_bytes) ||
+        !span_bytes(v_elems, elt, &v_bytes) || !span_bytes(mask_n, elt, &mask_bytes) ||
+        !span_bytes(out_elems, 4, &out_bytes))
         return GDN_ERR_ARG;
     if (nq_rows == 0) return GDN_OK;                  // no queries: nothing to do
     if (!q || !out || (kv_rows > 0 && (!k || !v))) return GDN_ERR_ARG;
@@ -636,14 +652,14 @@ int gdn_flash_attn(const void *q, const void *k, const void *v, const void *mask
         (mask && !aligned(mask, elt)))
         return GDN_ERR_ALIGN;
     const Range ro = range_of(out, out_bytes);
-    for (Range in : {range_of(q, q_bytes), range_of(k, kv_bytes), range_of(v, kv_bytes),
+    for (Range in : {range_of(q, q_bytes), range_of(k, k_bytes), range_of(v, v_bytes),
                      range_of(mask, mask ? mask_bytes : 0)})
         if (overlap(ro, in)) return GDN_ERR_ALIAS;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (n_kv == 0)   // empty cache: every output row is zero
         return cudaMemsetAsync(out, 0, out_bytes, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     const gdn::attn::AttnProblem p{q, k, v, mask, out, n_seqs, n_heads, n_heads_kv, n_q, n_kv,
-                                   head_dim_k, scale};
+                                   head_dim_k, head_dim_v, scale};
     cudaError_t e;
     if (dtype == GDN_DTYPE_BF16)
         e = gdn::attn::launch_dtype<__nv_bfloat16>(p, st);

@@ -1624,14 +1624,6 @@ bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
            CUDA_SUCCESS;
 }
 
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-        return 1;
-    return n;
-}
-
 // head_dim 256, and head_dim 128 with few pairs: the chunk transform for
 // every chunk into the workspace, then the state walk (D / 64 CTAs per head,
 // 64 value rows each) reading it.
@@ -1648,18 +1640,18 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
         !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, true))
         return cudaErrorInvalidValue;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(chunk_z_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(chunked_kernel<D>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    static PerDeviceOnce attrs;
+    const cudaError_t attr_err = attrs.run([] {
+        cudaError_t e = cudaFuncSetAttribute(chunk_z_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(chunked_kernel<D>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        return e;
     });
     if (attr_err != cudaSuccess) return attr_err;
     uint8_t *zws = static_cast<uint8_t *>(workspace);
-    const long long z_grid = std::min<long long>(n_tasks, 3LL * sm_count());
+    const long long z_grid = std::min<long long>(n_tasks, 3LL * current_sm_count());
     chunk_z_kernel<D><<<(unsigned)z_grid, NT, ZC::SMEM, stream>>>(
         mq, mk, p.g, p.beta, zws, p.T, p.H, p.Hk, n_chunks, (int)n_tasks, p.status);
     cudaError_t e = cudaGetLastError();
@@ -1678,11 +1670,10 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
         !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true) ||
         !make_map_out(&mo, p.out, p.B, p.T, p.H, D))
         return cudaErrorInvalidValue;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(d128::chunked_d128_kernel<D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, d128::SMEM);
+    static PerDeviceOnce attrs;
+    const cudaError_t attr_err = attrs.run([] {
+        return cudaFuncSetAttribute(d128::chunked_d128_kernel<D>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, d128::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
     d128::chunked_d128_kernel<D><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(

@@ -4,9 +4,54 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 namespace gdn {
+
+// Devices the library keeps per-device state for (status word, pool, kernel
+// attributes); a device index at or above this is refused.
+constexpr int kMaxDevices = 64;
+
+// Index of the current device, or -1 if it cannot be read or is out of range.
+inline int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+// Multiprocessors of the current device (1 if the query fails).
+inline int current_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 1;
+    return n;
+}
+
+// One-time set-up per device.  Function attributes such as the dynamic
+// shared-memory opt-in apply to the device that is current when they are set,
+// so each device gets its own run of `setup` (with that device current), and
+// later calls on the device return the recorded result.
+class PerDeviceOnce {
+  public:
+    template <class F>
+    cudaError_t run(F &&setup) {
+        const int dev = current_device();
+        if (dev < 0) return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lock(mu_);
+        if (!done_[dev]) {
+            err_[dev] = setup();
+            done_[dev] = true;
+        }
+        return err_[dev];
+    }
+
+  private:
+    std::mutex mu_;
+    bool done_[kMaxDevices] = {};
+    cudaError_t err_[kMaxDevices] = {};
+};
 
 // One validated call.  All pointers are device pointers; sizes are >= 1.
 struct Problem {

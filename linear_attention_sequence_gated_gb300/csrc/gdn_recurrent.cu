@@ -491,7 +491,8 @@ cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     // several times over (more bytes in flight per thread); one otherwise.
     constexpr int RB2 = 4 * 2 * (32 / L);
     const long long blocks2 = (long long)p.B * p.H * (D / RB2);
-    if (D % RB2 == 0 && blocks2 >= 4 * 152) return launch_one<D, L, 2, Tin>(p, stream);
+    if (D % RB2 == 0 && blocks2 >= 4LL * current_sm_count())
+        return launch_one<D, L, 2, Tin>(p, stream);
     return launch_one<D, L, 1, Tin>(p, stream);
 }
 
@@ -500,6 +501,7 @@ cudaError_t launch_dtype(const Problem &p, cudaStream_t stream) {
     switch (p.d) {
         case 32: return launch_one<32, 8, 1, Tin>(p, stream);
         case 64: return launch_d<64, 8, Tin>(p, stream);
+        case 96: return launch_d<96, 8, Tin>(p, stream);
         case 128: return launch_d<128, 8, Tin>(p, stream);
         case 256: return launch_d<256, 16, Tin>(p, stream);
         default: return cudaErrorInvalidValue;

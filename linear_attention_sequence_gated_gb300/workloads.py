@@ -118,7 +118,8 @@ def to_numpy_f32(inputs):
 
 @dataclasses.dataclass(frozen=True)
 class AttnWorkload:
-    """Decode attention: q (B, H, n_q, d); k, v (B, Hkv, n_kv, d); optional
+    """Decode attention: q (B, H, n_q, d); k (B, Hkv, n_kv, d); v (B, Hkv,
+    n_kv, dv), dv = d unless given; optional
     additive mask (B, 1, n_q, n_kv).  q, k, v ~ N(0, 1); the mask, when
     present, is 0 on visible keys and -inf on the last ``masked_tail`` keys
     of each query row shifted by the query index (a causal tail, as when the
@@ -135,6 +136,11 @@ class AttnWorkload:
     masked_tail: int = 0
     mask_std: float = 0.0
     seed: int = 0
+    dv_: int = 0          # head_dim of v when it differs from q / k's (0: same as d)
+
+    @property
+    def dv(self) -> int:
+        return self.dv_ or self.d
 
     @property
     def torch_dtype(self):
@@ -163,7 +169,7 @@ def make_attn_inputs(w: AttnWorkload, device="cpu", seed: int | None = None):
     f = dict(generator=gen, device=device, dtype=torch.float32)
     q = torch.randn((w.B, w.H, w.n_q, w.d), **f)
     k = torch.randn((w.B, w.Hkv, w.n_kv, w.d), **f)
-    v = torch.randn((w.B, w.Hkv, w.n_kv, w.d), **f)
+    v = torch.randn((w.B, w.Hkv, w.n_kv, w.dv), **f)
     mask = None
     if w.mask:
         mask = torch.randn((w.B, 1, w.n_q, w.n_kv), **f) * w.mask_std

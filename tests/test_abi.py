@@ -49,9 +49,10 @@ def test_library_is_built_for_sm_103a():
 
 def test_supports(L):
     assert gdn.supports(32) == 1
+    assert gdn.supports(96) == 1                            # recurrent only
     for d in (64, 128, 256):
         assert gdn.supports(d) == 3
-    for d in (0, -1, 16, 48, 96, 100, 192, 512):
+    for d in (0, -1, 16, 48, 100, 160, 192, 512):
         assert gdn.supports(d) == 0
 
 
@@ -70,6 +71,7 @@ def test_workspace_and_path_queries(L):
     assert gdn.select_path(1, 1, 32, 128) == "recurrent"
     assert gdn.select_path(1, 5, 32, 32) == "recurrent"
     assert gdn.select_path(1, 4096, 32, 32) == "recurrent"            # no chunked d = 32
+    assert gdn.select_path(1, 4096, 32, 96) == "recurrent"            # no chunked d = 96
     # measured switch points: (pairs, head_dim) -> first chunked length
     for pairs, d, t_switch in ((32, 64, 48), (256, 64, 48), (2048, 64, 64), (32, 128, 72),
                                (64, 128, 44), (96, 128, 24), (128, 128, 24), (2048, 128, 24),
@@ -112,7 +114,8 @@ def call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, g=BASE + 192 * MB,
 @pytest.mark.parametrize("kw,code", [
     (dict(B=-1), gdn.ERR_ARG), (dict(T=-1), gdn.ERR_ARG), (dict(H=-2), gdn.ERR_ARG),
     (dict(d=0), gdn.ERR_ARG), (dict(dtype=7), gdn.ERR_ARG), (dict(path=9), gdn.ERR_ARG),
-    (dict(d=48), gdn.ERR_HEADDIM), (dict(d=96), gdn.ERR_HEADDIM), (dict(d=512), gdn.ERR_HEADDIM),
+    (dict(d=48), gdn.ERR_HEADDIM), (dict(d=96, path=2), gdn.ERR_HEADDIM),
+    (dict(d=160), gdn.ERR_HEADDIM), (dict(d=512), gdn.ERR_HEADDIM),
     (dict(q=None), gdn.ERR_ARG), (dict(k=None), gdn.ERR_ARG), (dict(v=None), gdn.ERR_ARG),
     (dict(g=None), gdn.ERR_ARG), (dict(beta=None), gdn.ERR_ARG), (dict(out=None), gdn.ERR_ARG),
     (dict(s_out=None), gdn.ERR_ARG),
@@ -174,9 +177,13 @@ def test_flash_attn_supports(L):
             assert gdn.flash_attn_supports(n_q, d, d)
         assert not gdn.flash_attn_supports(20, d, d)      # the vector variant only
         assert not gdn.flash_attn_supports(0, d, d)
-    assert not gdn.flash_attn_supports(1, 128, 64)        # unequal head dims
+    for dk in (64, 128, 256):                             # key and value widths apart
+        for dv in (64, 128, 256):
+            assert gdn.flash_attn_supports(1, dk, dv)
     for d in (32, 48, 96, 512):
         assert not gdn.flash_attn_supports(1, d, d)
+        assert not gdn.flash_attn_supports(1, d, 128)
+        assert not gdn.flash_attn_supports(1, 128, d)
 
 
 def attn_call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, mask=BASE + 192 * MB,
@@ -190,7 +197,7 @@ def attn_call(L, q=BASE, k=BASE + 64 * MB, v=BASE + 128 * MB, mask=BASE + 192 * 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=-1), gdn.ERR_ARG), (dict(n_kv=-1), gdn.ERR_ARG), (dict(n_q=-1), gdn.ERR_ARG),
     (dict(dtype=3), gdn.ERR_ARG), (dict(dk=48, dv=48), gdn.ERR_HEADDIM),
-    (dict(dk=128, dv=256), gdn.ERR_HEADDIM), (dict(n_q=20), gdn.ERR_SHAPE),
+    (dict(dk=128, dv=96), gdn.ERR_HEADDIM), (dict(n_q=20), gdn.ERR_SHAPE),
     (dict(Hkv=3), gdn.ERR_ARG), (dict(Hkv=0), gdn.ERR_ARG), (dict(Hkv=32), gdn.ERR_ARG),
     (dict(scale=float("inf")), gdn.ERR_ARG), (dict(scale=float("nan")), gdn.ERR_ARG),
     (dict(q=None), gdn.ERR_ARG), (dict(out=None), gdn.ERR_ARG), (dict(k=None), gdn.ERR_ARG),

@@ -35,7 +35,7 @@ def run_and_check(w, scale=None, tol=TOL):
     inp = W.make_attn_inputs(w, "cuda")
     out = gdn.flash_attn(inp["q"], inp["k"], inp["v"], inp["mask"], scale)
     torch.cuda.synchronize()
-    s = 1.0 / np.sqrt(w.d) if scale is None else scale
+    s = 1.0 / np.sqrt(w.d) if scale is None else scale      # w.d: the q / k width
     # the oracle takes the kernel's scale as the float32 value it receives
     s = float(np.float32(s))
     ref = attention(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), np64(inp["mask"]), s)
@@ -49,6 +49,19 @@ def run_and_check(w, scale=None, tol=TOL):
 @pytest.mark.parametrize("wname", list(W.ATTN_BY_NAME))
 def test_benchmark_workloads_full_size(wname):
     run_and_check(W.ATTN_BY_NAME[wname])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("dk,dv", [(64, 128), (64, 256), (128, 64), (128, 256), (256, 64),
+                                   (256, 128)])
+@pytest.mark.parametrize("n_kv", [1, 33, 257, 1000])
+def test_unequal_key_and_value_widths(dtype, dk, dv, n_kv):
+    """head_dim_k != head_dim_v (the model card's capability query takes the
+    two widths apart): every pair of 64 / 128 / 256, grouped heads, a mask."""
+    w = W.AttnWorkload(f"kv_{dtype}_{dk}_{dv}_{n_kv}", 2, 8, 2, 3, n_kv, dk, dtype, mask=True,
+                       mask_std=1.0, seed=n_kv + dk + 3 * dv, dv_=dv)
+    got, _ = run_and_check(w)
+    assert got.shape == (2, 3, 8, dv)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])

@@ -103,12 +103,58 @@ def test_prefill_4k_full(path):
     check(inp, w.dtype, path, TOL_RECURRENT if path == "recurrent" else None)
 
 
-def sampled_pairs(w, n):
+N_SMS = 152
+
+
+def ctas_per_pair(w, path):
+    """CTAs one (sequence, head) pair takes on the chunked path: the state walk
+    of the two-kernel path (which needs a workspace) runs head_dim / 64
+    value-row blocks per pair, the one-kernel path one CTA per pair."""
+    if path == "auto":
+        path = gdn.select_path(w.B, w.T, w.H, w.d, w.dtype)
+    if path == "chunked" and gdn.workspace_bytes(w.B, w.T, w.H, w.d, "bf16", "chunked"):
+        return w.d // 64
+    return 1
+
+
+def sampled_pairs(w, n, per_cta=1):
+    """n random (sequence, head) pairs plus the first and the last, plus one
+    pair from every wave of 152 CTAs (pairs are laid out b * H + h in launch
+    order, `per_cta` CTAs each), so that a fault tied to the second or a
+    later CTA on an SM cannot hide between samples."""
     r = np.random.default_rng(1234)
     pairs = {(0, 0), (w.B - 1, w.H - 1)}
-    while len(pairs) < n:
+    n_pairs = w.B * w.H
+    per_wave = max(1, N_SMS // per_cta)
+    for first in range(0, n_pairs, per_wave):
+        i = int(r.integers(first, min(n_pairs, first + per_wave)))
+        pairs.add(divmod(i, w.H))
+    while len(pairs) < n + 2:
         pairs.add((int(r.integers(w.B)), int(r.integers(w.H))))
     return sorted(pairs)
+
+
+_SAMPLE_REF = {}
+
+
+def sampled_reference(w, inp, pairs):
+    """The oracle on the sampled pairs, as one batch of independent problems
+    (one OpenMP thread per pair); cached per workload and sample."""
+    key = (w.name, tuple(pairs))
+    if key not in _SAMPLE_REF:
+        n = W.to_numpy_f32(inp)
+        bs = [b for b, _ in pairs]
+        hs = [h for _, h in pairs]
+        Hk = n["q"].shape[2]
+        hks = [h % Hk for h in hs]
+        pick = lambda x, heads: np.ascontiguousarray(
+            np.stack([x[b, :, hh] for b, hh in zip(bs, heads)])[:, :, None])
+        st = None if n["state"] is None else np.ascontiguousarray(
+            np.stack([n["state"][b, h] for b, h in pairs])[:, None])
+        _SAMPLE_REF[key] = oracle.recurrent_c(pick(n["q"], hks), pick(n["k"], hks),
+                                              pick(n["v"], hs), pick(n["g"], hs),
+                                              pick(n["beta"], hs), st)
+    return _SAMPLE_REF[key]
 
 
 @pytest.mark.parametrize("wname", [W.PREFILL_16K.name, W.PREFILL_16K_D64.name,
@@ -117,32 +163,26 @@ def sampled_pairs(w, n):
 def test_long_prefill_full_size_sampled(wname, path):
     """Full-size launch (the configuration the benchmark times); the oracle
     recomputes every output and the final state of a sample of (sequence,
-    head) pairs, which are independent problems."""
+    head) pairs, which are independent problems: at least one pair from
+    every wave of CTAs."""
     w = W.BY_NAME[wname]
     if path == "chunked" and not gdn.supports(w.d) & 2:
         pytest.skip("chunked path not built")
     inp = W.make_inputs(w, "cuda")
     out, st = run_gpu(inp, path)
     tol = TOL_RECURRENT if path == "recurrent" else TOL[w.dtype]
-    outs, refs, sts, ref_sts = [], [], [], []
-    for b, h in sampled_pairs(w, 6):
-        sl = {key: (None if val is None else
-                    (val[b:b + 1, :, h:h + 1] if val.dim() >= 3 and key != "state"
-                     else val[b:b + 1, h:h + 1]))
-              for key, val in inp.items()}
-        ro, rs = run_oracle(sl)
-        outs.append(out[b, :, h].double().cpu().numpy().ravel())
-        refs.append(ro.ravel())
-        sts.append(st[b, h].double().cpu().numpy().ravel())
-        ref_sts.append(rs.ravel())
-    e_out = oracle.parity_error(np.concatenate(outs), np.concatenate(refs))
-    e_st = oracle.parity_error(np.concatenate(sts), np.concatenate(ref_sts))
-    assert e_out <= tol and e_st <= tol, (e_out, e_st)
+    pairs = sampled_pairs(w, 6, ctas_per_pair(w, path))
+    ref_out, ref_st = sampled_reference(w, inp, pairs)
+    got_out = np.stack([out[b, :, h].double().cpu().numpy() for b, h in pairs])
+    got_st = np.stack([st[b, h].double().cpu().numpy() for b, h in pairs])
+    e_out = oracle.parity_error(got_out.ravel(), ref_out.ravel())
+    e_st = oracle.parity_error(got_st.ravel(), ref_st.ravel())
+    assert e_out <= tol and e_st <= tol, (e_out, e_st, len(pairs))
 
 
 # ------------------------------------------------------ shapes and dtypes
 
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 256])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("T", [1, 2, 7, 63, 64, 65, 200])
 def test_head_dims_dtypes_lengths(d, dtype, T):
@@ -215,6 +255,130 @@ def test_extreme_gates_and_betas():
     beta[:, 40:45] = 1.0
     for path in paths_for(w.d, w.T, "f32"):
         check(inp, "f32", path, TOL["f32"])
+
+
+# The chunked kernels, one case per kernel: head_dim 64 and head_dim 128 with
+# at least 80 (sequence, head) pairs run the one-kernel path; head_dim 128
+# with fewer pairs and head_dim 256 run the chunk-transform pass plus the
+# state walk on value-row blocks.
+CHUNKED_KERNELS = [("d64", 2, 4, 64), ("d128_one_kernel", 2, 48, 128),
+                   ("d128_two_kernel", 2, 4, 128), ("d256", 2, 4, 256)]
+
+
+def plant_extremes(inp):
+    """Method edge cases over 200 tokens (chunks 0-63, 64-127, 128-191 and a
+    ragged 192-199): a whole chunk of g = 0 (no decay), g = -inf (a total
+    reset) at a chunk's first token, mid-chunk, on a chunk's last token and
+    on the very last token, g = -1e4, a run of beta = 1 and of beta = 0, a
+    whole chunk of beta = 0 (that chunk only decays the state), and k = 0
+    rows (the token writes nothing)."""
+    g, beta, k = inp["g"], inp["beta"], inp["k"]
+    g[:, 0:64] = 0.0
+    g[:, 64] = -float("inf")
+    g[:, 100] = -float("inf")
+    g[:, 127] = -float("inf")
+    g[:, 150] = -1e4
+    g[:, 199] = -float("inf")
+    beta[:, 20:30] = 1.0
+    beta[:, 30:36] = 0.0
+    beta[:, 128:192] = 0.0
+    k[:, 40:44] = 0
+    k[:, 160] = 0
+    return inp
+
+
+@pytest.mark.parametrize("name,B,H,d", CHUNKED_KERNELS)
+def test_extreme_gates_and_betas_chunked(name, B, H, d):
+    """The chunked tensor-core kernels held to the method's edge cases: the
+    clamp of g before the in-chunk running sum, decays that flush to zero,
+    no NaN from (-inf) - (-inf), beta = 0 / 1 rows and a beta = 0 chunk in
+    the UT transform, k = 0 rows."""
+    w = W.Workload(f"edge_{name}", B, 200, H, d, "bf16", 0.0, 0.05, seed=6)
+    inp = plant_extremes(W.make_inputs(w, "cuda"))
+    out, st = run_gpu(inp, "chunked")
+    assert torch.isfinite(out).all() and torch.isfinite(st).all()
+    ref_out, ref_st = run_oracle(inp)
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+    # the same inputs on the recurrent path, at its own bound
+    check(inp, "bf16", "recurrent", TOL_RECURRENT)
+
+
+@pytest.mark.parametrize("name,B,H,d", CHUNKED_KERNELS)
+def test_reset_on_last_token_leaves_only_that_token_chunked(name, B, H, d):
+    """g = -inf and beta = 1 on the last token with unit k: the final state is
+    exactly v k^T of that token, whatever came before (forgetting pin)."""
+    w = W.Workload(f"reset_{name}", B, 130, H, d, "bf16", 0.0, 0.05, seed=8)
+    inp = W.make_inputs(w, "cuda")
+    inp["g"][:, -1] = -float("inf")
+    inp["beta"][:, -1] = 1.0
+    out, st = run_gpu(inp, "chunked")
+    k = inp["k"][:, -1].float()
+    v = inp["v"][:, -1].float()
+    Hk = k.shape[1]
+    kk = k[:, torch.arange(H, device="cuda") % Hk]
+    expect = v[:, :, :, None] * kk[:, :, None, :]
+    err = ((st - expect).abs().max() / expect.pow(2).mean().sqrt()).item()
+    assert err <= TOL["bf16"], err
+
+
+@pytest.mark.parametrize("name,B,H,d", CHUNKED_KERNELS)
+def test_in_place_state_update_chunked(name, B, H, d):
+    """state_out == state_in on every chunked kernel: the value-row blocks of
+    the two-kernel walk each read their own rows before writing them."""
+    w = W.Workload(f"inplace_{name}", B, 150, H, d, "bf16", 0.0, 0.02, seed=16)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    st = inp["state"].clone()
+    out, st2 = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st,
+                           state_out=st, path="chunked")
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    assert st2.data_ptr() == st.data_ptr()
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+
+
+def _named_call(fn, inp, out, st_out):
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    B, T, H, d = inp["v"].shape
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return fn(p(inp["q"]), p(inp["k"]), p(inp["v"]), p(inp["g"]), p(inp["beta"]),
+              p(inp["state"]), p(out), p(st_out), B, T, H, d, stream)
+
+
+@pytest.mark.parametrize("T,with_state", [(1, True), (5, False), (200, True)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_named_entry_point_fp32(T, with_state, d):
+    """gdn_forward, the signature as named (fp32 q/k/v, AUTO path), called
+    through ctypes on device tensors, against the oracle."""
+    w = W.Workload("named_f32", 2, T, 4, d, "f32", 0.0, 0.02 if with_state else 0.0, seed=21)
+    inp = W.make_inputs(w, "cuda")
+    out = torch.full((2, T, 4, d), float("nan"), device="cuda")
+    st = torch.full((2, 4, d, d), float("nan"), device="cuda")
+    assert _named_call(gdn.lib().gdn_forward, inp, out, st) == gdn.OK
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    ref_out, ref_st = run_oracle(inp)
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["f32"] and e_st <= TOL["f32"], (e_out, e_st)
+
+
+@pytest.mark.parametrize("B,T,H,d", [(2, 1, 4, 128), (2, 7, 4, 64), (2, 300, 4, 128),
+                                     (2, 300, 48, 128), (1, 200, 3, 256), (2, 150, 4, 64)])
+def test_named_entry_point_bf16(B, T, H, d):
+    """gdn_forward_bf16 (AUTO path: recurrent at short runs, every chunked
+    kernel at long ones) through ctypes, against the oracle."""
+    w = W.Workload("named_bf16", B, T, H, d, "bf16", 0.0, 0.02, seed=22)
+    inp = W.make_inputs(w, "cuda")
+    out = torch.full((B, T, H, d), float("nan"), device="cuda")
+    st = torch.full((B, H, d, d), float("nan"), device="cuda")
+    assert _named_call(gdn.lib().gdn_forward_bf16, inp, out, st) == gdn.OK
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    ref_out, ref_st = run_oracle(inp)
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
 def test_null_state_means_zeros():
@@ -354,7 +518,7 @@ def test_short_run_and_key_head_workloads_full_size(wname):
 
 
 @pytest.mark.parametrize("T", [2, 3, 7, 8, 9, 15, 16, 17, 23, 33, 63])
-@pytest.mark.parametrize("d", [32, 64, 128, 256])
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 256])
 def test_multi_token_runs_recurrent(T, d):
     """Short runs (2..63 tokens): windows of staged tokens with ragged last
     windows, for every head_dim, against the oracle."""

@@ -8,8 +8,11 @@ pairs -- then use a fixed 64 MiB array inside the library instead of caller
 or stream-ordered memory.  These tests call it
 through the C ABI twice in a row, with different inputs (the array keeps the
 previous call's contents), and compare each result with the existing entry
-point's on the same inputs, within the bf16 parity bound used by the other
-tests.  The file is named so that pytest collects it last.
+point's on the same inputs.  Both run the same deterministic kernels on the
+same inputs, only with the scratch at another address, so the results must be
+identical bit for bit (a scratch-addressing fault that moved them by less than
+the parity bound would still be caught); the bf16 parity bound of the other
+tests is checked as well.  The file is named so that pytest collects it last.
 """
 import ctypes
 
@@ -64,6 +67,7 @@ def test_two_calls_in_a_row_match_the_existing_entry_point(L):
         assert gdn.device_status() == gdn.OK
         assert rel_err(out, ref_out) <= TOL
         assert rel_err(st, ref_st) <= TOL
+        assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
 
 
 def test_head_dim_128_with_and_without_scratch_and_auto(L):
@@ -81,6 +85,40 @@ def test_head_dim_128_with_and_without_scratch_and_auto(L):
         torch.cuda.synchronize()
         assert gdn.device_status() == gdn.OK
         assert rel_err(out, ref_out) <= TOL and rel_err(st, ref_st) <= TOL
+        assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
+
+
+SCRATCH = 64 << 20
+
+
+def test_a_call_that_needs_exactly_the_whole_scratch(L):
+    # 1 sequence x 4096 tokens x 32 heads at head_dim 128 takes the two-kernel
+    # path: 32 pairs x 64 chunks x 32 KiB = 64 MiB, the whole array
+    w = W.Workload("noalloc_full", 1, 4096, 32, 128, "bf16", 2.0, 0.02, seed=75)
+    assert L.gdn_workspace_bytes(w.B, w.T, w.H, w.d, gdn.DTYPE_BF16, gdn.PATHS["auto"]) == SCRATCH
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  inp["state"])
+    out = torch.full_like(ref_out, float("nan"))
+    st = torch.full_like(ref_st, float("nan"))
+    assert noalloc(L, inp, out, st, path=gdn.PATHS["auto"]) == gdn.OK
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
+
+
+def test_one_chunk_beyond_the_scratch_is_rejected_before_any_work(L):
+    # one more token opens a 65th chunk: 64 MiB + 32 x 32 KiB
+    w = W.Workload("noalloc_over", 1, 4097, 32, 128, "bf16", 2.0, 0.02, seed=76)
+    assert L.gdn_workspace_bytes(w.B, w.T, w.H, w.d, gdn.DTYPE_BF16, gdn.PATHS["auto"]) == \
+        SCRATCH + 32 * 32768
+    inp = W.make_inputs(w, "cuda")
+    out = torch.full((w.B, w.T, w.H, w.d), 7.0, device="cuda")
+    st = torch.full((w.B, w.H, w.d, w.d), 7.0, device="cuda")
+    torch.cuda.synchronize()
+    assert noalloc(L, inp, out, st, path=gdn.PATHS["auto"]) == gdn.ERR_SCRATCH
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all()) and bool((st == 7.0).all())     # nothing was written
 
 
 def test_rejects_calls_beyond_the_fixed_scratch(L):
