@@ -11,6 +11,9 @@ Contents
                      (``gdn_oracle.c``), OpenMP over (sequence, head) pairs.
 ``recurrent_np``     the same recurrence in numpy, float64, for tiny cases and
                      as an independent twin of the C code.
+``l2_normalize``     x / |x| per vector in float64 (zero stays zero): the
+                     op's optional fused q / k preprocessing, which both
+                     recurrences above apply when asked (``l2norm_qk``).
 ``chunked_np``       a float64 chunked (WY / UT-transform) evaluation of the
                      same recurrence, used only to check the chunk algebra
                      that the CUDA prefill path relies on against the
@@ -61,7 +64,7 @@ def _load():
         lib = ctypes.CDLL(build())
         f = lib.gdn_oracle_forward
         f.restype = ctypes.c_int
-        f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 6
+        f.argtypes = [ctypes.c_void_p] * 8 + [ctypes.c_int] * 7
         lib.gdn_oracle_max_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -75,11 +78,13 @@ def _f32(x):
     return np.ascontiguousarray(np.asarray(x, dtype=np.float32))
 
 
-def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0):
+def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0, l2norm_qk: bool = False):
     """float64 recurrence in C.  q, k: (B, T, Hk, d); v: (B, T, H, d); g, beta:
     (B, T, H); state: (B, H, d, d) [value][key] or None for zeros; value head
     h reads key head h % Hk (Hk == H: identity).  Inputs are taken as float32
-    (exact for bf16 data).  Returns (out (B,T,H,d), state_out (B,H,d,d)), both
+    (exact for bf16 data).  l2norm_qk: q and k are first divided by their
+    Euclidean norm per (sequence, token, key head), in float64 (a zero vector
+    stays zero).  Returns (out (B,T,H,d), state_out (B,H,d,d)), both
     float64."""
     q, k, v, g, beta = (_f32(x) for x in (q, k, v, g, beta))
     B, T, H, d = v.shape
@@ -93,17 +98,27 @@ def recurrent_c(q, k, v, g, beta, state=None, n_threads: int = 0):
     s_out = np.empty((B, H, d, d), dtype=np.float64)
     p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     rc = _load().gdn_oracle_forward(p(q), p(k), p(v), p(g), p(beta), p(st), p(out), p(s_out),
-                                    B, T, H, Hk, d, int(n_threads))
+                                    B, T, H, Hk, d, int(n_threads), int(bool(l2norm_qk)))
     if rc != 0:
         raise RuntimeError(f"gdn_oracle_forward failed ({rc})")
     return out, s_out
 
 
-def recurrent_np(q, k, v, g, beta, state=None):
+def l2_normalize(x):
+    """x / |x| over the last axis in float64; an all-zero vector stays zero."""
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return np.divide(x, n, out=np.zeros_like(x), where=n > 0)
+
+
+def recurrent_np(q, k, v, g, beta, state=None, l2norm_qk: bool = False):
     """The same float64 recurrence in numpy, token by token:
     decay, read r = S k, overwrite S += beta (v - r) k^T, emit S q / sqrt(d).
-    q, k may carry fewer heads (Hk) than v: value head h reads key head h % Hk."""
+    q, k may carry fewer heads (Hk) than v: value head h reads key head h % Hk.
+    l2norm_qk: q and k are first replaced by l2_normalize(q), l2_normalize(k)."""
     q, k, v, g, beta = (np.asarray(x, dtype=np.float64) for x in (q, k, v, g, beta))
+    if l2norm_qk:
+        q, k = l2_normalize(q), l2_normalize(k)
     B, T, H, d = v.shape
     Hk = q.shape[2]
     out = np.zeros((B, T, H, d))

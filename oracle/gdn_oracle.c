@@ -38,6 +38,13 @@
  *     head i % n_k_heads (the tiled convention).  q and k then carry n_k_heads
  *     heads; n_k_heads == n_heads is the identity mapping.
  *
+ * Option l2norm_qk (the op's fused preprocessing, off by default): q_t and
+ * k_t are first replaced by q_t / |q_t| and k_t / |k_t| (Euclidean norm over
+ * the head's d components, in double); a zero vector stays zero.  The model
+ * card's "Ops" section counts this normalisation among the eager ops that
+ * surround the recurrence in a Gated DeltaNet layer, and the synthetic
+ * workloads normalise q and k per head this way.
+ *
  * Inputs are float32 (bf16 data is upcast exactly by the caller); every
  * operation is done in double.  No blocking, no reordering beyond the
  * definition above, no fast-math.
@@ -56,12 +63,28 @@
  *   v/out:     token t, component i at [t * tok_stride + i]
  *   g/beta:    token t at [t * gate_stride]
  *   state:     S[i][j] at [i * d + j]                                      */
+/* x (d floats) as double into y, divided by its Euclidean norm when
+ * `normalise` is set (a zero vector stays zero). */
+static void load_vec(const float *x, double *y, int d, int normalise)
+{
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) {
+        y[j] = (double)x[j];
+        ss += y[j] * y[j];
+    }
+    if (normalise && ss > 0.0) {
+        const double n = sqrt(ss);
+        for (int j = 0; j < d; ++j)
+            y[j] /= n;
+    }
+}
+
 static void oracle_one_head(const float *q, const float *k, const float *v,
                             const float *g, const float *beta, long qk_stride,
                             long tok_stride, long gate_stride,
                             const float *state_in, double *out,
                             double *state_out, int T, int d, double *S,
-                            double *r)
+                            double *r, double *qv, double *kv, int l2norm_qk)
 {
     const double inv_sqrt_d = 1.0 / sqrt((double)d);
     for (int i = 0; i < d; ++i)
@@ -69,8 +92,10 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
             S[(size_t)i * d + j] = state_in ? (double)state_in[(size_t)i * d + j] : 0.0;
 
     for (int t = 0; t < T; ++t) {
-        const float *qt = q + (size_t)t * qk_stride;
-        const float *kt = k + (size_t)t * qk_stride;
+        load_vec(q + (size_t)t * qk_stride, qv, d, l2norm_qk);
+        load_vec(k + (size_t)t * qk_stride, kv, d, l2norm_qk);
+        const double *qt = qv;
+        const double *kt = kv;
         const float *vt = v + (size_t)t * tok_stride;
         const double alpha = exp((double)g[(size_t)t * gate_stride]);
         const double b = (double)beta[(size_t)t * gate_stride];
@@ -82,21 +107,21 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
         for (int i = 0; i < d; ++i) {
             double acc = 0.0;
             for (int j = 0; j < d; ++j)
-                acc += S[(size_t)i * d + j] * (double)kt[j];
+                acc += S[(size_t)i * d + j] * kt[j];
             r[i] = acc;
         }
         /* delta rule: S <- S + beta (v - r) k^T */
         for (int i = 0; i < d; ++i) {
             const double c = b * ((double)vt[i] - r[i]);
             for (int j = 0; j < d; ++j)
-                S[(size_t)i * d + j] += c * (double)kt[j];
+                S[(size_t)i * d + j] += c * kt[j];
         }
         /* o = S q / sqrt(d) */
         double *ot = out + (size_t)t * tok_stride;
         for (int i = 0; i < d; ++i) {
             double acc = 0.0;
             for (int j = 0; j < d; ++j)
-                acc += S[(size_t)i * d + j] * (double)qt[j];
+                acc += S[(size_t)i * d + j] * qt[j];
             ot[i] = acc * inv_sqrt_d;
         }
     }
@@ -109,12 +134,14 @@ static void oracle_one_head(const float *q, const float *k, const float *v,
  *   g, beta      : (B, T, H) contiguous
  *   state_in     : (B, H, d, d) contiguous, [value][key]; NULL means zeros
  *   state_out    : (B, H, d, d) contiguous, [value][key]
- * n_threads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad sizes or
- * an allocation failure (outputs are then unspecified).                    */
+ * n_threads <= 0 uses the OpenMP default.  l2norm_qk != 0 normalises q and k
+ * first (see the header).  Returns 0, or -1 on bad sizes or an allocation
+ * failure (outputs are then unspecified).                                  */
 int gdn_oracle_forward(const float *q, const float *k, const float *v,
                        const float *g, const float *beta,
                        const float *state_in, double *out, double *state_out,
-                       int B, int T, int H, int Hk, int d, int n_threads)
+                       int B, int T, int H, int Hk, int d, int n_threads,
+                       int l2norm_qk)
 {
     if (B < 0 || T < 0 || H < 0 || d <= 0 || Hk <= 0 || Hk > (H > 0 ? H : 1))
         return -1;
@@ -132,7 +159,7 @@ int gdn_oracle_forward(const float *q, const float *k, const float *v,
 #pragma omp parallel
     {
         double *S = (double *)malloc(sizeof(double) * (size_t)d * d);
-        double *r = (double *)malloc(sizeof(double) * (size_t)d);
+        double *r = (double *)malloc(sizeof(double) * (size_t)d * 3);
         if (!S || !r) {
 #pragma omp atomic write
             failed = 1;
@@ -149,7 +176,8 @@ int gdn_oracle_forward(const float *q, const float *k, const float *v,
             oracle_one_head(q + qk_off, k + qk_off, v + in_off, g + gb_off,
                             beta + gb_off, qk_stride, tok_stride, gate_stride,
                             state_in ? state_in + st_off : NULL,
-                            out + in_off, state_out + st_off, T, d, S, r);
+                            out + in_off, state_out + st_off, T, d, S, r, r + d,
+                            r + 2 * (size_t)d, l2norm_qk);
         }
         free(S);
         free(r);

@@ -406,3 +406,137 @@ def test_planted_mistake_is_caught(kind):
     with np.errstate(all="ignore"):
         failed = [p.__name__ for p in PINS if not p(impl)]
     assert failed, f"mutant {kind} passed every pin"
+
+
+# --------------------------------------------------------------------------
+# the op's optional fused preprocessing: q and k divided by their Euclidean
+# norm per (sequence, token, key head) before the recurrence (a zero vector
+# stays zero).  Pinned by facts of the normalisation itself, against the
+# plain recurrence that the pins above hold: exactly-unit inputs pass
+# through unchanged, a power-of-two rescaling of any q or k changes nothing,
+# parallel q and k give the closed-form single step, and zero vectors write
+# nothing and read nothing.
+# --------------------------------------------------------------------------
+
+def half_unit(shape, seed, zero_every=0):
+    """Vectors with four entries of +-1/2 (unit norm exactly in binary
+    floating point); with zero_every > 0 every such token is all zeros."""
+    r = np.random.default_rng(seed)
+    x = np.zeros(shape)
+    for idx in np.ndindex(shape[:-1]):
+        if zero_every and idx[1] % zero_every == zero_every - 1:
+            continue
+        pos = r.choice(shape[-1], 4, replace=False)
+        x[idx + (pos,)] = r.choice([-0.5, 0.5], 4)
+    return x
+
+
+def pin_norm_unit_inputs_unchanged(impl):
+    """Already-unit q and k (and zero vectors) are left as they are: the
+    normalised op equals the plain recurrence bit for bit."""
+    q, k, v, g, beta, S0 = rand_problem(40, T=9, d=8)
+    q, k = half_unit(q.shape, 41, zero_every=4), half_unit(k.shape, 42, zero_every=3)
+    o1, S1 = impl(q, k, v, g, beta, S0)
+    o2, S2 = oracle.recurrent_np(q, k, v, g, beta, S0)
+    return rel(o1, o2) < 1e-14 and rel(S1, S2) < 1e-14 and np.isfinite(o1).all()
+
+
+def pin_norm_scale_invariance(impl):
+    """q and k rescaled by powers of two, a different one per token and head
+    (exact in float32), give the same result as the unscaled inputs."""
+    q, k, v, g, beta, S0 = rand_problem(43, T=9, d=8, unit=False)
+    r = np.random.default_rng(44)
+    cq = 2.0 ** r.integers(-6, 7, size=q.shape[:3] + (1,))
+    ck = 2.0 ** r.integers(-6, 7, size=k.shape[:3] + (1,))
+    o1, S1 = impl(q, k, v, g, beta, S0)
+    o2, S2 = impl(q * cq, k * ck, v, g, beta, S0)
+    return rel(o1, o2) < 1e-14 and rel(S1, S2) < 1e-14
+
+
+def pin_norm_parallel_single_step(impl):
+    """From a zero state, one token with q = a u and k = c u (the same
+    direction u, any positive a, c): S = beta v u^T / |u| and o = beta v /
+    sqrt(d) exactly, since the unit key and query meet at 1."""
+    _, _, v, g, beta, _ = rand_problem(45, T=1, d=8)
+    r = np.random.default_rng(46)
+    u = r.standard_normal(v.shape).astype(np.float32).astype(np.float64)
+    a = 2.0 ** r.integers(-3, 4, size=v.shape[:3] + (1,))
+    c = 2.0 ** r.integers(-3, 4, size=v.shape[:3] + (1,))
+    out, S = impl(u * a, u * c, v, g, beta, None)
+    d = v.shape[-1]
+    want_o = beta[..., None] * v / math.sqrt(d)
+    un = u / np.linalg.norm(u, axis=-1, keepdims=True)
+    want_S = beta[:, 0, :, None, None] * v[:, 0, :, :, None] * un[:, 0, :, None, :]
+    return rel(out, want_o) < 1e-13 and rel(S, want_S) < 1e-13
+
+
+NORM_PINS = [pin_norm_unit_inputs_unchanged, pin_norm_scale_invariance,
+             pin_norm_parallel_single_step]
+
+
+def c_norm(q, k, v, g, beta, S0):
+    return oracle.recurrent_c(q, k, v, g, beta, S0, l2norm_qk=True)
+
+
+def np_norm(q, k, v, g, beta, S0):
+    return oracle.recurrent_np(q, k, v, g, beta, S0, l2norm_qk=True)
+
+
+NORM_IMPLS = {"c": c_norm, "numpy": np_norm}
+
+
+@pytest.mark.parametrize("impl", list(NORM_IMPLS))
+@pytest.mark.parametrize("pin", NORM_PINS, ids=lambda p: p.__name__)
+def test_oracle_norm_pin(impl, pin):
+    assert pin(NORM_IMPLS[impl])
+
+
+def test_norm_c_matches_numpy_twin_key_heads():
+    q, k, v, g, beta, S0 = _key_head_problem(47, 6, 3, 9)
+    q, k = q * 4.0, k * 0.25                     # exact in float32
+    o1, S1 = oracle.recurrent_c(q, k, v, g, beta, S0, l2norm_qk=True)
+    o2, S2 = oracle.recurrent_np(q, k, v, g, beta, S0, l2norm_qk=True)
+    assert rel(o1, o2) < 1e-13 and rel(S1, S2) < 1e-13
+
+
+def _norm_mutant(kind):
+    def nrm(x, axis=-1, power=0.5):
+        n = np.sum(x * x, axis=axis, keepdims=True) ** power
+        if kind == "zero_to_nan":
+            return x / n
+        return np.divide(x, n, out=np.zeros_like(x), where=n > 0)
+
+    def impl(q, k, v, g, beta, S0):
+        q, k = np.asarray(q, dtype=np.float64), np.asarray(k, dtype=np.float64)
+        if kind in ("none", "zero_to_nan"):
+            q, k = nrm(q), nrm(k)
+        elif kind == "q_only":
+            q = nrm(q)
+        elif kind == "k_only":
+            k = nrm(k)
+        elif kind == "squared_norm":
+            q, k = nrm(q, power=1.0), nrm(k, power=1.0)
+        elif kind == "over_heads":
+            q, k = nrm(q, axis=2), nrm(k, axis=2)
+        elif kind == "k_norm_for_both":
+            n = np.sqrt(np.sum(k * k, axis=-1, keepdims=True))
+            q, k = q / n, k / n
+        return oracle.recurrent_np(q, k, v, g, beta, S0)
+    return impl
+
+
+NORM_MUTANTS = ["skip", "q_only", "k_only", "squared_norm", "over_heads", "zero_to_nan",
+                "k_norm_for_both"]
+
+
+def test_unmutated_norm_copy_passes_every_norm_pin():
+    impl = _norm_mutant("none")
+    assert all(p(impl) for p in NORM_PINS)
+
+
+@pytest.mark.parametrize("kind", NORM_MUTANTS)
+def test_planted_norm_mistake_is_caught(kind):
+    impl = _norm_mutant(kind)
+    with np.errstate(all="ignore"):
+        failed = [p.__name__ for p in NORM_PINS if not p(impl)]
+    assert failed, f"mutant {kind} passed every normalisation pin"
