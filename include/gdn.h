@@ -86,6 +86,23 @@ enum gdn_dtype { GDN_DTYPE_F32 = 0, GDN_DTYPE_BF16 = 1, GDN_DTYPE_F16 = 2 };
 enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 };
 
 /*
+ * Options, OR-ed into the `path` argument of gdn_forward_ex,
+ * gdn_forward_noalloc and gdn_workspace_bytes (bits above the low byte;
+ * unknown bits are rejected with GDN_ERR_ARG).
+ *
+ * GDN_OPT_L2NORM_QK: q and k are L2-normalised inside the op, per (sequence,
+ *   token, key head) over head_dim: x -> x / |x|, in float32, a zero vector
+ *   staying zero (a vector whose squared norm underflows float32 counts as
+ *   zero).  The call then computes the recurrence of the normalised q and k.
+ *   This is one of the eager operations that the model card ("Ops") counts
+ *   around the recurrence of a Gated DeltaNet layer; fused here it saves a
+ *   read and a write of q and k.  Both paths and every head_dim serve it; on
+ *   the chunked path the norms are applied as per-token scalars in float32,
+ *   so raw bf16 q and k still enter the tensor-core products exactly.
+ */
+#define GDN_OPT_L2NORM_QK 0x100
+
+/*
  * gdn_forward -- the op with float32 q, k, v.
  * q, k, v: (n_seqs, n_tokens, n_heads, head_dim) float32.  Other arguments as
  * described above.  Uses the AUTO path; if that path needs a workspace it is
@@ -115,7 +132,7 @@ int gdn_forward_bf16(const void *q, const void *k, const void *v,
  *   contract notes under the "Ops" shape table give for upstream; with
  *   n_k_heads == n_heads it is the identity.  n_k_heads must divide n_heads
  *   (else GDN_ERR_ARG).  v, g, beta, out and the state keep n_heads heads.
- * dtype: GDN_DTYPE_*; path: GDN_PATH_*.
+ * dtype: GDN_DTYPE_*; path: GDN_PATH_*, optionally OR-ed with GDN_OPT_* flags.
  * workspace: caller-owned device buffer of at least
  *   gdn_workspace_bytes(n_seqs, n_tokens, n_heads, head_dim, dtype, path)
  *   bytes, 256-byte aligned; or NULL, in which case the call allocates and

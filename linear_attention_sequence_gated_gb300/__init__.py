@@ -30,6 +30,7 @@ ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE
     ERR_DTYPE, ERR_SHAPE, ERR_SCRATCH = -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -11
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
+OPT_L2NORM_QK = 0x100
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
@@ -126,13 +127,15 @@ def _ptr(t):
 
 
 def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str = "auto",
-            workspace=None, stream=None):
+            workspace=None, stream=None, l2norm_qk: bool = False):
     """Run the gated delta rule over every token of every sequence.
 
     Returns (out, final_state).  ``state_out`` may be ``state`` itself for
     an in-place update.  ``workspace`` is an optional uint8 CUDA tensor of at
     least ``workspace_bytes(...)`` bytes; without it the library allocates
-    stream-ordered scratch when the chosen path needs any."""
+    stream-ordered scratch when the chosen path needs any.  ``l2norm_qk``
+    divides q and k by their norm per (sequence, token, head) inside the op
+    (the library's GDN_OPT_L2NORM_QK)."""
     import torch
     L = lib()
     if q.dtype == torch.bfloat16:
@@ -177,7 +180,8 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
         ws_ptr, ws_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     with torch.cuda.device(q.device):
         rc = L.gdn_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                              _ptr(out), _ptr(state_out), B, T, H, Hk, d, dt, PATHS[path],
+                              _ptr(out), _ptr(state_out), B, T, H, Hk, d, dt,
+                              PATHS[path] | (OPT_L2NORM_QK if l2norm_qk else 0),
                               ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != OK:
         raise GdnError(rc, "gdn_forward_ex")

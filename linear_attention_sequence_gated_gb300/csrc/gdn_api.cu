@@ -156,9 +156,15 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     return GDN_OK;
 }
 
+constexpr int kPathMask = 0xff;
+constexpr int kKnownOptions = GDN_OPT_L2NORM_QK;
+
 int run(const void *q, const void *k, const void *v, const float *g, const float *beta,
         const float *state_in, float *out, float *state_out, int B, int T, int H, int Hk, int d,
-        int dtype, int path, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+        int dtype, int path_opts, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (path_opts < 0 || (path_opts & ~kPathMask & ~kKnownOptions)) return GDN_ERR_ARG;
+    int path = path_opts & kPathMask;
+    const bool l2norm = (path_opts & GDN_OPT_L2NORM_QK) != 0;
     Sizes sz{};
     int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype, path,
                       &sz);
@@ -188,7 +194,7 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
     if (!status) return GDN_ERR_CUDA;
 
     gdn::Problem p{q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype,
-                   (float)(1.0 / std::sqrt((double)d)), status};
+                   (float)(1.0 / std::sqrt((double)d)), status, l2norm};
 
     if (path == GDN_PATH_RECURRENT) {
         return gdn::launch_recurrent(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
@@ -239,8 +245,10 @@ int gdn_forward_ex(const void *q, const void *k, const void *v, const float *g,
 }
 
 size_t gdn_workspace_bytes(int n_seqs, int n_tokens, int n_heads, int head_dim, int dtype,
-                           int path) {
+                           int path_opts) {
     if (n_seqs < 0 || n_tokens < 0 || n_heads < 0 || head_dim <= 0) return 0;
+    if (path_opts < 0 || (path_opts & ~kPathMask & ~kKnownOptions)) return 0;
+    int path = path_opts & kPathMask;
     if (dtype != GDN_DTYPE_F32 && dtype != GDN_DTYPE_BF16) return 0;
     if (n_tokens == 0 || (long long)n_seqs * n_heads == 0) return 0;
     if (path == GDN_PATH_AUTO)

@@ -85,7 +85,8 @@ struct Cfg {
     static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
     static constexpr int OFF_RU = OFF_S + 2 * D * 128;     // R (then U~) hi, lo: 64 rows x 128 B
     static constexpr int OFF_MISC = OFF_RU + 2 * 8192;     // 2 gate sets: G, beta, gamma, end-decay
-    static constexpr int SMEM = OFF_MISC + 2 * 4 * 64 * 4 + 1024;  // + alignment slack
+    static constexpr int OFF_NRM = OFF_MISC + 2 * 4 * 64 * 4;  // 1/|k|, 1/|q| of the chunk
+    static constexpr int SMEM = OFF_NRM + 2 * 64 * 4 + 1024;   // + alignment slack
     // TMEM columns
     static constexpr int COL_X = 0;
     static constexpr int COL_Y = BV;
@@ -115,8 +116,8 @@ struct ZCfg {
     static constexpr int OFF_Z = OFF_PLO + 8192;           // Z hi | Z lo (W lives here during the solve)
     static constexpr int REGION = (D / 64) * 16384 > OFF_Z + Z_BYTES ? (D / 64) * 16384
                                                                      : OFF_Z + Z_BYTES;
-    static constexpr int OFF_MISC = REGION;                // G, beta
-    static constexpr int SMEM = OFF_MISC + 2 * 64 * 4 + 1024;
+    static constexpr int OFF_MISC = REGION;                // G, beta, 1/|k|, 1/|q|
+    static constexpr int SMEM = OFF_MISC + 4 * 64 * 4 + 1024;
     static_assert(SZ_F <= OFF_PHI, "A / T below the P tiles");
     static_assert(OFF_PHI % 1024 == 0 && OFF_Z % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
     static_assert(16 * 96 * 4 <= Z_BYTES, "solve scratch inside the Z tile");
@@ -135,6 +136,36 @@ __device__ __forceinline__ float fast_exp(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
     return y;
+}
+
+// 1 / |x| from a squared norm, 0 for a zero vector (q / k normalisation).
+__device__ __forceinline__ float inv_norm(float sq) { return sq > 0.f ? rsqrtf(sq) : 0.f; }
+
+// Squared norms of K row r and Q row r of a stacked [K;Q] stage: NSLAB slabs
+// of 64 keys, 16384 bytes apart, each holding 64 K rows then 64 Q rows of
+// 128 bytes (128-byte swizzled; a sum of squares does not depend on the order
+// in which a row's 16-byte pieces are visited).
+template <int NSLAB>
+__device__ __forceinline__ void qk_row_sumsq(const uint8_t *qk, int r, float &kk, float &qq) {
+    kk = 0.f;
+    qq = 0.f;
+#pragma unroll
+    for (int sl = 0; sl < NSLAB; ++sl) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(qk + sl * 16384 + r * 128 + c * 16);
+            const uint4 b =
+                *reinterpret_cast<const uint4 *>(qk + sl * 16384 + 8192 + r * 128 + c * 16);
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float k0 = __uint_as_float(wa[e] << 16), k1 = __uint_as_float(wa[e] & 0xffff0000u);
+                const float q0 = __uint_as_float(wb[e] << 16), q1 = __uint_as_float(wb[e] & 0xffff0000u);
+                kk = fmaf(k0, k0, fmaf(k1, k1, kk));
+                qq = fmaf(q0, q0, fmaf(q1, q1, qq));
+            }
+        }
+    }
 }
 
 // Store 16 consecutive fp32 values as bf16 hi / lo into two 128-B-swizzled
@@ -362,7 +393,7 @@ __device__ __forceinline__ void ut_transform16(float *sAT, float *sW, int t, int
 //   3. A and P, T = (I + A)^-1 by 32 x 32 blocks, MMA [P hi; P lo] T, and
 //      Z = [T; P T] as bf16 hi + lo in the swizzled tile layout;
 //   4. one bulk copy writes the 32 KB tile to the workspace.
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(NT, 3)
 chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const float *__restrict__ g, const float *__restrict__ beta,
@@ -376,6 +407,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     __shared__ Bars bars;
     float *sG = reinterpret_cast<float *>(sm + ZC::OFF_MISC);
     float *sBeta = sG + 64;
+    float *sNk = sG + 128, *sNq = sG + 192;          // with q / k normalisation
     uint8_t *sQK = sm + ZC::OFF_QK;
     float *sA = reinterpret_cast<float *>(sm + ZC::OFF_A);
     uint8_t *sPhi = sm + ZC::OFF_PHI, *sPlo = sm + ZC::OFF_PLO;
@@ -452,6 +484,14 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (tid >= 32 && tid < 64) sG[tid] += sG[31];
         if (!ptx::mbar_wait(&bars.tma, phase, abort_flag)) fail();
         else if (tid == 0) tma_pending = false;
+        if constexpr (NORM) {
+            if (tid < 64 && !*abort_flag) {
+                float kk, qq;
+                qk_row_sumsq<D / 64>(sQK, tid, kk, qq);
+                sNk[tid] = inv_norm(kk);
+                sNq[tid] = inv_norm(qq);
+            }
+        }
         __syncthreads();
         if (*abort_flag) break;
 
@@ -480,19 +520,23 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::tmem_ld_wait();
             const int r = row & 63;
             const float Gr = sG[r];
+            // with q / k normalisation A[r,i] and P[r,i] carry nk_i and nk_r / nq_r
             if (row < 64) {
-                const float br = sBeta[r];
+                const float br = NORM ? sBeta[r] * sNk[r] : sBeta[r];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int i = wg * 32 + j;
-                    sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                    const float kn = NORM ? kq[j] * sNk[i] : kq[j];
+                    sA[r * FST + i] = (i < r) ? br * fast_exp(Gr - sG[i]) * kn : 0.f;
                 }
             } else {
+                const float pr = NORM ? sNq[r] : 1.f;
                 float pv[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int i = wg * 32 + j;
-                    pv[j] = (i <= r) ? fast_exp(Gr - sG[i]) * kq[j] : 0.f;
+                    const float kn = NORM ? kq[j] * sNk[i] : kq[j];
+                    pv[j] = (i <= r) ? pr * fast_exp(Gr - sG[i]) * kn : 0.f;
                 }
                 store_split16(sPhi, sPlo, r, wg * 32, *reinterpret_cast<float(*)[16]>(pv));
                 store_split16(sPhi, sPlo, r, wg * 32 + 16, *reinterpret_cast<float(*)[16]>(pv + 16));
@@ -563,7 +607,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0) ptx::tmem_dealloc(tmem, 64);
 }
 
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(NT, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
@@ -580,6 +624,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                               ~uintptr_t(1023));
     __shared__ Bars bars;
     float *gsets = reinterpret_cast<float *>(sm + CF::OFF_MISC);   // set i: gsets + 256 i
+    float *sNk = reinterpret_cast<float *>(sm + CF::OFF_NRM), *sNq = sNk + 64;
     uint8_t *sQK = sm + CF::OFF_QK;
     uint8_t *sV = sm + CF::OFF_V;
     uint8_t *sZhi = sm + CF::OFF_Z, *sZlo = sm + CF::OFF_Z + 16384;
@@ -764,6 +809,15 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             ptx::mma_commit(&bars.mma);
         }
+        if constexpr (NORM) {                         // 1/|k|, 1/|q| of the chunk's tokens
+            if (tid >= 128 && tid < 192) {
+                float kk, qq;
+                qk_row_sumsq<D / 64>(sQK, tid - 128, kk, qq);
+                sNk[tid - 128] = inv_norm(kk);
+                sNq[tid - 128] = inv_norm(qq);
+            }
+            __syncthreads();
+        }
         wait_mma();
 
         // ---------------- 5. R = beta V - beta gamma K S^T  (lanes 0-63)
@@ -777,7 +831,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::tmem_ld_wait();
             if (row < 64) {
                 const int r = row;
-                const float br = sBeta[r], bg = br * sGam[r];
+                const float br = sBeta[r], bg = br * (NORM ? sGam[r] * sNk[r] : sGam[r]);
 #pragma unroll
                 for (int j = 0; j < HALF; j += 16) {
                     float rr[16];
@@ -848,7 +902,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (row >= 64) {
                 const int r = row - 64;
                 if (r < n) {
-                    const float gr = sGam[r];
+                    const float gr = NORM ? sGam[r] * sNq[r] : sGam[r];
                     float *orow = out + ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D + v0 +
                                   wg * HALF;
 #pragma unroll
@@ -863,7 +917,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             } else {
                 const int r = row;
-                const float er = sEnd[r];
+                const float er = NORM ? sEnd[r] * sNk[r] : sEnd[r];
 #pragma unroll
                 for (int j = 0; j < HALF; j += 16) {
                     float u[16];
@@ -999,8 +1053,9 @@ constexpr int OFF_PP = 147456;          // P hi (rows 0-63) | P lo (rows 64-127)
 constexpr int OFF_AT = 163840;          // A, then T in place: fp32 64 x FST
 constexpr int OFF_W = OFF_AT + 64 * FST * 4;   // 16 x 96 or 32 x 40 fp32
 constexpr int OFF_RT = 187392;          // R^T (then U~^T) hi | lo: 128 rows x 128 B each
-constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets x {G, beta, gamma, end-decay}
-constexpr int SMEM = OFF_G + 4 * 1024 + 1024;
+constexpr int OFF_G = OFF_RT + 32768;   // 4 gate sets of GS floats (layout at scan_gates)
+constexpr int GS = 512;                 // floats per gate set
+constexpr int SMEM = OFF_G + 4 * GS * 4 + 1024;
 static_assert(OFF_W + 16 * 96 * 4 <= OFF_RT && 16 * 96 >= 32 * 40, "scratch overlaps R^T");
 static_assert(OFF_PP + 24576 <= OFF_RT, "P lo rows 64-127 are read from the scratch");
 static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
@@ -1055,11 +1110,18 @@ __device__ __forceinline__ void load_gates(GateRegs &r, const float *g, const fl
     r.bown = (t < n) ? beta[base + (size_t)t * H] : 0.f;
 }
 
-// G = inclusive cumsum of max(g, -30), kept in log2 units (G2 = G log2 e),
-// gamma = exp(G) = 2^G2, end = exp(G_63 - G) into a gate set
-// {G2, beta, gamma, end} (4 x 64 floats).  Threads 0-63 of a stream (t), no
-// barrier inside.
-__device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) {
+// Gate set of one chunk, 8 x 64 floats indexed by token:
+//   [0]   G2    = G log2 e, G the inclusive cumsum of max(g, -30)
+//   [64]  beta
+//   [128] gamma = exp(G)
+//   [192] end   = exp(G_63 - G) nk       (scales U for the state update)
+//   [256] gk    = gamma nk               (the K S^T term of R)
+//   [320] gq    = gamma nq               (the Q S^T term of O)
+//   [384] nk, [448] nq: 1 / |k|, 1 / |q| with q / k normalisation, else 1.
+// scan_gates writes [0, 192) and returns the token's end decay; set_norms
+// writes the rest once the chunk's [K;Q] tiles have landed.  Threads 0-63 of
+// a stream (t), no barrier inside.
+__device__ __forceinline__ float scan_gates(const GateRegs &r, float *gs, int t) {
     const int l = t & 31;
     float sa = fmaxf(r.ga, -30.f), sb = fmaxf(r.gb, -30.f);
 #pragma unroll
@@ -1074,7 +1136,24 @@ __device__ __forceinline__ void scan_gates(const GateRegs &r, float *gs, int t) 
     gs[t] = G * LOG2E;
     gs[64 + t] = r.bown;
     gs[128 + t] = ex2(G * LOG2E);
-    gs[192 + t] = ex2((tot - G) * LOG2E);
+    return ex2((tot - G) * LOG2E);
+}
+
+template <int NSLAB, bool NORM>
+__device__ __forceinline__ void set_norms(float *gs, const uint8_t *qk, int t, float end) {
+    float nk = 1.f, nq = 1.f;
+    if constexpr (NORM) {
+        float kk, qq;
+        qk_row_sumsq<NSLAB>(qk, t, kk, qq);
+        nk = inv_norm(kk);
+        nq = inv_norm(qq);
+    }
+    const float gam = gs[128 + t];
+    gs[192 + t] = end * nk;
+    gs[256 + t] = gam * nk;
+    gs[320 + t] = gam * nq;
+    gs[384 + t] = nk;
+    gs[448 + t] = nq;
 }
 
 // 32 consecutive keys of one state row: hi / lo pairs -> 16 + 16 packed TMEM
@@ -1094,7 +1173,7 @@ __device__ __forceinline__ void put_state32(uint32_t tmem_lane, int key0, float 
     ptx::tmem_st16(tmem_lane + C_SACC + key0 + 16, lo);
 }
 
-template <int D>
+template <int D, bool NORM>
 __global__ void __launch_bounds__(NTH, 1)
 chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -1203,15 +1282,17 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int c = 0; c < n_chunks; ++c) {
             const int st = c & 1;
             const uint32_t aQK = ptx::smem_u32(sm + OFF_QK + st * 32768);
-            float *gs = gsets + (c & 3) * 256;
-            const float *sG = gs, *sBeta = gs + 64;
+            float *gs = gsets + (c & 3) * GS;
+            const float *sG = gs, *sBeta = gs + 64, *sNk = gs + 384, *sNq = gs + 448;
             uint8_t *sZhi = sm + OFF_Z + st * 32768, *sZlo = sZhi + 16384;
 
+            float end = 0.f;
             if (t < 64) {
-                scan_gates(gr, gs, t);
+                end = scan_gates(gr, gs, t);
                 if (c + 1 < n_chunks) load_gates(gr, g, beta, b, h, T, H, c + 1, t);
             }
             wait(&sh.qk_full[st], (uint32_t)((c >> 1) & 1));
+            if (t < 64) set_norms<NSLAB, NORM>(gs, sm + OFF_QK + st * 32768, t, end);
             ptx::named_sync(BAR_Z, NS);
             const bool ok = !*abort_flag;
             if (t == 0) {
@@ -1233,11 +1314,13 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             mma_phase ^= 1;
             ptx::tc_fence_after();
 
-            // A (rows 0-63) as fp32; P (rows 64-127) as hi / lo rows
+            // A (rows 0-63) as fp32; P (rows 64-127) as hi / lo rows; with q / k
+            // normalisation A[r,i] and P[r,i] carry nk_r nk_i and nq_r nk_i
             {
                 const int r = row & 63;
                 const float Gr = sG[r];
-                const float br = sBeta[r];
+                const float br = NORM ? sBeta[r] * sNk[r] : sBeta[r];
+                const float pr = NORM ? sNq[r] : 1.f;
 #pragma unroll 1
                 for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
                     float kq[16];
@@ -1249,6 +1332,15 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     for (int q = 0; q < 4; ++q) {
                         const float4 v4 = g4[q];
                         gi[4 * q] = v4.x; gi[4 * q + 1] = v4.y; gi[4 * q + 2] = v4.z; gi[4 * q + 3] = v4.w;
+                    }
+                    if constexpr (NORM) {             // column factor nk_i into the K K^T / Q K^T entries
+                        const float4 *n4 = reinterpret_cast<const float4 *>(sNk + jc);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 v4 = n4[q];
+                            kq[4 * q] *= v4.x; kq[4 * q + 1] *= v4.y;
+                            kq[4 * q + 2] *= v4.z; kq[4 * q + 3] *= v4.w;
+                        }
                     }
                     if (row < 64) {
                         float a[16];
@@ -1266,7 +1358,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int i = jc + j;
-                            p[j] = (i <= r) ? ex2(Gr - gi[j]) * kq[j] : 0.f;
+                            p[j] = (i <= r) ? pr * ex2(Gr - gi[j]) * kq[j] : 0.f;
                         }
                         ptx::store_split8(sPhi, sPlo, r, jc, p);
                         ptx::store_split8(sPhi, sPlo, r, jc + 8, p + 8);
@@ -1392,8 +1484,10 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             const int t0 = c * C;
             const int n = min(C, T - t0);
             const bool last = (c + 1 == n_chunks);
-            const float *gs = gsets + (c & 3) * 256;
-            const float *sBeta = gs + 64, *sGam = gs + 128, *sEnd = gs + 192;
+            const float *gs = gsets + (c & 3) * GS;
+            // gamma nk for R, gamma nq for O, end nk for U~ (nk = nq = 1 unless
+            // q and k are normalised)
+            const float *sBeta = gs + 64, *sGamK = gs + 256, *sGamQ = gs + 320, *sEnd = gs + 192;
             const uint32_t aQK = ptx::smem_u32(sm + OFF_QK + st * 32768);
             uint8_t *sZhi = sm + OFF_Z + st * 32768, *sZlo = sZhi + 16384;
 
@@ -1432,7 +1526,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
 #pragma unroll
                     for (int j = 0; j < 16; j += 4) {
                         const float4 b4 = *reinterpret_cast<const float4 *>(sBeta + jc + j);
-                        const float4 g4 = *reinterpret_cast<const float4 *>(sGam + jc + j);
+                        const float4 g4 = *reinterpret_cast<const float4 *>(sGamK + jc + j);
                         bt[j] = b4.x; bt[j + 1] = b4.y; bt[j + 2] = b4.z; bt[j + 3] = b4.w;
                         gm[j] = g4.x; gm[j + 1] = g4.y; gm[j + 2] = g4.z; gm[j + 3] = g4.w;
                     }
@@ -1513,7 +1607,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             // O = (gamma Q S^T + P U) / sqrt(d), staged as a [token][value]
             // fp32 tile and written by one TMA store that clips tokens past T
             if constexpr (kOInZ) {
-                o_epilogue(sZhi, sGam, t0);   // while the S product runs (it writes only S)
+                o_epilogue(sZhi, sGamQ, t0);  // while the S product runs (it writes only S)
                 wait(&sh.mma_s, mma_phase);
                 mma_phase ^= 1;
                 ptx::tc_fence_after();
@@ -1521,7 +1615,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 wait(&sh.mma_s, mma_phase);
                 mma_phase ^= 1;
                 ptx::tc_fence_after();
-                o_epilogue(sRhi, sGam, t0);   // the S product has finished reading U~
+                o_epilogue(sRhi, sGamQ, t0);  // the S product has finished reading U~
             }
             // this stage is free: bring chunk c + 2 into it
             if (t == 0 && c + 2 < n_chunks && !*abort_flag) issue_qk(c + 2);
@@ -1531,7 +1625,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             float gC = 1.f;
             if (!last) {
                 wait(&sh.g_ready[(c + 1) & 3], (uint32_t)(((c + 1) >> 2) & 1));
-                gC = gsets[((c + 1) & 3) * 256 + 128 + 63];
+                gC = gsets[((c + 1) & 3) * GS + 128 + 63];
             }
 #pragma unroll 1
             for (int kg = 0; kg < (vrow ? D / 2 : 0); kg += 32) {
@@ -1627,7 +1721,7 @@ bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
 // head_dim 256, and head_dim 128 with few pairs: the chunk transform for
 // every chunk into the workspace, then the state walk (D / 64 CTAs per head,
 // 64 value rows each) reading it.
-template <int D>
+template <int D, bool NORM>
 cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     using CF = Cfg<D>;
     using ZC = ZCfg<D>;
@@ -1642,27 +1736,27 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
-        cudaError_t e = cudaFuncSetAttribute(chunk_z_kernel<D>,
+        cudaError_t e = cudaFuncSetAttribute(chunk_z_kernel<D, NORM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunked_kernel<D>,
+            e = cudaFuncSetAttribute(chunked_kernel<D, NORM>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
         return e;
     });
     if (attr_err != cudaSuccess) return attr_err;
     uint8_t *zws = static_cast<uint8_t *>(workspace);
     const long long z_grid = std::min<long long>(n_tasks, 3LL * current_sm_count());
-    chunk_z_kernel<D><<<(unsigned)z_grid, NT, ZC::SMEM, stream>>>(
+    chunk_z_kernel<D, NORM><<<(unsigned)z_grid, NT, ZC::SMEM, stream>>>(
         mq, mk, p.g, p.beta, zws, p.T, p.H, p.Hk, n_chunks, (int)n_tasks, p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunked_kernel<D><<<(unsigned)(p.B * p.H * CF::NVB), NT, CF::SMEM, stream>>>(
+    chunked_kernel<D, NORM><<<(unsigned)(p.B * p.H * CF::NVB), NT, CF::SMEM, stream>>>(
         mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
         p.status);
     return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool NORM>
 cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mo;
     if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
@@ -1672,11 +1766,11 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
-        return cudaFuncSetAttribute(d128::chunked_d128_kernel<D>,
+        return cudaFuncSetAttribute(d128::chunked_d128_kernel<D, NORM>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, d128::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    d128::chunked_d128_kernel<D><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
+    d128::chunked_d128_kernel<D, NORM><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
         mq, mk, mv, mo, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale,
         p.status);
     return cudaGetLastError();
@@ -1729,17 +1823,24 @@ size_t chunked_workspace_bytes(int B, int T, int H, int d, int) {
     return (size_t)B * (size_t)H * n_chunks * (size_t)Z_BYTES;
 }
 
+template <bool NORM>
+cudaError_t launch_chunked_t(const Problem &p, void *workspace, size_t ws_bytes,
+                             cudaStream_t stream) {
+    switch (p.d) {
+        case 64: return launch_ws<64, NORM>(p, stream);
+        case 128:
+            return d128_split(p.B, p.H) ? launch_d<128, NORM>(p, workspace, ws_bytes, stream)
+                                        : launch_ws<128, NORM>(p, stream);
+        case 256: return launch_d<256, NORM>(p, workspace, ws_bytes, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
                            cudaStream_t stream) {
     if (p.dtype != GDN_DTYPE_BF16) return cudaErrorInvalidValue;
-    switch (p.d) {
-        case 64: return launch_ws<64>(p, stream);
-        case 128:
-            return d128_split(p.B, p.H) ? launch_d<128>(p, workspace, ws_bytes, stream)
-                                        : launch_ws<128>(p, stream);
-        case 256: return launch_d<256>(p, workspace, ws_bytes, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return p.l2norm_qk ? launch_chunked_t<true>(p, workspace, ws_bytes, stream)
+                       : launch_chunked_t<false>(p, workspace, ws_bytes, stream);
 }
 
 }  // namespace gdn

@@ -65,6 +65,7 @@ struct Problem {
     int dtype;                     // GDN_DTYPE_F32 / GDN_DTYPE_BF16
     float scale;                   // (float)(1 / sqrt((double)d))
     int *status;                   // device status word (bounded waits report here)
+    bool l2norm_qk;                // divide q and k by their norm per token first
 };
 
 // Recurrent path (gdn_recurrent.cu): any T >= 1, d in {32, 64, 128, 256}.

@@ -22,6 +22,12 @@
 // written once: the state streams through HBM exactly once per call.  q, k,
 // v, g, beta of the next token are prefetched while the current one is
 // computed.
+//
+// Optional fused preprocessing (NORM): q and k are divided by their Euclidean
+// norm per token before the recurrence.  The two squared norms join the same
+// butterfly as the dot products, and the division is applied as scalars:
+// S k^ = (S k) / |k|, S q^ = (S q) / |q|, k^.q^ = (k.q) / (|k| |q|), and the
+// update adds (delta / |k|) k.  A zero vector stays zero (its scale is 0).
 #include <cuda_bf16.h>
 
 #include "../../include/gdn.h"
@@ -96,7 +102,10 @@ struct TokenInputs {
     float g, beta;
 };
 
-template <int D, int L, int R, typename Tin>
+// 1 / |x| from the squared norm, 0 for a zero vector.
+__device__ __forceinline__ float inv_norm(float sq) { return sq > 0.f ? rsqrtf(sq) : 0.f; }
+
+template <int D, int L, int R, typename Tin, bool NORM>
 __global__ void __launch_bounds__(128)
 recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const Tin *__restrict__ v, const float *__restrict__ g,
@@ -185,7 +194,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
         for (int j = 0; j < NV; ++j) { unpack4(cur.q[j], qv[j]); unpack4(cur.k[j], kv[j]); }
 
-        float kq = 0.f, pk[R], pq[R];
+        float kq = 0.f, pk[R], pq[R], qq = 0.f, kk = 0.f;
 #pragma unroll
         for (int u = 0; u < R; ++u) { pk[u] = 0.f; pq[u] = 0.f; }
 #pragma unroll
@@ -193,6 +202,10 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 kq = fmaf(kv[j][e], qv[j][e], kq);
+                if constexpr (NORM) {
+                    qq = fmaf(qv[j][e], qv[j][e], qq);
+                    kk = fmaf(kv[j][e], kv[j][e], kk);
+                }
 #pragma unroll
                 for (int u = 0; u < R; ++u) {
                     pk[u] = fmaf(s[u][j][e], kv[j][e], pk[u]);
@@ -204,11 +217,23 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
         for (int off = L / 2; off > 0; off >>= 1) {
             kq += __shfl_xor_sync(0xffffffffu, kq, off);
+            if constexpr (NORM) {
+                qq += __shfl_xor_sync(0xffffffffu, qq, off);
+                kk += __shfl_xor_sync(0xffffffffu, kk, off);
+            }
 #pragma unroll
             for (int u = 0; u < R; ++u) {
                 pk[u] += __shfl_xor_sync(0xffffffffu, pk[u], off);
                 pq[u] += __shfl_xor_sync(0xffffffffu, pq[u], off);
             }
+        }
+        float ik = 1.f;                               // 1 / |k| (NORM), else 1
+        if constexpr (NORM) {
+            ik = inv_norm(kk);
+            const float iq = inv_norm(qq);
+            kq *= ik * iq;
+#pragma unroll
+            for (int u = 0; u < R; ++u) { pk[u] *= ik; pq[u] *= iq; }
         }
 
         const float alpha = expf(cur.g);
@@ -216,11 +241,12 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
         for (int u = 0; u < R; ++u) {
             const float delta = cur.beta * (cur.v[u] - alpha * pk[u]);
+            const float dk = NORM ? delta * ik : delta;   // the update adds delta k^
 #pragma unroll
             for (int j = 0; j < NV; ++j)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    s[u][j][e] = fmaf(alpha, s[u][j][e], delta * kv[j][e]);
+                    s[u][j][e] = fmaf(alpha, s[u][j][e], dk * kv[j][e]);
             const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
             if (sub == 0) op[o + row0 + u * RU] = ov;
         }
@@ -277,11 +303,13 @@ struct alignas(16) TokenWindow {
     Tin v[WT][RB];
     float g[WT];
     float beta[WT];
-    float kq[WT];      // k . q of each token, shared by every row
+    float kq[WT];      // k . q of each token (of the normalised q, k with NORM)
     float alpha[WT];   // exp(g) of each token
+    float ik[WT];      // 1 / |k| of each token (NORM)
+    float iq[WT];      // 1 / |q| of each token (NORM)
 };
 
-template <int D, int L, int R, typename Tin, int WT>
+template <int D, int L, int R, typename Tin, int WT, bool NORM>
 __global__ void __launch_bounds__(128)
 recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         const Tin *__restrict__ v, const float *__restrict__ g,
@@ -378,13 +406,31 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         const int nt = min(WT, T - t0);
         // the per-token scalars every row needs, once per token: one warp each
         for (int j = warp; j < nt; j += 4) {
-            float acc = 0.f;
+            float acc = 0.f, qq = 0.f, kk = 0.f;
 #pragma unroll
-            for (int e = lane; e < D; e += 32)
-                acc = fmaf(lds_scalar(&W_.q[j][e]), lds_scalar(&W_.k[j][e]), acc);
+            for (int e = lane; e < D; e += 32) {
+                const float qe = lds_scalar(&W_.q[j][e]), ke = lds_scalar(&W_.k[j][e]);
+                acc = fmaf(qe, ke, acc);
+                if constexpr (NORM) {
+                    qq = fmaf(qe, qe, qq);
+                    kk = fmaf(ke, ke, kk);
+                }
+            }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            for (int off = 16; off > 0; off >>= 1) {
+                acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                if constexpr (NORM) {
+                    qq += __shfl_xor_sync(0xffffffffu, qq, off);
+                    kk += __shfl_xor_sync(0xffffffffu, kk, off);
+                }
+            }
             if (lane == 0) {
+                if constexpr (NORM) {
+                    const float ik = inv_norm(kk), iq = inv_norm(qq);
+                    W_.ik[j] = ik;
+                    W_.iq[j] = iq;
+                    acc *= ik * iq;
+                }
                 W_.kq[j] = acc;
                 W_.alpha[j] = expf(W_.g[j]);
             }
@@ -426,11 +472,19 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             const float kq = W_.kq[j];
             const float bt = W_.beta[j];
             const size_t o = (size_t)(t0 + j) * tok_stride;
+            float ik = 1.f;
+            if constexpr (NORM) {
+                ik = W_.ik[j];
+                const float iq = W_.iq[j];
+#pragma unroll
+                for (int u = 0; u < R; ++u) { pk[u] *= ik; pq[u] *= iq; }
+            }
 #pragma unroll
             for (int u = 0; u < R; ++u) {
                 const float vv = lds_scalar(&W_.v[j][lrow0 + u * RU]);
                 const float delta = bt * (vv - alpha * pk[u]);
-                const float2 a2 = make_float2(alpha, alpha), d2 = make_float2(delta, delta);
+                const float dk = NORM ? delta * ik : delta;    // the update adds delta k^
+                const float2 a2 = make_float2(alpha, alpha), d2 = make_float2(dk, dk);
 #pragma unroll
                 for (int jv = 0; jv < NV; ++jv)
 #pragma unroll
@@ -460,7 +514,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 // Tokens staged per window by the multi-token kernel.
 constexpr int kWindow = 8;
 
-template <int D, int L, int R, typename Tin>
+template <int D, int L, int R, typename Tin, bool NORM>
 cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     constexpr int RB = 4 * R * (32 / L);
     cudaLaunchConfig_t cfg = {};
@@ -476,34 +530,34 @@ cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.T >= 2)
-        return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow>,
+        return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow, NORM>,
                                   static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
                                   static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in,
                                   p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
-    return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin>, static_cast<const Tin *>(p.q),
+    return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin, NORM>, static_cast<const Tin *>(p.q),
                               static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v), p.g,
                               p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
 }
 
-template <int D, int L, typename Tin>
+template <int D, int L, typename Tin, bool NORM>
 cudaError_t launch_d(const Problem &p, cudaStream_t stream) {
     // Two rows per warp unit when there are enough blocks to fill the GPU
     // several times over (more bytes in flight per thread); one otherwise.
     constexpr int RB2 = 4 * 2 * (32 / L);
     const long long blocks2 = (long long)p.B * p.H * (D / RB2);
     if (D % RB2 == 0 && blocks2 >= 4LL * current_sm_count())
-        return launch_one<D, L, 2, Tin>(p, stream);
-    return launch_one<D, L, 1, Tin>(p, stream);
+        return launch_one<D, L, 2, Tin, NORM>(p, stream);
+    return launch_one<D, L, 1, Tin, NORM>(p, stream);
 }
 
-template <typename Tin>
+template <typename Tin, bool NORM>
 cudaError_t launch_dtype(const Problem &p, cudaStream_t stream) {
     switch (p.d) {
-        case 32: return launch_one<32, 8, 1, Tin>(p, stream);
-        case 64: return launch_d<64, 8, Tin>(p, stream);
-        case 96: return launch_d<96, 8, Tin>(p, stream);
-        case 128: return launch_d<128, 8, Tin>(p, stream);
-        case 256: return launch_d<256, 16, Tin>(p, stream);
+        case 32: return launch_one<32, 8, 1, Tin, NORM>(p, stream);
+        case 64: return launch_d<64, 8, Tin, NORM>(p, stream);
+        case 96: return launch_d<96, 8, Tin, NORM>(p, stream);
+        case 128: return launch_d<128, 8, Tin, NORM>(p, stream);
+        case 256: return launch_d<256, 16, Tin, NORM>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -511,8 +565,10 @@ cudaError_t launch_dtype(const Problem &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream) {
-    if (p.dtype == GDN_DTYPE_BF16) return launch_dtype<__nv_bfloat16>(p, stream);
-    return launch_dtype<float>(p, stream);
+    if (p.dtype == GDN_DTYPE_BF16)
+        return p.l2norm_qk ? launch_dtype<__nv_bfloat16, true>(p, stream)
+                           : launch_dtype<__nv_bfloat16, false>(p, stream);
+    return p.l2norm_qk ? launch_dtype<float, true>(p, stream) : launch_dtype<float, false>(p, stream);
 }
 
 }  // namespace gdn

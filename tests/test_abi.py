@@ -219,5 +219,16 @@ def test_flash_attn_empty_is_a_no_op(L):
     assert attn_call(L, H=0, Hkv=0, q=None, k=None, v=None, mask=None, out=None) == gdn.OK
 
 
+def test_option_bits(L):
+    # GDN_OPT_L2NORM_QK is accepted in the path argument; unknown bits are not
+    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | gdn.OPT_L2NORM_QK) == 32 * 64 * 32768
+    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | 0x200) == 0
+    assert call(L, path=0x200) == gdn.ERR_ARG
+    assert call(L, path=0x101 | 0x400) == gdn.ERR_ARG
+    assert call(L, path=-1) == gdn.ERR_ARG
+    # a valid option still goes through host validation (here: misaligned q)
+    assert call(L, q=BASE + 8, path=gdn.OPT_L2NORM_QK) == gdn.ERR_ALIGN
+
+
 def test_gdn_entry_points_reject_f16(L):
     assert call(L, dtype=2) == gdn.ERR_ARG

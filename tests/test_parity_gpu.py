@@ -541,3 +541,78 @@ def test_bounded_wait_reports_timeout_and_the_context_stays_usable():
     assert gdn.device_status() == gdn.OK                 # read and cleared
     w = W.Workload("after_timeout", 1, 100, 2, 128, "bf16", 0.0, 0.02, seed=90)
     check(W.make_inputs(w, "cuda"), "bf16", "chunked")
+
+
+# ------------------------------------------------- fused q / k normalisation
+
+def raw_qk(inp, seed, Hk=None):
+    """Unnormalised q, k in place of the workload's: N(0, 1) times a
+    per-token, per-head power of two in [1/8, 8], and a few all-zero
+    vectors (which must stay zero)."""
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    out = dict(inp)
+    for name in ("q", "k"):
+        x = inp[name]
+        B, T, Hx, d = x.shape
+        raw = torch.randn((B, T, Hx, d), generator=gen, device="cuda")
+        e = torch.randint(-3, 4, (B, T, Hx, 1), generator=gen, device="cuda").float()
+        raw = raw * torch.pow(2.0, e)
+        raw[:, T // 3::7, 0] = 0.0
+        out[name] = raw.to(x.dtype).contiguous()
+    return out
+
+
+def check_l2norm(inp, dtype, path, tol):
+    out, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                          path=path, l2norm_qk=True)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    n = W.to_numpy_f32(inp)
+    ref_out, ref_st = oracle.recurrent_c(n["q"], n["k"], n["v"], n["g"], n["beta"], n["state"],
+                                         l2norm_qk=True)
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= tol and e_st <= tol, (path, e_out, e_st)
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 256])
+@pytest.mark.parametrize("T", [1, 5, 70, 200])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fused_qk_l2norm(d, T, dtype):
+    """q and k normalised inside the op (GDN_OPT_L2NORM_QK) on every path:
+    the recurrent kernels fold the norms into their butterfly, the chunked
+    kernels into per-token scalars of the chunk algebra."""
+    w = W.Workload(f"l2n_d{d}_t{T}", 2, T, 4, d, dtype, 0.0, 0.02, seed=80 + T)
+    inp = raw_qk(W.make_inputs(w, "cuda"), seed=81 + d)
+    for path in ["auto"] + paths_for(d, T, dtype):
+        tol = TOL_RECURRENT if path == "recurrent" else TOL[dtype]
+        check_l2norm(inp, dtype, path, tol)
+
+
+@pytest.mark.parametrize("H,Hk", [(48, 48), (48, 12), (8, 2)])
+def test_fused_qk_l2norm_chunked_kernels_and_key_heads(H, Hk):
+    """The one-kernel head_dim-128 path (96 pairs), fewer key heads, and the
+    two-kernel path, with in-op normalisation and a ragged tail."""
+    w = W.Workload(f"l2n_h{H}_hk{Hk}", 2, 150, H, 128, "bf16", 2.0, 0.02, seed=82)
+    inp = W.make_inputs(w, "cuda")
+    inp["q"] = inp["q"][:, :, :Hk].contiguous()
+    inp["k"] = inp["k"][:, :, :Hk].contiguous()
+    inp = raw_qk(inp, seed=83)
+    for path in ("chunked", "recurrent"):
+        check_l2norm(inp, "bf16", path, TOL_RECURRENT if path == "recurrent" else TOL["bf16"])
+
+
+def test_fused_qk_l2norm_of_unit_inputs_changes_nothing_measurable():
+    """On already-normalised inputs (the workloads') the option leaves the
+    result within fp32 rounding of the plain call."""
+    w = W.Workload("l2n_unit", 2, 130, 4, 128, "bf16", 0.0, 0.02, seed=84)
+    inp = W.make_inputs(w, "cuda")
+    for path in ("recurrent", "chunked"):
+        o1, s1 = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                             path=path)
+        o2, s2 = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                             path=path, l2norm_qk=True)
+        torch.cuda.synchronize()
+        rel = lambda a, b: ((a - b).abs().max() / b.pow(2).mean().sqrt()).item()
+        # bf16 q / k normalised in fp32 have norms within ~2^-8 of 1
+        assert rel(o2, o1) < 2e-2 and rel(s2, s1) < 2e-2, path
