@@ -616,3 +616,27 @@ def test_fused_qk_l2norm_of_unit_inputs_changes_nothing_measurable():
         rel = lambda a, b: ((a - b).abs().max() / b.pow(2).mean().sqrt()).item()
         # bf16 q / k normalised in fp32 have norms within ~2^-8 of 1
         assert rel(o2, o1) < 2e-2 and rel(s2, s1) < 2e-2, path
+
+
+# ------------------------------------------------ back-to-back state reuse
+
+@pytest.mark.parametrize("T", [1, 5])
+def test_default_reads_state_after_the_previous_kernel(T):
+    """A call that reads the state the previous call on the stream is still
+    writing (in place, back to back, launched with programmatic stream
+    serialization) sees the finished state: ten chained steps equal one
+    ten-token run."""
+    w = W.Workload("chain", 2, 10 * T, 4, 128, "bf16", 0.0, 0.02, seed=23)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    st = inp["state"].clone()
+    outs = []
+    for i in range(10):
+        sl = slice(i * T, (i + 1) * T)
+        o, _ = gdn.forward(inp["q"][:, sl].contiguous(), inp["k"][:, sl].contiguous(),
+                           inp["v"][:, sl].contiguous(), inp["g"][:, sl].contiguous(),
+                           inp["beta"][:, sl].contiguous(), st, state_out=st, path="recurrent")
+        outs.append(o)
+    torch.cuda.synchronize()
+    e_out, e_st = errs(torch.cat(outs, dim=1), st, ref_out, ref_st)
+    assert e_out <= TOL_RECURRENT and e_st <= TOL_RECURRENT, (e_out, e_st)
