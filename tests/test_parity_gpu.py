@@ -142,15 +142,17 @@ def sampled_reference(w, inp, pairs):
     (one OpenMP thread per pair); cached per workload and sample."""
     key = (w.name, tuple(pairs))
     if key not in _SAMPLE_REF:
-        n = W.to_numpy_f32(inp)
         bs = [b for b, _ in pairs]
         hs = [h for _, h in pairs]
-        Hk = n["q"].shape[2]
+        Hk = inp["q"].shape[2]
         hks = [h % Hk for h in hs]
+        # gather the sampled pairs on the device, then copy only them
+        f32 = lambda t: t.float().cpu().numpy()
         pick = lambda x, heads: np.ascontiguousarray(
-            np.stack([x[b, :, hh] for b, hh in zip(bs, heads)])[:, :, None])
-        st = None if n["state"] is None else np.ascontiguousarray(
-            np.stack([n["state"][b, h] for b, h in pairs])[:, None])
+            f32(torch.stack([x[b, :, hh] for b, hh in zip(bs, heads)]))[:, :, None])
+        n = {key_: inp[key_] for key_ in ("q", "k", "v", "g", "beta")}
+        st = None if inp["state"] is None else np.ascontiguousarray(
+            f32(torch.stack([inp["state"][b, h] for b, h in pairs]))[:, None])
         _SAMPLE_REF[key] = oracle.recurrent_c(pick(n["q"], hks), pick(n["k"], hks),
                                               pick(n["v"], hs), pick(n["g"], hs),
                                               pick(n["beta"], hs), st)
@@ -640,3 +642,53 @@ def test_default_reads_state_after_the_previous_kernel(T):
     torch.cuda.synchronize()
     e_out, e_st = errs(torch.cat(outs, dim=1), st, ref_out, ref_st)
     assert e_out <= TOL_RECURRENT and e_st <= TOL_RECURRENT, (e_out, e_st)
+
+
+# ------------------------------------------------------------- maximum sizes
+
+def _check_sample(w, inp, out, st, pairs, tol):
+    ref_out, ref_st = sampled_reference(w, inp, pairs)
+    got_out = np.stack([out[b, :, h].double().cpu().numpy() for b, h in pairs])
+    got_st = np.stack([st[b, h].double().cpu().numpy() for b, h in pairs])
+    e_out = oracle.parity_error(got_out.ravel(), ref_out.ravel())
+    e_st = oracle.parity_error(got_st.ravel(), ref_st.ravel())
+    assert e_out <= tol and e_st <= tol, (e_out, e_st)
+
+
+def test_decode_with_65536_sequence_head_pairs():
+    """One decode launch over 2048 sequences x 32 heads (a 65,536-row grid,
+    4 GiB of fp32 state updated in place); the oracle recomputes a sample of
+    pairs with at least one from every wave of blocks."""
+    w = W.Workload("decode_b2048_h32_d128", 2048, 1, 32, 128, "bf16", 0.0, 0.02, seed=91)
+    inp = W.make_inputs(w, "cuda")
+    st0 = inp["state"]
+    pairs = sampled_pairs(w, 24, per_cta=1)
+    ref = sampled_reference(w, inp, pairs)            # before the in-place update
+    out, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st0,
+                          state_out=st0)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    got_out = np.stack([out[b, :, h].double().cpu().numpy() for b, h in pairs])
+    got_st = np.stack([st[b, h].double().cpu().numpy() for b, h in pairs])
+    assert oracle.parity_error(got_out.ravel(), ref[0].ravel()) <= TOL_RECURRENT
+    assert oracle.parity_error(got_st.ravel(), ref[1].ravel()) <= TOL_RECURRENT
+
+
+@pytest.mark.parametrize("T,H,d", [(131072, 2, 64), (65536, 2, 128)])
+def test_long_sequences_chunked(T, H, d):
+    """Long runs on the chunked path: 2048 chunks of 64 tokens on the
+    one-kernel path (head_dim 64) and 1024 chunks on the two-kernel path
+    (head_dim 128, two (sequence, head) pairs, a 64 MiB transform workspace),
+    every output and the final state against the oracle."""
+    w = W.Workload(f"long_t{T}_d{d}", 1, T, H, d, "bf16", 0.0, 0.02, seed=92)
+    inp = W.make_inputs(w, "cuda")
+    out, st = run_gpu(inp, "chunked")
+    _check_sample(w, inp, out, st, [(0, h) for h in range(H)], TOL["bf16"])
+
+
+def test_long_run_recurrent_window():
+    """65,536 tokens through the windowed recurrent kernel (8192 windows)."""
+    w = W.Workload("long_rec", 1, 65536, 4, 64, "bf16", 0.0, 0.02, seed=93)
+    inp = W.make_inputs(w, "cuda")
+    out, st = run_gpu(inp, "recurrent")
+    _check_sample(w, inp, out, st, [(0, h) for h in range(4)], TOL_RECURRENT)
