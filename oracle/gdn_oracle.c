@@ -151,12 +151,13 @@ int gdn_oracle_forward(const float *q, const float *k, const float *v,
     const long n_pairs = (long)B * H;
     int failed = 0;
 #ifdef _OPENMP
-    if (n_threads > 0)
-        omp_set_num_threads(n_threads);
+    /* The count applies to this call only: a one-thread call leaves the
+     * default for the calls after it unchanged. */
+    const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
 #else
     (void)n_threads;
 #endif
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
     {
         double *S = (double *)malloc(sizeof(double) * (size_t)d * d);
         double *r = (double *)malloc(sizeof(double) * (size_t)d * 3);

@@ -48,3 +48,18 @@ def test_launch_counts():
     assert bench.launches_per_call("recurrent", 0) == 1
     assert bench.launches_per_call("chunked", 0) == 1          # one-kernel chunked path
     assert bench.launches_per_call("chunked", 1 << 20) == 2    # transform pass + state walk
+
+
+def test_one_thread_oracle_call_keeps_the_default_thread_count():
+    """The bench times the oracle on one thread once; the CPU baselines
+    measured after it must still see every OpenMP thread."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    before = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    x = {n: rng.standard_normal(s).astype(np.float32)
+         for n, s in (("q", (1, 2, 2, 8)), ("k", (1, 2, 2, 8)), ("v", (1, 2, 2, 8)),
+                      ("g", (1, 2, 2)), ("beta", (1, 2, 2)))}
+    oracle.recurrent_c(x["q"], x["k"], x["v"], -np.abs(x["g"]), x["beta"], None, n_threads=1)
+    assert oracle.max_threads() == before
