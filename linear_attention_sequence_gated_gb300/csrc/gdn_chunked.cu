@@ -29,7 +29,8 @@
 //   - chunk_z_kernel + chunked_kernel (head_dim 256, and head_dim 128 with
 //     few (sequence, head) pairs): persistent CTAs write every chunk's Z to
 //     a workspace; the state walk then runs one CTA per block of 64 value
-//     rows, keys on lanes, the fp32 state in registers.
+//     rows (32 where that still fits the pairs into one wave of CTAs), keys
+//     on lanes, the fp32 state in registers.
 // Per chunk:
 //   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile) and
 //      V; plain loads bring g, beta.
@@ -69,22 +70,42 @@ constexpr int NT = 256;          // threads per CTA (two warpgroups)
 constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrices (16-B rows)
 
 // Shared-memory and TMEM map of the state kernel (head_dim 256, and 128 with
-// few pairs).  The chunk
-// transform Z = [T; P T] arrives ready-made from the workspace (written by
-// chunk_z_kernel), so a CTA only carries BV = 64 value rows of the state.
-template <int D>
+// few pairs).  The chunk transform Z = [T; P T] arrives ready-made from the
+// workspace (written by chunk_z_kernel), so a CTA only carries BV value rows
+// of the state: 64, or 32 to double the CTAs of a small problem.  The tiles
+// whose columns are value indices (V, S hi / lo, R / U~ hi / lo) have rows
+// of BV bf16: 128 B with the 128-byte swizzle (BV 64), 64 B with the 64-byte
+// swizzle (BV 32).
+template <int D, int BV_>
 struct Cfg {
-    static constexpr int BV = 64;                          // value rows per CTA
+    static constexpr int BV = BV_;                         // value rows per CTA
+    static constexpr int ROWB = 2 * BV;                    // bytes per row of a value tile
+    static constexpr uint64_t SWZ = BV == 64 ? ptx::kSwizzle128 : ptx::kSwizzle64;
     static constexpr int NVB = D / BV;                     // CTAs per (sequence, head)
     static constexpr int KT = (D + 127) / 128;            // 128-key tiles of the state update
     static constexpr int NSLAB = D / 64;                   // 64-key slabs of [K;Q]
+    static_assert(BV == 64 || BV == 32, "value block of 64 or 32 rows");
+    static constexpr int QK_BYTES = NSLAB * 16384;         // one chunk's [K;Q]: NSLAB x (128 rows x 128 B)
+    static constexpr int V_BYTES = 64 * ROWB;              // one chunk's V block: 64 rows x ROWB
+    static constexpr int ZT_BYTES = 2 * 16384;             // one chunk's Z hi, Z lo: 128 rows x 128 B each
+    // PW: a ninth warp issues the loads, into two slots of each streamed tile
+    // where shared memory allows, so that the next chunk's tiles land while
+    // this one is computed.  Not at head_dim 256 with 64-row blocks: its
+    // 64-register state block needs the register budget of eight warps (a
+    // ninth rounds the budget to twelve), and only one slot of [K;Q] and V
+    // fits.  There thread 0 issues each load as soon as its slot is free.
+    static constexpr bool PW = !(D == 256 && BV == 64);
+    static constexpr int NQK = PW && D == 128 ? 2 : 1;
+    static constexpr int NZS = PW ? 2 : 1;
+    static constexpr int NVS = PW ? 2 : 1;
+    static constexpr int NTH = PW ? NT + 32 : NT;          // threads per CTA
     // shared memory map (bytes from a 1024-aligned base)
-    static constexpr int OFF_QK = 0;                       // [K;Q]: NSLAB x (128 rows x 128 B)
-    static constexpr int OFF_V = OFF_QK + NSLAB * 16384;   // V block, 64 rows
-    static constexpr int OFF_Z = OFF_V + 8192;             // Z hi, Z lo: 128 rows x 128 B each
-    static constexpr int OFF_S = OFF_Z + 2 * 16384;        // S hi, S lo: D rows x 128 B each
-    static constexpr int OFF_RU = OFF_S + 2 * D * 128;     // R (then U~) hi, lo: 64 rows x 128 B
-    static constexpr int OFF_MISC = OFF_RU + 2 * 8192;     // 2 gate sets: G, beta, gamma, end-decay
+    static constexpr int OFF_QK = 0;
+    static constexpr int OFF_V = OFF_QK + NQK * QK_BYTES;
+    static constexpr int OFF_Z = OFF_V + NVS * V_BYTES;
+    static constexpr int OFF_S = OFF_Z + NZS * ZT_BYTES;   // S hi, S lo: D rows x ROWB each
+    static constexpr int OFF_RU = OFF_S + 2 * D * ROWB;    // R (then U~) hi, lo: 64 rows x ROWB
+    static constexpr int OFF_MISC = OFF_RU + 2 * 64 * ROWB; // 2 gate sets: G, beta, gamma, end-decay
     static constexpr int OFF_NRM = OFF_MISC + 2 * 4 * 64 * 4;  // 1/|k|, 1/|q| of the chunk
     static constexpr int SMEM = OFF_NRM + 2 * 64 * 4 + 1024;   // + alignment slack
     // TMEM columns
@@ -93,7 +114,10 @@ struct Cfg {
     static constexpr int COL_DS = 2 * BV;
     static constexpr int TMEM_COLS = 256;
     static_assert(COL_DS + KT * BV <= TMEM_COLS, "TMEM columns");
-    static_assert(SMEM + 64 <= 232448, "shared memory (dynamic + static)");
+    static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
+    static_assert(OFF_V % 1024 == 0 && V_BYTES % 1024 == 0 && OFF_Z % 1024 == 0 && OFF_S % 1024 == 0 && OFF_RU % 1024 == 0 &&
+                  (D * ROWB) % 1024 == 0 && (64 * ROWB) % 1024 == 0,
+                  "swizzled tiles on 1024-byte boundaries");
 };
 
 // Bytes of one chunk's Z = [T; P T] in the workspace: bf16 hi then lo, each
@@ -125,6 +149,18 @@ struct ZCfg {
 
 struct Bars {
     uint64_t tma;
+    uint64_t mma;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Barriers of the state walk: a full / empty pair for each slot of each
+// streamed tile ([K;Q], V, Z), the MMA-completion barrier, the TMEM base
+// and the abort flag.
+struct WalkBars {
+    uint64_t full_qk[2], empty_qk[2];
+    uint64_t full_v[2], empty_v[2];
+    uint64_t full_z[2], empty_z[2];
     uint64_t mma;
     uint32_t tmem_base;
     int abort;
@@ -171,10 +207,12 @@ __device__ __forceinline__ void qk_row_sumsq(const uint8_t *qk, int r, float &kk
 // Store 16 consecutive fp32 values as bf16 hi / lo into two 128-B-swizzled
 // tiles at (row, col0 .. col0+15); col0 is a multiple of 8.  hi keeps the top
 // 16 bits of each value, lo = bf16_rn(x - hi): ~16 significant bits together.
+template <int ROWB = 128>
 __device__ __forceinline__ void store_split16(uint8_t *hi_tile, uint8_t *lo_tile, int row, int col0,
                                               const float (&x)[16]) {
-    ptx::store_split8(hi_tile, lo_tile, row, col0, *reinterpret_cast<const float(*)[8]>(x));
-    ptx::store_split8(hi_tile, lo_tile, row, col0 + 8, *reinterpret_cast<const float(*)[8]>(x + 8));
+    ptx::store_split8<ROWB>(hi_tile, lo_tile, row, col0, *reinterpret_cast<const float(*)[8]>(x));
+    ptx::store_split8<ROWB>(hi_tile, lo_tile, row, col0 + 8,
+                            *reinterpret_cast<const float(*)[8]>(x + 8));
 }
 
 // Warp-level bf16 MMA, m16n8k16, fp32 accumulate in place: d += a b.
@@ -607,29 +645,30 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (warp == 0) ptx::tmem_dealloc(tmem, 64);
 }
 
-template <int D, bool NORM>
-__global__ void __launch_bounds__(NT, 1)
+template <int D, int BV_, bool NORM>
+__global__ void __launch_bounds__(Cfg<D, BV_>::NTH, 1)
 chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
                const float *__restrict__ beta, const float *state_in, float *state_out,
                float *__restrict__ out, const uint8_t *__restrict__ zws, int T, int H, int Hk,
                float scale, int *status)
 {
-    using CF = Cfg<D>;
+    using CF = Cfg<D, BV_>;
     constexpr int BV = CF::BV;
+    constexpr int ROWB = CF::ROWB;
     constexpr int KT = CF::KT;
     constexpr int HALF = BV / 2;          // value columns per warpgroup
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-    __shared__ Bars bars;
+    __shared__ WalkBars bars;
     float *gsets = reinterpret_cast<float *>(sm + CF::OFF_MISC);   // set i: gsets + 256 i
     float *sNk = reinterpret_cast<float *>(sm + CF::OFF_NRM), *sNq = sNk + 64;
-    uint8_t *sQK = sm + CF::OFF_QK;
-    uint8_t *sV = sm + CF::OFF_V;
-    uint8_t *sZhi = sm + CF::OFF_Z, *sZlo = sm + CF::OFF_Z + 16384;
-    uint8_t *sShi = sm + CF::OFF_S, *sSlo = sm + CF::OFF_S + D * 128;
-    uint8_t *sRhi = sm + CF::OFF_RU, *sRlo = sm + CF::OFF_RU + 8192;
+    uint8_t *sQK0 = sm + CF::OFF_QK;      // slot s at + s * QK_BYTES
+    uint8_t *sV0 = sm + CF::OFF_V;        // slot s at + s * V_BYTES
+    uint8_t *sZ0 = sm + CF::OFF_Z;        // slot s at + s * Z_BYTES (hi, then lo)
+    uint8_t *sShi = sm + CF::OFF_S, *sSlo = sm + CF::OFF_S + D * ROWB;
+    uint8_t *sRhi = sm + CF::OFF_RU, *sRlo = sm + CF::OFF_RU + 64 * ROWB;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -637,6 +676,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int wg = tid >> 7;                 // warpgroup: which half of the value columns
     const int row = tid & 127;               // TMEM lane this thread reads
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    constexpr bool PW = CF::PW;
+    const bool producer = PW && warp == NT / 32;   // warp 8: the loads; warps 0-7: the chain
     // the value blocks of one head are neighbours in the grid, so they share
     // their [K;Q] and Z reads through L2
     const int bh = blockIdx.x / CF::NVB;
@@ -647,7 +688,15 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     if (tid == 0) {
         bars.abort = 0;
-        ptx::mbar_init(&bars.tma, 1);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(&bars.full_qk[s], 1);
+            ptx::mbar_init(&bars.empty_qk[s], 1);
+            ptx::mbar_init(&bars.full_v[s], 1);
+            ptx::mbar_init(&bars.empty_v[s], 1);
+            ptx::mbar_init(&bars.full_z[s], 1);
+            ptx::mbar_init(&bars.empty_z[s], 1);
+        }
         ptx::mbar_init(&bars.mma, 1);
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tm_q);
@@ -658,30 +707,32 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         ptx::tmem_alloc(&bars.tmem_base, CF::TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    // ---- initial state block into registers: key = kt*128 + row, values
-    //      v0 + wg*HALF + j; coalesced over keys
+    // ---- initial state block into registers (warps 0-7): key = kt*128 +
+    //      row, values v0 + wg*HALF + j; coalesced over keys
     float S[KT][HALF];
     const size_t st_base = (size_t)bh * D * D;
+    if (!producer) {
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
-        const int key = kt * 128 + row;
+        for (int kt = 0; kt < KT; ++kt) {
+            const int key = kt * 128 + row;
 #pragma unroll
-        for (int j = 0; j < HALF; ++j) {
-            const int v = v0 + wg * HALF + j;
-            S[kt][j] = (state_in && key < D) ? state_in[st_base + (size_t)v * D + key] : 0.f;
+            for (int j = 0; j < HALF; ++j) {
+                const int v = v0 + wg * HALF + j;
+                S[kt][j] = (state_in && key < D) ? state_in[st_base + (size_t)v * D + key] : 0.f;
+            }
         }
-    }
-    // S hi / lo tiles: row = key, columns = value index within the block
+        // S hi / lo tiles: row = key, columns = value index within the block
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt) {
-        const int key = kt * 128 + row;
-        if (key < D) {
+        for (int kt = 0; kt < KT; ++kt) {
+            const int key = kt * 128 + row;
+            if (key < D) {
 #pragma unroll
-            for (int j = 0; j < HALF; j += 16) {
-                float x[16];
+                for (int j = 0; j < HALF; j += 16) {
+                    float x[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
-                store_split16(sShi, sSlo, key, wg * HALF + j, x);
+                    for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
+                    store_split16<ROWB>(sShi, sSlo, key, wg * HALF + j, x);
+                }
             }
         }
     }
@@ -691,332 +742,406 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     ptx::tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
     volatile int *abort_flag = &bars.abort;
-
-    uint32_t mma_phase = 0;
     auto fail = [&]() {
         if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
     };
-    // wait for the next MMA commit (all threads)
-    auto wait_mma = [&]() {
-        if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
-        mma_phase ^= 1;
-        ptx::tc_fence_after();
-    };
 
-    const uint32_t aQK = ptx::smem_u32(sQK);
-    const size_t tok_stride = (size_t)H * D;
-
-    // Loads of chunk c (thread 0).  Each buffer is refilled for the next chunk
-    // as soon as this chunk is done with it: V after R, Z after the Z R
-    // product, [K;Q] after the state-update product; all three land on the
-    // one transaction barrier of that chunk, armed with the first issue.
-    auto load_v = [&](int cc) {
-        constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192 + 64 * BV * 2 + Z_BYTES;
-        ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
-        ptx::tma_load_4d(sV, &tm_v, &bars.tma, v0, h, cc * C, b);
+    // ---- loads (one thread: lane 0 of warp 8, or thread 0).  Chunk c's
+    // [K;Q], V and Z go to slot c % (slots of that tile); the thread records
+    // the last chunk it loaded into each slot.
+    int last_qk[2] = {-1, -1}, last_v[2] = {-1, -1}, last_z[2] = {-1, -1};
+    auto issue_v = [&](int c) {
+        const int sv = c % CF::NVS;
+        ptx::mbar_arrive_expect_tx(&bars.full_v[sv], CF::V_BYTES);
+        ptx::tma_load_4d(sV0 + sv * CF::V_BYTES, &tm_v, &bars.full_v[sv], v0, h, c * C, b);
+        last_v[sv] = c;
     };
-    auto load_z = [&](int cc) {
-        ptx::bulk_load(sZhi, zbh + (size_t)cc * Z_BYTES, Z_BYTES, &bars.tma);
+    // Z as eight 4 KB copies: one 32 KB bulk copy was measured to land more
+    // than a chunk step after it was issued, several smaller ones in flight
+    // at once land sooner.
+    auto issue_z = [&](int c) {
+        const int sz = c % CF::NZS;
+        ptx::mbar_arrive_expect_tx(&bars.full_z[sz], Z_BYTES);
+#pragma unroll
+        for (int part = 0; part < 8; ++part)
+            ptx::bulk_load(sZ0 + sz * Z_BYTES + part * (Z_BYTES / 8),
+                           zbh + (size_t)c * Z_BYTES + part * (Z_BYTES / 8), Z_BYTES / 8,
+                           &bars.full_z[sz]);
+        last_z[sz] = c;
     };
-    auto load_qk = [&](int cc) {
+    auto issue_qk = [&](int c) {
+        const int sq = c % CF::NQK;
+        ptx::mbar_arrive_expect_tx(&bars.full_qk[sq], CF::QK_BYTES);
+        uint8_t *dst = sQK0 + sq * CF::QK_BYTES;
 #pragma unroll
         for (int s = 0; s < D / 64; ++s) {
-            ptx::tma_load_4d(sQK + s * 16384, &tm_k, &bars.tma, s * 64, h % Hk, cc * C, b);
-            ptx::tma_load_4d(sQK + s * 16384 + 8192, &tm_q, &bars.tma, s * 64, h % Hk, cc * C, b);
+            ptx::tma_load_4d(dst + s * 16384, &tm_k, &bars.full_qk[sq], s * 64, h % Hk, c * C, b);
+            ptx::tma_load_4d(dst + s * 16384 + 8192, &tm_q, &bars.full_qk[sq], s * 64, h % Hk,
+                             c * C, b);
+        }
+        last_qk[sq] = c;
+    };
+    // every copy addressed to this CTA's shared memory lands before the CTA
+    // can exit (a bounded wait; on the normal path each of these phases has
+    // completed already)
+    auto drain = [&]() {
+        const volatile int never = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (last_v[s] >= 0)
+                ptx::mbar_wait(&bars.full_v[s], (uint32_t)((last_v[s] / CF::NVS) & 1), &never,
+                               1000000000LL);
+            if (last_z[s] >= 0)
+                ptx::mbar_wait(&bars.full_z[s], (uint32_t)((last_z[s] / CF::NZS) & 1), &never,
+                               1000000000LL);
+            if (last_qk[s] >= 0)
+                ptx::mbar_wait(&bars.full_qk[s], (uint32_t)((last_qk[s] / CF::NQK) & 1), &never,
+                               1000000000LL);
         }
     };
-    // thread 0 tracks the chunk whose loads are armed but not yet waited for
-    // (and which of its three loads were issued), to drain them on abort
-    int armed = -1, issued = 0;
-    if (tid == 0 && n_chunks > 0) {
-        load_v(0);
-        load_z(0);
-        load_qk(0);
-        armed = 0;
-        issued = 7;
-    }
 
-    // Gates: warps 2 and 3 (threads 64-127, TMEM lanes 64-127, idle while the
-    // other warps build R) scan the next chunk's g into the other of two gate
-    // sets during step 5, from g and beta they loaded one chunk earlier; the
-    // set of chunk 0 is built here.  Set layout: G (in-chunk running sum of g,
-    // each clamped at -30: exp(-30) ~ 1e-13, a reset stays a reset), beta,
-    // gamma = exp(G), end-decay = exp(G_63 - G).
-    const bool gate_thread = tid >= 64 && tid < 128;
-    const int gr_ = tid - 64;                          // token of the chunk (gate threads)
-    float gnext = 0.f, bnext = 0.f;
-    auto load_gates = [&](int cc) {                   // g, beta of chunk cc into gnext / bnext
-        gnext = 0.f;
-        bnext = 0.f;
-        if (cc * C + gr_ < T) {
-            const size_t gi = ((size_t)b * T + cc * C + gr_) * H + h;
-            gnext = fmaxf(g[gi], -30.f);
-            bnext = beta[gi];
+    if (producer) {
+        // Warp 8 refills a slot once the chunk that used it before has
+        // released it: V after its R epilogue, Z and [K;Q] when the last
+        // product reading them completes.  With two slots the loads run one
+        // chunk ahead of the products.  The order V, Z, [K;Q] is the order in
+        // which a chunk releases them.  A wait that gives up here records
+        // the timeout in the status word only: the abort flag is written by
+        // warps 0-7 alone, always before a barrier they all pass, so that
+        // they all read the same value after it; they then give up on their
+        // own bounded waits for the loads that never come.
+        if (lane == 0) {
+            int c = 0;
+            for (; c < n_chunks; ++c) {
+                const int sq = c % CF::NQK, sv = c % CF::NVS, sz = c % CF::NZS;
+                if (c >= CF::NVS && !ptx::mbar_wait(&bars.empty_v[sv],
+                                                    (uint32_t)((c / CF::NVS - 1) & 1), abort_flag))
+                    break;
+                issue_v(c);
+                if (c >= CF::NZS && !ptx::mbar_wait(&bars.empty_z[sz],
+                                                    (uint32_t)((c / CF::NZS - 1) & 1), abort_flag))
+                    break;
+                issue_z(c);
+                if (c >= CF::NQK && !ptx::mbar_wait(&bars.empty_qk[sq],
+                                                    (uint32_t)((c / CF::NQK - 1) & 1), abort_flag))
+                    break;
+                issue_qk(c);
+            }
+            if (c < n_chunks && !*abort_flag)
+                atomicExch(status, GDN_ERR_TIMEOUT);   // gave up with loads still to issue
+            drain();
         }
-    };
-    auto scan_gates = [&](float *set) {               // gate threads only
-        float sacc = gnext;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, sacc, o);
-            if (lane >= o) sacc += y;
-        }
-        set[gr_] = sacc;
-        set[64 + gr_] = bnext;
-        ptx::named_sync(3, 64);
-        if (gr_ >= 32) set[gr_] = sacc + set[31];
-        ptx::named_sync(3, 64);
-        set[128 + gr_] = fast_exp(set[gr_]);
-        set[192 + gr_] = fast_exp(set[63] - set[gr_]);
-    };
-    if (gate_thread && n_chunks > 0) {
-        load_gates(0);
-        scan_gates(gsets);
-        if (n_chunks > 1) load_gates(1);
-    }
-    __syncthreads();
-
-    for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
-        const int t0 = c * C;
-        const int n = min(C, T - t0);
-        const bool more = c + 1 < n_chunks;
-        float *sG = gsets + (c & 1) * 256;            // this chunk's gate set
-        float *sBeta = sG + 64;
-        float *sGam = sG + 128;
-        float *sEnd = sG + 192;
-        (void)sG;
-
-        // ---------------- 1. wait for the chunk's tiles (issued earlier)
-        if (!ptx::mbar_wait(&bars.tma, (uint32_t)(c & 1), abort_flag)) fail();
-        else if (tid == 0) armed = -1;
-        __syncthreads();
-        if (*abort_flag) break;
-
-        // ---------------- 4. MMA: [K;Q] S^T  (M=128, N=BV, K=D; S as hi + lo)
-        if (tid == 0) {
+        __syncwarp();
+    } else {
+        uint32_t mma_phase = 0;
+        // wait for the next MMA commit (warps 0-7)
+        auto wait_mma = [&]() {
+            if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
+            mma_phase ^= 1;
             ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
-            const uint32_t bS[2] = {ptx::smem_u32(sShi), ptx::smem_u32(sSlo)};
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t da =
-                        ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    const uint64_t db = ptx::smem_desc(bS[part] + kk * 2048, 8192, 1024);
-                    ptx::mma_bf16(tmem + CF::COL_X, da, db, idesc, part > 0 || kk > 0);
-                }
-            }
-            ptx::mma_commit(&bars.mma);
-        }
-        if constexpr (NORM) {                         // 1/|k|, 1/|q| of the chunk's tokens
-            if (tid >= 128 && tid < 192) {
-                float kk, qq;
-                qk_row_sumsq<D / 64>(sQK, tid - 128, kk, qq);
-                sNk[tid - 128] = inv_norm(kk);
-                sNq[tid - 128] = inv_norm(qq);
-            }
-            __syncthreads();
-        }
-        wait_mma();
+        };
+        const size_t tok_stride = (size_t)H * D;
 
-        // ---------------- 5. R = beta V - beta gamma K S^T  (lanes 0-63)
-        float xq[HALF];   // Q S^T for this thread's output row (lanes 64-127)
-        {
-            float x[HALF];
-#pragma unroll
-            for (int j = 0; j < HALF; j += 16)
-                ptx::tmem_ld16(tmem + lane_off + CF::COL_X + wg * HALF + j,
-                               *reinterpret_cast<float(*)[16]>(x + j));
-            ptx::tmem_ld_wait();
-            if (row < 64) {
-                const int r = row;
-                const float br = sBeta[r], bg = br * (NORM ? sGam[r] * sNk[r] : sGam[r]);
-#pragma unroll
-                for (int j = 0; j < HALF; j += 16) {
-                    float rr[16];
-#pragma unroll
-                    for (int e8 = 0; e8 < 16; e8 += 8) {
-                        // 8 values of row r: one 16-byte chunk of the swizzled V tile
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            sV + ptx::sw128_offset(r, wg * HALF + j + e8));
-                        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float vv = __uint_as_float(
-                                (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
-                            rr[e8 + e] = fmaf(br, vv, -bg * x[j + e8 + e]);
-                        }
-                    }
-                    store_split16(sRhi, sRlo, r, wg * HALF + j, rr);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) xq[j] = x[j];
-                if (gate_thread && more) {            // the next chunk's gates
-                    scan_gates(gsets + ((c + 1) & 1) * 256);
-                    if (c + 2 < n_chunks) load_gates(c + 2);
-                }
+        // Gates: warps 2 and 3 (threads 64-127, TMEM lanes 64-127, idle while
+        // the other warps build R) scan the next chunk's g into the other of
+        // two gate sets during step 5, from g and beta they loaded one chunk
+        // earlier; the set of chunk 0 is built here.  Set layout: G (in-chunk
+        // running sum of g, each clamped at -30: exp(-30) ~ 1e-13, a reset
+        // stays a reset), beta, gamma = exp(G), end-decay = exp(G_63 - G).
+        const bool gate_thread = tid >= 64 && tid < 128;
+        const int gr_ = tid - 64;                      // token of the chunk (gate threads)
+        float gnext = 0.f, bnext = 0.f;
+        // g, beta of chunk cc into gnext / bnext.  Nothing reads them until
+        // the scan a chunk later, so the loads stay in flight meanwhile.
+        auto load_gates = [&](int cc) {
+            gnext = 0.f;
+            bnext = 0.f;
+            if (cc * C + gr_ < T) {
+                const size_t gi = ((size_t)b * T + cc * C + gr_) * H + h;
+                gnext = g[gi];
+                bnext = beta[gi];
             }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        if (tid == 0 && more) {                       // V of this chunk has been read
-            load_v(c + 1);
-            armed = c + 1;
-            issued = 1;
-        }
-
-        // ---------------- 6. MMA: Z R  (M=128, N=BV, K=64; hi*hi + hi*lo + lo*hi)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
-            const uint32_t aZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZhi), ptx::smem_u32(sZlo)};
-            const uint32_t bR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo), ptx::smem_u32(sRhi)};
+        };
+        auto scan_gates = [&](float *set) {           // gate threads only
+            float sacc = fmaxf(gnext, -30.f);
 #pragma unroll
-            for (int part = 0; part < 3; ++part) {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t da = ptx::smem_desc(aZ[part] + kk * 32, 16, 1024);
-                    const uint64_t db = ptx::smem_desc(bR[part] + kk * 2048, 8192, 1024);
-                    ptx::mma_bf16(tmem + CF::COL_Y, da, db, idesc, part > 0 || kk > 0);
-                }
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, sacc, o);
+                if (lane >= o) sacc += y;
             }
-            ptx::mma_commit(&bars.mma);
+            set[gr_] = sacc;
+            set[64 + gr_] = bnext;
+            ptx::named_sync(3, 64);
+            if (gr_ >= 32) set[gr_] = sacc + set[31];
+            ptx::named_sync(3, 64);
+            set[128 + gr_] = fast_exp(set[gr_]);
+            set[192 + gr_] = fast_exp(set[63] - set[gr_]);
+        };
+        // Without warp 8, one thread per tile issues its loads: [K;Q] thread
+        // 0, V thread 32, Z thread 64; each loads the next chunk's tile as
+        // soon as this chunk is done with it.
+        if (!PW && n_chunks > 0) {                   // chunk 0's tiles
+            if (tid == 0) issue_qk(0);
+            else if (tid == 32) issue_v(0);
+            else if (tid == 64) issue_z(0);
         }
-        wait_mma();
-        if (tid == 0 && more) {                       // the Z R product has read Z
-            load_z(c + 1);
-            issued |= 2;
+        if (gate_thread && n_chunks > 0) {
+            load_gates(0);
+            scan_gates(gsets);
+            if (n_chunks > 1) load_gates(1);
         }
+        ptx::named_sync(1, NT);
 
-        // ---------------- 7. O (lanes 64-127) and U~ hi / lo (lanes 0-63)
-        {
-            float y[HALF];
-#pragma unroll
-            for (int j = 0; j < HALF; j += 16)
-                ptx::tmem_ld16(tmem + lane_off + CF::COL_Y + wg * HALF + j,
-                               *reinterpret_cast<float(*)[16]>(y + j));
-            ptx::tmem_ld_wait();
-            if (row >= 64) {
-                const int r = row - 64;
-                if (r < n) {
-                    const float gr = NORM ? sGam[r] * sNq[r] : sGam[r];
-                    float *orow = out + ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D + v0 +
-                                  wg * HALF;
-#pragma unroll
-                    for (int j = 0; j < HALF; j += 4) {
-                        float4 o4;
-                        o4.x = fmaf(gr, xq[j + 0], y[j + 0]) * scale;
-                        o4.y = fmaf(gr, xq[j + 1], y[j + 1]) * scale;
-                        o4.z = fmaf(gr, xq[j + 2], y[j + 2]) * scale;
-                        o4.w = fmaf(gr, xq[j + 3], y[j + 3]) * scale;
-                        *reinterpret_cast<float4 *>(orow + j) = o4;
-                    }
-                }
-            } else {
-                const int r = row;
-                const float er = NORM ? sEnd[r] * sNk[r] : sEnd[r];
-#pragma unroll
-                for (int j = 0; j < HALF; j += 16) {
-                    float u[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) u[e] = er * y[j + e];
-                    store_split16(sRhi, sRlo, r, wg * HALF + j, u);   // R no longer needed
-                }
+        for (int c = 0; c < n_chunks && !*abort_flag; ++c) {
+            const int t0 = c * C;
+            const int n = min(C, T - t0);
+            const bool more = c + 1 < n_chunks;
+            const int sq = c % CF::NQK, sv = c % CF::NVS, sz = c % CF::NZS;
+            const uint8_t *sQK = sQK0 + sq * CF::QK_BYTES;
+            const uint8_t *sV = sV0 + sv * CF::V_BYTES;
+            const uint8_t *sZhi = sZ0 + sz * Z_BYTES, *sZlo = sZhi + 16384;
+            const uint32_t aQK = ptx::smem_u32(sQK);
+            float *sG = gsets + (c & 1) * 256;        // this chunk's gate set
+            float *sBeta = sG + 64;
+            float *sGam = sG + 128;
+            float *sEnd = sG + 192;
+
+            // ---------------- 1. the chunk's tiles: [K;Q] seen by the threads
+            // that read it (thread 0 issues the products, threads 128-191 take
+            // the norms), V and Z by thread 64 for everyone, so that thread 0
+            // issues the Z R product without a wait of its own.  A wait that
+            // gives up sets the abort flag before one of the chunk's barriers,
+            // and the loop stops at its next test, all threads together.
+            if (tid == 0 || (NORM && tid >= 128 && tid < 192)) {
+                if (!ptx::mbar_wait(&bars.full_qk[sq], (uint32_t)((c / CF::NQK) & 1), abort_flag))
+                    fail();
+            } else if (tid == 64) {
+                if (!ptx::mbar_wait(&bars.full_v[sv], (uint32_t)((c / CF::NVS) & 1), abort_flag) ||
+                    !ptx::mbar_wait(&bars.full_z[sz], (uint32_t)((c / CF::NZS) & 1), abort_flag))
+                    fail();
             }
-        }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
+            ptx::named_sync(1, NT);
 
-        // ---------------- 8. MMA: K^T U~  (per 128-key tile: M=128, N=BV, K=64)
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, true, true);
-            const uint32_t bU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
-#pragma unroll
-            for (int kt = 0; kt < KT; ++kt) {
+            // ---------------- 4. MMA: [K;Q] S^T  (M=128, N=BV, K=D; S as hi + lo)
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
+                const uint32_t bS[2] = {ptx::smem_u32(sShi), ptx::smem_u32(sSlo)};
 #pragma unroll
                 for (int part = 0; part < 2; ++part) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
+                    for (int kk = 0; kk < D / 16; ++kk) {
                         const uint64_t da =
-                            ptx::smem_desc(aQK + kt * 2 * 16384 + kk * 2048, 16384, 1024);
-                        const uint64_t db = ptx::smem_desc(bU[part] + kk * 2048, 8192, 1024);
-                        ptx::mma_bf16(tmem + CF::COL_DS + kt * BV, da, db, idesc,
-                                      part > 0 || kk > 0);
+                            ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t db =
+                            ptx::smem_desc(bS[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
+                        ptx::mma_bf16(tmem + CF::COL_X, da, db, idesc, part > 0 || kk > 0);
                     }
                 }
+                ptx::mma_commit(&bars.mma);
             }
-            ptx::mma_commit(&bars.mma);
-        }
-        wait_mma();
-        if (tid == 0 && more) {                       // both products have read [K;Q]
-            load_qk(c + 1);
-            issued |= 4;
-        }
+            if constexpr (NORM) {                     // 1/|k|, 1/|q| of the chunk's tokens
+                if (tid >= 128 && tid < 192) {
+                    float kk, qq;
+                    qk_row_sumsq<D / 64>(sQK, tid - 128, kk, qq);
+                    sNk[tid - 128] = inv_norm(kk);
+                    sNq[tid - 128] = inv_norm(qq);
+                }
+                ptx::named_sync(1, NT);
+            }
+            wait_mma();
 
-        // ---------------- 9. S = gamma_C S + dS^T; S hi / lo for the next chunk
-        {
-            const float gC = sGam[63];
-#pragma unroll
-            for (int kt = 0; kt < KT; ++kt) {
-                float ds[HALF];
+            // ---------------- 5. R = beta V - beta gamma K S^T  (lanes 0-63)
+            float xq[HALF];   // Q S^T for this thread's output row (lanes 64-127)
+            {
+                float x[HALF];
 #pragma unroll
                 for (int j = 0; j < HALF; j += 16)
-                    ptx::tmem_ld16(tmem + lane_off + CF::COL_DS + kt * BV + wg * HALF + j,
-                                   *reinterpret_cast<float(*)[16]>(ds + j));
+                    ptx::tmem_ld16(tmem + lane_off + CF::COL_X + wg * HALF + j,
+                                   *reinterpret_cast<float(*)[16]>(x + j));
                 ptx::tmem_ld_wait();
-                const int key = kt * 128 + row;
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) S[kt][j] = fmaf(gC, S[kt][j], ds[j]);
-                if (key < D) {
+                if (row < 64) {
+                    const int r = row;
+                    const float br = sBeta[r], bg = br * (NORM ? sGam[r] * sNk[r] : sGam[r]);
 #pragma unroll
                     for (int j = 0; j < HALF; j += 16) {
-                        float x[16];
+                        float rr[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
-                        store_split16(sShi, sSlo, key, wg * HALF + j, x);
+                        for (int e8 = 0; e8 < 16; e8 += 8) {
+                            // 8 values of row r: one 16-byte chunk of the swizzled V tile
+                            const uint4 raw = *reinterpret_cast<const uint4 *>(
+                                sV + ptx::swz_offset<ROWB>(r, wg * HALF + j + e8));
+                            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float vv = __uint_as_float(
+                                    (e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+                                rr[e8 + e] = fmaf(br, vv, -bg * x[j + e8 + e]);
+                            }
+                        }
+                        store_split16<ROWB>(sRhi, sRlo, r, wg * HALF + j, rr);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < HALF; ++j) xq[j] = x[j];
+                    if (gate_thread && more) {        // the next chunk's gates
+                        scan_gates(gsets + ((c + 1) & 1) * 256);
+                        if (c + 2 < n_chunks) load_gates(c + 2);
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(1, NT);
+            if (tid == 32) {                          // V of this chunk has been read
+                if constexpr (PW) ptx::mbar_arrive(&bars.empty_v[sv]);
+                else if (more) issue_v(c + 1);
+            }
+
+            // ---------------- 6. MMA: Z R  (M=128, N=BV, K=64; hi*hi + hi*lo + lo*hi)
+            if (tid == 0) {
+                {
+                    ptx::tc_fence_after();
+                    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
+                    const uint32_t aZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZhi),
+                                            ptx::smem_u32(sZlo)};
+                    const uint32_t bR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo),
+                                            ptx::smem_u32(sRhi)};
+#pragma unroll
+                    for (int part = 0; part < 3; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t da = ptx::smem_desc(aZ[part] + kk * 32, 16, 1024);
+                            const uint64_t db =
+                                ptx::smem_desc(bR[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
+                            ptx::mma_bf16(tmem + CF::COL_Y, da, db, idesc, part > 0 || kk > 0);
+                        }
+                    }
+                    ptx::mma_commit(&bars.mma);
+                    if constexpr (PW) ptx::mma_commit(&bars.empty_z[sz]);   // Z free once it is done
+                }
+            }
+            wait_mma();
+            if (!PW && tid == 64 && more) issue_z(c + 1); // the Z R product has read Z
+
+            // ---------------- 7. O (lanes 64-127) and U~ hi / lo (lanes 0-63)
+            {
+                float y[HALF];
+#pragma unroll
+                for (int j = 0; j < HALF; j += 16)
+                    ptx::tmem_ld16(tmem + lane_off + CF::COL_Y + wg * HALF + j,
+                                   *reinterpret_cast<float(*)[16]>(y + j));
+                ptx::tmem_ld_wait();
+                if (row >= 64) {
+                    const int r = row - 64;
+                    if (r < n) {
+                        const float gr = NORM ? sGam[r] * sNq[r] : sGam[r];
+                        float *orow = out + ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D +
+                                      v0 + wg * HALF;
+#pragma unroll
+                        for (int j = 0; j < HALF; j += 4) {
+                            float4 o4;
+                            o4.x = fmaf(gr, xq[j + 0], y[j + 0]) * scale;
+                            o4.y = fmaf(gr, xq[j + 1], y[j + 1]) * scale;
+                            o4.z = fmaf(gr, xq[j + 2], y[j + 2]) * scale;
+                            o4.w = fmaf(gr, xq[j + 3], y[j + 3]) * scale;
+                            *reinterpret_cast<float4 *>(orow + j) = o4;
+                        }
+                    }
+                } else {
+                    const int r = row;
+                    const float er = NORM ? sEnd[r] * sNk[r] : sEnd[r];
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 16) {
+                        float u[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) u[e] = er * y[j + e];
+                        store_split16<ROWB>(sRhi, sRlo, r, wg * HALF + j, u);   // R no longer needed
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(1, NT);
+
+            // ---------------- 8. MMA: K^T U~  (per 128-key tile: M=128, N=BV, K=64)
+            if (tid == 0) {
+                ptx::tc_fence_after();
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, true, true);
+                const uint32_t bU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+#pragma unroll
+                for (int kt = 0; kt < KT; ++kt) {
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t da =
+                                ptx::smem_desc(aQK + kt * 2 * 16384 + kk * 2048, 16384, 1024);
+                            const uint64_t db =
+                                ptx::smem_desc(bU[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
+                            ptx::mma_bf16(tmem + CF::COL_DS + kt * BV, da, db, idesc,
+                                          part > 0 || kk > 0);
+                        }
+                    }
+                }
+                ptx::mma_commit(&bars.mma);
+                if constexpr (PW) ptx::mma_commit(&bars.empty_qk[sq]);   // both products read [K;Q]
+            }
+            wait_mma();
+            if (!PW && tid == 0 && more) issue_qk(c + 1); // both products have read [K;Q]
+
+            // ---------------- 9. S = gamma_C S + dS^T; S hi / lo for the next chunk
+            {
+                const float gC = sGam[63];
+#pragma unroll
+                for (int kt = 0; kt < KT; ++kt) {
+                    float ds[HALF];
+#pragma unroll
+                    for (int j = 0; j < HALF; j += 16)
+                        ptx::tmem_ld16(tmem + lane_off + CF::COL_DS + kt * BV + wg * HALF + j,
+                                       *reinterpret_cast<float(*)[16]>(ds + j));
+                    ptx::tmem_ld_wait();
+                    const int key = kt * 128 + row;
+#pragma unroll
+                    for (int j = 0; j < HALF; ++j) S[kt][j] = fmaf(gC, S[kt][j], ds[j]);
+                    if (key < D) {
+#pragma unroll
+                        for (int j = 0; j < HALF; j += 16) {
+                            float x[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) x[e] = S[kt][j + e];
+                            store_split16<ROWB>(sShi, sSlo, key, wg * HALF + j, x);
+                        }
+                    }
+                }
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::tc_fence_before();
+            ptx::named_sync(1, NT);
+            ptx::tc_fence_after();
+        }
+
+        if (!PW && (tid == 0 || tid == 32 || tid == 64)) drain();
+
+        // ---- final state block
+        if (!*abort_flag) {
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt) {
+                const int key = kt * 128 + row;
+                if (key < D) {
+#pragma unroll
+                    for (int j = 0; j < HALF; ++j) {
+                        const int v = v0 + wg * HALF + j;
+                        state_out[st_base + (size_t)v * D + key] = S[kt][j];
                     }
                 }
             }
         }
-        ptx::fence_proxy_async_smem();
-        ptx::tc_fence_before();
-        __syncthreads();
-        ptx::tc_fence_after();
-    }
-
-    // ---- final state block
-    if (!*abort_flag) {
-#pragma unroll
-        for (int kt = 0; kt < KT; ++kt) {
-            const int key = kt * 128 + row;
-            if (key < D) {
-#pragma unroll
-                for (int j = 0; j < HALF; ++j) {
-                    const int v = v0 + wg * HALF + j;
-                    state_out[st_base + (size_t)v * D + key] = S[kt][j];
-                }
-            }
-        }
-    }
-    // after an abort: let the copies still addressed to this CTA's shared
-    // memory land (issuing any of the armed chunk's loads not yet issued, so
-    // that its byte count can complete), within a bounded wait
-    if (tid == 0 && armed >= 0) {
-        if (!(issued & 2)) load_z(armed);
-        if (!(issued & 4)) load_qk(armed);
-        const volatile int never = 0;
-        ptx::mbar_wait(&bars.tma, (uint32_t)(armed & 1), &never, 1000000000LL);
     }
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) ptx::tmem_dealloc(tmem, CF::TMEM_COLS);
 }
-
 // ---------------------------------------------------------------------------
 // head_dim 64 and 128: one CTA per (sequence, head) owns every value row, so
 // the chunk-local UT transform is built once per chunk and head.  The state
@@ -1684,9 +1809,9 @@ EncodeTiledFn encode_fn() {
 }
 
 // 4-D map over a (B, T, H, d) bf16 tensor; box = {box0 elements of d, 1 head,
-// 64 tokens, 1 sequence}.  Tokens past T read as zeros.
-bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, int box0,
-              bool swizzle128) {
+// 64 tokens, 1 sequence}, box0 * 2 bytes = the swizzle span (128 B: box0 64,
+// 64 B: box0 32).  Tokens past T read as zeros.
+bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, int box0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
@@ -1696,7 +1821,7 @@ bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, in
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               box0 == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
 }
@@ -1719,27 +1844,27 @@ bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
 }
 
 // head_dim 256, and head_dim 128 with few pairs: the chunk transform for
-// every chunk into the workspace, then the state walk (D / 64 CTAs per head,
-// 64 value rows each) reading it.
-template <int D, bool NORM>
+// every chunk into the workspace, then the state walk (D / BV CTAs per head,
+// BV value rows each) reading it.
+template <int D, int BV, bool NORM>
 cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
-    using CF = Cfg<D>;
+    using CF = Cfg<D, BV>;
     using ZC = ZCfg<D>;
     const int n_chunks = (p.T + C - 1) / C;
     const long long n_tasks = (long long)p.B * p.H * n_chunks;
     if (!workspace || ws_bytes < (size_t)n_tasks * Z_BYTES || n_tasks > INT_MAX)
         return cudaErrorInvalidValue;
     CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
-        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV, true))
+    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64) ||
+        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV))
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
         cudaError_t e = cudaFuncSetAttribute(chunk_z_kernel<D, NORM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunked_kernel<D, NORM>,
+            e = cudaFuncSetAttribute(chunked_kernel<D, BV, NORM>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
         return e;
     });
@@ -1750,7 +1875,7 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
         mq, mk, p.g, p.beta, zws, p.T, p.H, p.Hk, n_chunks, (int)n_tasks, p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunked_kernel<D, NORM><<<(unsigned)(p.B * p.H * CF::NVB), NT, CF::SMEM, stream>>>(
+    chunked_kernel<D, BV, NORM><<<(unsigned)(p.B * p.H * CF::NVB), CF::NTH, CF::SMEM, stream>>>(
         mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
         p.status);
     return cudaGetLastError();
@@ -1759,9 +1884,9 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
 template <int D, bool NORM>
 cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     CUtensorMap mq, mk, mv, mo;
-    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64, true) ||
-        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64, true) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, D, 64, true) ||
+    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64) ||
+        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64) ||
+        !make_map(&mv, p.v, p.B, p.T, p.H, D, 64) ||
         !make_map_out(&mo, p.out, p.B, p.T, p.H, D))
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
@@ -1823,15 +1948,26 @@ size_t chunked_workspace_bytes(int B, int T, int H, int d, int) {
     return (size_t)B * (size_t)H * n_chunks * (size_t)Z_BYTES;
 }
 
+// The two-kernel state walk takes value blocks of 32 rows where D / 32 CTAs
+// per (sequence, head) still fit every pair into one wave on this device's
+// SMs: a small problem then runs twice the CTAs, each with half the work per
+// chunk on the chain of dependent steps.  Otherwise blocks of 64 rows.
+template <int D, bool NORM>
+cudaError_t launch_walk(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+    if ((long long)p.B * p.H * (D / 32) <= current_sm_count())
+        return launch_d<D, 32, NORM>(p, workspace, ws_bytes, stream);
+    return launch_d<D, 64, NORM>(p, workspace, ws_bytes, stream);
+}
+
 template <bool NORM>
 cudaError_t launch_chunked_t(const Problem &p, void *workspace, size_t ws_bytes,
                              cudaStream_t stream) {
     switch (p.d) {
         case 64: return launch_ws<64, NORM>(p, stream);
         case 128:
-            return d128_split(p.B, p.H) ? launch_d<128, NORM>(p, workspace, ws_bytes, stream)
+            return d128_split(p.B, p.H) ? launch_walk<128, NORM>(p, workspace, ws_bytes, stream)
                                         : launch_ws<128, NORM>(p, stream);
-        case 256: return launch_d<256, NORM>(p, workspace, ws_bytes, stream);
+        case 256: return launch_walk<256, NORM>(p, workspace, ws_bytes, stream);
         default: return cudaErrorInvalidValue;
     }
 }

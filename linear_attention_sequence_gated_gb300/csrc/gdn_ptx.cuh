@@ -142,7 +142,10 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // 8-row groups); an MN-major operand stores 64 consecutive M/N elements per
 // 128-byte row, one row per K index, 8 K rows per atom (SBO = distance
 // between 8-K-row groups, LBO = distance between 64-element M/N atoms).
+// With 64-byte swizzling the same holds for rows of 32 bf16 (64 B), 8-row
+// atoms of 512 B.
 constexpr uint64_t kSwizzle128 = 2;
+constexpr uint64_t kSwizzle64 = 4;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
                                               uint64_t swizzle = kSwizzle128) {
@@ -160,6 +163,22 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __device__ __forceinline__ uint32_t sw128_offset(int row, int col_bf16) {
     const int chunk = col_bf16 >> 3;  // 16-byte chunk within the row
     return (uint32_t)(row * 128 + (((chunk ^ (row & 7)) << 4) | ((col_bf16 & 7) << 1)));
+}
+
+// Byte offset of element (row, col) of a 64-byte-swizzled tile whose rows
+// are 32 bf16 wide (64 B) and whose 8-row atoms are 512-byte aligned: the
+// 16-byte chunk index (address bits 4-5) is XORed with address bits 7-8.
+__device__ __forceinline__ uint32_t sw64_offset(int row, int col_bf16) {
+    const int chunk = col_bf16 >> 3;  // 16-byte chunk within the row
+    return (uint32_t)(row * 64 + (((chunk ^ ((row >> 1) & 3)) << 4) | ((col_bf16 & 7) << 1)));
+}
+
+// The swizzled offset for a tile with ROWB-byte rows (128 or 64).
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz_offset(int row, int col_bf16) {
+    static_assert(ROWB == 128 || ROWB == 64, "128- or 64-byte rows");
+    if constexpr (ROWB == 128) return sw128_offset(row, col_bf16);
+    else return sw64_offset(row, col_bf16);
 }
 
 // tcgen05 instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
@@ -317,13 +336,15 @@ __device__ __forceinline__ void split_pair(float a, float b, uint32_t &hi, uint3
 }
 
 // Split 8 consecutive values and store them as one 16-byte chunk into each
-// of two 128-byte-swizzled tiles at (row, col0 .. col0 + 7), col0 % 8 == 0.
+// of two swizzled tiles (rows of ROWB bytes) at (row, col0 .. col0 + 7),
+// col0 % 8 == 0.
+template <int ROWB = 128>
 __device__ __forceinline__ void store_split8(uint8_t *hi_tile, uint8_t *lo_tile, int row, int col0,
                                              const float *x) {
     uint32_t h[4], l[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) split_pair(x[2 * e], x[2 * e + 1], h[e], l[e]);
-    const uint32_t off = sw128_offset(row, col0);
+    const uint32_t off = swz_offset<ROWB>(row, col0);
     *reinterpret_cast<uint4 *>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4 *>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }

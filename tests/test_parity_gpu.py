@@ -263,8 +263,12 @@ def test_extreme_gates_and_betas():
 # at least 80 (sequence, head) pairs run the one-kernel path; head_dim 128
 # with fewer pairs and head_dim 256 run the chunk-transform pass plus the
 # state walk on value-row blocks.
+# Every chunked kernel and state-walk width on a 152-SM GB300: the two-kernel
+# walk takes 32-row value blocks while (pairs x head_dim / 32) <= 152, else
+# 64-row blocks; head_dim 128 runs the two-kernel path below 80 pairs.
 CHUNKED_KERNELS = [("d64", 2, 4, 64), ("d128_one_kernel", 2, 48, 128),
-                   ("d128_two_kernel", 2, 4, 128), ("d256", 2, 4, 256)]
+                   ("d128_two_kernel_bv32", 2, 4, 128), ("d128_two_kernel_bv64", 2, 24, 128),
+                   ("d256_bv32", 2, 4, 256), ("d256_bv64", 2, 12, 256)]
 
 
 def plant_extremes(inp):
