@@ -1394,6 +1394,24 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
         for (int s = 0; s < NSLAB; ++s)
             ptx::tma_load_4d(sV + s * 8192, &tm_v, &sh.v_full, s * 64, h, c * C, b);
     };
+    // The same loads split over one thread in each of warps 0-3 (the state
+    // stream issues them mid-chunk, where a single thread would hold up the
+    // products it also issues): box i of [K;Q] (K slab 0, Q slab 0, K slab
+    // 1, Q slab 1) and of V by thread 32 i.  Thread 0 arms the barrier for
+    // the whole tile; a box that lands before that leaves the transaction
+    // count negative, which keeps the phase open until the rest has landed.
+    auto issue_qk_part = [&](int c, int i) {
+        const int st = c & 1;
+        uint8_t *qk = sm + OFF_QK + st * 32768;
+        if (i == 0) ptx::mbar_arrive_expect_tx(&sh.qk_full[st], NSLAB * 2 * 8192);
+        if (i < 2 * NSLAB)
+            ptx::tma_load_4d(qk + (i >> 1) * 16384 + (i & 1) * 8192, (i & 1) ? &tm_q : &tm_k,
+                             &sh.qk_full[st], (i >> 1) * 64, h % Hk, c * C, b);
+    };
+    auto issue_v_part = [&](int c, int i) {
+        if (i == 0) ptx::mbar_arrive_expect_tx(&sh.v_full, NSLAB * 8192);
+        if (i < NSLAB) ptx::tma_load_4d(sV + i * 8192, &tm_v, &sh.v_full, i * 64, h, c * C, b);
+    };
     if (tid == 0) {
         issue_qk(0);
         if (n_chunks > 1) issue_qk(1);
@@ -1598,7 +1616,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             }
             ptx::fence_proxy_async_smem();
             ptx::named_sync(BAR_S, NS);
-            if (t == 0 && !*abort_flag) {
+            if (t == 64) {                             // thread 64 owns the O stores
                 ptx::tma_store_4d(&tm_o, stage, 0, h, t0, b);
                 ptx::bulk_commit_group();
             }
@@ -1620,7 +1638,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             wait(&sh.qk_full[st], (uint32_t)((c >> 1) & 1));
 
             // X^T = S [K;Q]^T  (A = S hi / lo from TMEM, M = 128, N = 128, K = 128)
-            if (t == 0 && !*abort_flag) {
+            if (t == 0) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
@@ -1669,11 +1687,11 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
-            if (t == 0 && !last && !*abort_flag) issue_v(c + 1);   // V of this chunk consumed
+            if (!last && (t & 31) == 0 && t < 32 * NSLAB) issue_v_part(c + 1, t >> 5);   // V consumed
 
             // [U^T | (P U)^T] = R^T Z^T with Z = [T; P T]: one N = 128 product
             wait(&sh.z_ready[st], (uint32_t)((c >> 1) & 1));
-            if (t == 0 && !*abort_flag) {
+            if (t == 0) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false, false);
                 const uint32_t aR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
@@ -1716,7 +1734,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::named_sync(BAR_S, NS);
 
             // S += U~^T K  (M = 128 values, N = D keys, K = 64 tokens)
-            if (t == 0 && !*abort_flag) {
+            if (t == 0) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, D, false, true);
                 const uint32_t aU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
@@ -1743,7 +1761,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 o_epilogue(sRhi, sGamQ, t0);  // the S product has finished reading U~
             }
             // this stage is free: bring chunk c + 2 into it
-            if (t == 0 && c + 2 < n_chunks && !*abort_flag) issue_qk(c + 2);
+            if (c + 2 < n_chunks && (t & 31) == 0 && t < 64 * NSLAB) issue_qk_part(c + 2, t >> 5);
 
             // S: split for the next chunk's X^T and pre-scale by its gamma_C,
             // or write the final state
@@ -1770,14 +1788,24 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                 }
             }
             if (!last && vrow) ptx::tmem_st_wait();
-            if (t == 0) {
+            if (t == 64) {
                 ptx::bulk_wait_read_all();               // the O tile has left its buffer
                 if constexpr (kOInZ) ptx::mbar_arrive(&sh.z_free[st]);
             }
             ptx::tc_fence_before();
             ptx::named_sync(BAR_S, NS);
         }
-        if (t == 0) ptx::bulk_wait_all();
+        if (t == 64) ptx::bulk_wait_all();
+        // every load addressed to this CTA's shared memory has landed before
+        // it exits (on the normal path these phases completed long ago; after
+        // a wait gave up they may not have)
+        if (t == 0) {
+            const volatile int never = 0;
+            for (int c = (n_chunks > 2 ? n_chunks - 2 : 0); c < n_chunks; ++c)
+                ptx::mbar_wait(&sh.qk_full[c & 1], (uint32_t)((c >> 1) & 1), &never, 1000000000LL);
+            if (n_chunks > 0)
+                ptx::mbar_wait(&sh.v_full, (uint32_t)((n_chunks - 1) & 1), &never, 1000000000LL);
+        }
     }
 
     ptx::tc_fence_before();
