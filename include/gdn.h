@@ -34,12 +34,14 @@
  *     row-major in the torch order above.  q, k, v, out, state_in and
  *     state_out must be 16-byte aligned; g and beta 4-byte aligned.
  *   - g and beta are float32.  state_in / state_out are float32 [value][key].
- *     out is float32 (n_seqs, n_tokens, n_heads, head_dim), already scaled.
+ *     out is float32 (n_seqs, n_tokens, n_heads, head_dim), already scaled
+ *     (bfloat16 with the GDN_OPT_OUT_BF16 option of gdn_forward_ex).
  *   - state_in may be NULL: the initial state is then zeros.
  *   - state_out == state_in (the same pointer) updates the state in place.
  *     Any other overlap between an output (out, state_out) and any other
  *     buffer is rejected with GDN_ERR_ALIAS.
- *   - q and k are used as given: the op does not L2-normalise them.
+ *   - q and k are used as given: the op does not L2-normalise them (the
+ *     GDN_OPT_L2NORM_QK option of gdn_forward_ex does).
  *   - Sizes: n_seqs, n_heads >= 0, n_tokens >= 0.  A call with n_seqs == 0 or
  *     n_heads == 0 does nothing.  n_tokens == 0 copies state_in (or zeros)
  *     into state_out and writes no output.
@@ -101,6 +103,17 @@ enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 
  *   so raw bf16 q and k still enter the tensor-core products exactly.
  */
 #define GDN_OPT_L2NORM_QK 0x100
+
+/*
+ * GDN_OPT_OUT_BF16: `out` is bfloat16 (raw 16-bit words, __nv_bfloat16
+ *   layout), same shape, still scaled by 1/sqrt(head_dim).  Each element is
+ *   the float32 value the call writes without this option, rounded to
+ *   nearest even; the recurrence and the state stay float32.  The call then
+ *   needs half the output bytes (its size, alignment and overlap checks count
+ *   2-byte elements).  The extra error is that one rounding: at most 2^-9 of
+ *   each element's magnitude.
+ */
+#define GDN_OPT_OUT_BF16 0x200
 
 /*
  * gdn_forward -- the op with float32 q, k, v.

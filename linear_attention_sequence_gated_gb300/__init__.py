@@ -31,6 +31,7 @@ ERR_ARG, ERR_HEADDIM, ERR_ALIGN, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT, ERR_WORKSPACE
 DTYPE_F32, DTYPE_BF16, DTYPE_F16 = 0, 1, 2
 PATHS = {"auto": 0, "recurrent": 1, "chunked": 2}
 OPT_L2NORM_QK = 0x100
+OPT_OUT_BF16 = 0x200
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ["gdn_forward", "gdn_forward_bf16", "gdn_forward_ex", "gdn_workspace_bytes",
@@ -127,7 +128,7 @@ def _ptr(t):
 
 
 def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str = "auto",
-            workspace=None, stream=None, l2norm_qk: bool = False):
+            workspace=None, stream=None, l2norm_qk: bool = False, out_dtype=None):
     """Run the gated delta rule over every token of every sequence.
 
     Returns (out, final_state).  ``state_out`` may be ``state`` itself for
@@ -135,7 +136,10 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
     least ``workspace_bytes(...)`` bytes; without it the library allocates
     stream-ordered scratch when the chosen path needs any.  ``l2norm_qk``
     divides q and k by their norm per (sequence, token, head) inside the op
-    (the library's GDN_OPT_L2NORM_QK)."""
+    (the library's GDN_OPT_L2NORM_QK).  ``out_dtype`` torch.bfloat16 writes
+    the output as bf16, each value the fp32 one rounded to nearest even
+    (GDN_OPT_OUT_BF16); a given ``out`` must have that dtype.  The default is
+    fp32, or the dtype of a given ``out``."""
     import torch
     L = lib()
     if q.dtype == torch.bfloat16:
@@ -161,8 +165,12 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
         if tuple(state.shape) != (B, H, d, d) or state.dtype != torch.float32:
             raise ValueError("state must be (n_seqs, n_heads, head_dim, head_dim) fp32")
         tensors.append(state)
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.float32
+    if out_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError(f"out_dtype must be float32 or bfloat16, got {out_dtype}")
     if out is None:
-        out = torch.empty((B, T, H, d), dtype=torch.float32, device=q.device)
+        out = torch.empty((B, T, H, d), dtype=out_dtype, device=q.device)
     if state_out is None:
         state_out = torch.empty((B, H, d, d), dtype=torch.float32, device=q.device)
     tensors += [out, state_out]
@@ -171,8 +179,8 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
             raise ValueError("all tensors must be contiguous CUDA tensors")
         if t.device != q.device:
             raise ValueError("all tensors must be on one CUDA device")
-    if tuple(out.shape) != (B, T, H, d) or out.dtype != torch.float32:
-        raise ValueError("out must be (n_seqs, n_tokens, n_heads, head_dim) fp32")
+    if tuple(out.shape) != (B, T, H, d) or out.dtype != out_dtype:
+        raise ValueError(f"out must be (n_seqs, n_tokens, n_heads, head_dim) {out_dtype}")
     if tuple(state_out.shape) != (B, H, d, d) or state_out.dtype != torch.float32:
         raise ValueError("state_out must be (n_seqs, n_heads, head_dim, head_dim) fp32")
     ws_ptr, ws_bytes = None, 0
@@ -181,7 +189,8 @@ def forward(q, k, v, g, beta, state=None, *, out=None, state_out=None, path: str
     with torch.cuda.device(q.device):
         rc = L.gdn_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
                               _ptr(out), _ptr(state_out), B, T, H, Hk, d, dt,
-                              PATHS[path] | (OPT_L2NORM_QK if l2norm_qk else 0),
+                              PATHS[path] | (OPT_L2NORM_QK if l2norm_qk else 0)
+                              | (OPT_OUT_BF16 if out_dtype == torch.bfloat16 else 0),
                               ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != OK:
         raise GdnError(rc, "gdn_forward_ex")

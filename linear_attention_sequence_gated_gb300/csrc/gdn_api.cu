@@ -104,7 +104,7 @@ struct Sizes {
 // Host-side validation; fills `sz`.  Launches nothing.
 int validate(const void *q, const void *k, const void *v, const float *g, const float *beta,
              const float *state_in, const float *out, const float *state_out, int B, int T,
-             int H, int Hk, int d, int dtype, int path, Sizes *sz) {
+             int H, int Hk, int d, int dtype, int path, bool out_bf16, Sizes *sz) {
     if (B < 0 || T < 0 || H < 0 || d <= 0) return GDN_ERR_ARG;
     // key heads: value head i reads key head i % Hk; Hk must divide H
     if (H > 0 && (Hk < 1 || Hk > H || H % Hk != 0)) return GDN_ERR_ARG;
@@ -128,7 +128,8 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
     const unsigned long long elt = dtype == GDN_DTYPE_BF16 ? 2 : 4;
     if (!span_bytes(bthkd, elt, &sz->qk_bytes) || !span_bytes(bthd, elt, &sz->v_bytes) ||
         !span_bytes(bth, 4, &sz->gb_bytes) ||
-        !span_bytes(bhdd, 4, &sz->state_bytes) || !span_bytes(bthd, 4, &sz->out_bytes))
+        !span_bytes(bhdd, 4, &sz->state_bytes) ||
+        !span_bytes(bthd, out_bf16 ? 2 : 4, &sz->out_bytes))
         return GDN_ERR_ARG;
 
     if (bh == 0) return GDN_OK;  // nothing to do, nothing to check
@@ -157,7 +158,7 @@ int validate(const void *q, const void *k, const void *v, const float *g, const 
 }
 
 constexpr int kPathMask = 0xff;
-constexpr int kKnownOptions = GDN_OPT_L2NORM_QK;
+constexpr int kKnownOptions = GDN_OPT_L2NORM_QK | GDN_OPT_OUT_BF16;
 
 int run(const void *q, const void *k, const void *v, const float *g, const float *beta,
         const float *state_in, float *out, float *state_out, int B, int T, int H, int Hk, int d,
@@ -165,9 +166,10 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
     if (path_opts < 0 || (path_opts & ~kPathMask & ~kKnownOptions)) return GDN_ERR_ARG;
     int path = path_opts & kPathMask;
     const bool l2norm = (path_opts & GDN_OPT_L2NORM_QK) != 0;
+    const bool out_bf16 = (path_opts & GDN_OPT_OUT_BF16) != 0;
     Sizes sz{};
     int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype, path,
-                      &sz);
+                      out_bf16, &sz);
     if (rc != GDN_OK) return rc;
     if ((long long)B * H == 0) return GDN_OK;
 
@@ -194,7 +196,7 @@ int run(const void *q, const void *k, const void *v, const float *g, const float
     if (!status) return GDN_ERR_CUDA;
 
     gdn::Problem p{q, k, v, g, beta, state_in, out, state_out, B, T, H, Hk, d, dtype,
-                   (float)(1.0 / std::sqrt((double)d)), status, l2norm};
+                   (float)(1.0 / std::sqrt((double)d)), status, l2norm, out_bf16};
 
     if (path == GDN_PATH_RECURRENT) {
         return gdn::launch_recurrent(p, stream) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;

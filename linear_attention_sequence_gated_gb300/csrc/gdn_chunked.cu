@@ -651,7 +651,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
                const float *__restrict__ beta, const float *state_in, float *state_out,
                float *__restrict__ out, const uint8_t *__restrict__ zws, int T, int H, int Hk,
-               float scale, int *status)
+               float scale, int *status, bool out_bf16)
 {
     using CF = Cfg<D, BV_>;
     constexpr int BV = CF::BV;
@@ -1036,8 +1036,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     const int r = row - 64;
                     if (r < n) {
                         const float gr = NORM ? sGam[r] * sNq[r] : sGam[r];
-                        float *orow = out + ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D +
-                                      v0 + wg * HALF;
+                        // output element of (token t0 + r, value v0 + wg * HALF)
+                        const size_t oi = ((size_t)b * T + t0 + r) * tok_stride + (size_t)h * D +
+                                          v0 + wg * HALF;
 #pragma unroll
                         for (int j = 0; j < HALF; j += 4) {
                             float4 o4;
@@ -1045,7 +1046,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                             o4.y = fmaf(gr, xq[j + 1], y[j + 1]) * scale;
                             o4.z = fmaf(gr, xq[j + 2], y[j + 2]) * scale;
                             o4.w = fmaf(gr, xq[j + 3], y[j + 3]) * scale;
-                            *reinterpret_cast<float4 *>(orow + j) = o4;
+                            if (out_bf16) {                // 4 values rounded to nearest even
+                                const __nv_bfloat162 lo = __floats2bfloat162_rn(o4.x, o4.y);
+                                const __nv_bfloat162 hi = __floats2bfloat162_rn(o4.z, o4.w);
+                                uint2 w;
+                                w.x = *reinterpret_cast<const uint32_t *>(&lo);
+                                w.y = *reinterpret_cast<const uint32_t *>(&hi);
+                                *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(out) +
+                                                           oi + j) = w;
+                            } else {
+                                *reinterpret_cast<float4 *>(out + oi + j) = o4;
+                            }
                         }
                     }
                 } else {
@@ -1306,7 +1317,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ g,
                     const float *__restrict__ beta, const float *state_in, float *state_out,
                     float *__restrict__ out, int T, int H, int Hk, float scale,
-                    int *status)
+                    int *status, bool out_bf16)
 {
     // Where O is staged.  head_dim 128: in the chunk's Z buffer, so that it
     // overlaps the S product, which still reads the R^T / U~^T buffer; the
@@ -1599,6 +1610,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (vrow) {
                 const int v = row;
                 float *ot = reinterpret_cast<float *>(stage);
+                __nv_bfloat16 *otb = reinterpret_cast<__nv_bfloat16 *>(stage);
 #pragma unroll 1
                 for (int jc = wg * 32; jc < wg * 32 + 32; jc += 16) {
                     float xq[16], pu[16], gm[16];
@@ -1611,7 +1623,11 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
                     }
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) ot[(jc + j) * D + v] = fmaf(gm[j], xq[j], pu[j]) * scale;
+                    for (int j = 0; j < 16; ++j) {
+                        const float o = fmaf(gm[j], xq[j], pu[j]) * scale;
+                        if (out_bf16) otb[(jc + j) * D + v] = __float2bfloat16_rn(o);
+                        else ot[(jc + j) * D + v] = o;
+                    }
                 }
             }
             ptx::fence_proxy_async_smem();
@@ -1854,18 +1870,20 @@ bool make_map(CUtensorMap *map, const void *base, int B, int T, int H, int d, in
            CUDA_SUCCESS;
 }
 
-// 4-D map over the (B, T, H, d) fp32 output; box = {d, 1 head, 64 tokens,
-// 1 sequence}, unswizzled: a [token][value] tile of one chunk.  Tokens past
-// T are clipped by the store.
-bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d) {
+// 4-D map over the (B, T, H, d) output, fp32 or bf16; box = {d, 1 head, 64
+// tokens, 1 sequence}, unswizzled: a [token][value] tile of one chunk.
+// Tokens past T are clipped by the store.
+bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d, bool bf16) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
+    const cuuint64_t es = bf16 ? 2 : 4;
     const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4,
-                                   (cuuint64_t)T * H * d * 4};
+    const cuuint64_t strides[3] = {(cuuint64_t)d * es, (cuuint64_t)H * d * es,
+                                   (cuuint64_t)T * H * d * es};
     const cuuint32_t box[4] = {(cuuint32_t)d, 1, (cuuint32_t)C, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+    return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+               base, dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
@@ -1905,7 +1923,7 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
     if (e != cudaSuccess) return e;
     chunked_kernel<D, BV, NORM><<<(unsigned)(p.B * p.H * CF::NVB), CF::NTH, CF::SMEM, stream>>>(
         mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
-        p.status);
+        p.status, p.out_bf16);
     return cudaGetLastError();
 }
 
@@ -1915,7 +1933,7 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64) ||
         !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64) ||
         !make_map(&mv, p.v, p.B, p.T, p.H, D, 64) ||
-        !make_map_out(&mo, p.out, p.B, p.T, p.H, D))
+        !make_map_out(&mo, p.out, p.B, p.T, p.H, D, p.out_bf16))
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
@@ -1925,7 +1943,7 @@ cudaError_t launch_ws(const Problem &p, cudaStream_t stream) {
     if (attr_err != cudaSuccess) return attr_err;
     d128::chunked_d128_kernel<D, NORM><<<(unsigned)(p.B * p.H), d128::NTH, d128::SMEM, stream>>>(
         mq, mk, mv, mo, p.g, p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale,
-        p.status);
+        p.status, p.out_bf16);
     return cudaGetLastError();
 }
 

@@ -6,6 +6,9 @@
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+#endif
 
 namespace gdn {
 
@@ -59,14 +62,26 @@ struct Problem {
     const void *v;                 // (B, T, H, d), dtype below
     const float *g, *beta;         // (B, T, H)
     const float *state_in;         // (B, H, d, d) [value][key] or nullptr (zeros)
-    float *out;                    // (B, T, H, d) fp32, scaled by 1/sqrt(d)
+    float *out;                    // (B, T, H, d) fp32 (bf16 with out_bf16), scaled by 1/sqrt(d)
     float *state_out;              // (B, H, d, d) [value][key]; may equal state_in
     int B, T, H, Hk, d;            // value head h reads key head h % Hk (Hk divides H)
     int dtype;                     // GDN_DTYPE_F32 / GDN_DTYPE_BF16
     float scale;                   // (float)(1 / sqrt((double)d))
     int *status;                   // device status word (bounded waits report here)
     bool l2norm_qk;                // divide q and k by their norm per token first
+    bool out_bf16;                 // out holds bf16: each value rounded to nearest even
 };
+
+#ifdef __CUDACC__
+// Output element i of a call: float32, or bf16 rounded to nearest even when
+// the caller asked for bf16 output (the same value, rounded once).
+__device__ __forceinline__ void put_out(float *out, size_t i, float x, bool bf16) {
+    if (bf16)
+        reinterpret_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(x);
+    else
+        out[i] = x;
+}
+#endif
 
 // Recurrent path (gdn_recurrent.cu): any T >= 1, d in {32, 64, 128, 256}.
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);

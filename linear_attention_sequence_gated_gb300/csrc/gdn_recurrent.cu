@@ -111,7 +111,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const Tin *__restrict__ v, const float *__restrict__ g,
                  const float *__restrict__ beta, const float *state_in,
                  float *state_out, float *__restrict__ out, int T, int H, int Hk,
-                 float scale)
+                 float scale, bool out_bf16)
 {
     constexpr int NV = D / (4 * L);   // 128-bit vectors per lane per row
     constexpr int RU = 32 / L;        // rows per warp unit
@@ -168,7 +168,6 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const Tin *vp = v + in_base;
     const float *gp = g + gb_base;
     const float *bp = beta + gb_base;
-    float *op = out + in_base;
 
     using In = TokenInputs<D, L, R, Tin>;
     auto load_token = [&](int t, In &x) {
@@ -248,7 +247,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 for (int e = 0; e < 4; ++e)
                     s[u][j][e] = fmaf(alpha, s[u][j][e], dk * kv[j][e]);
             const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
-            if (sub == 0) op[o + row0 + u * RU] = ov;
+            if (sub == 0) put_out(out, in_base + o + row0 + u * RU, ov, out_bf16);
         }
         if (t + 1 < T) cur = nxt;
     }
@@ -315,7 +314,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         const Tin *__restrict__ v, const float *__restrict__ g,
                         const float *__restrict__ beta, const float *state_in,
                         float *state_out, float *__restrict__ out, int T, int H, int Hk,
-                        float scale)
+                        float scale, bool out_bf16)
 {
     constexpr int NV = D / (4 * L);
     constexpr int RU = 32 / L;
@@ -370,7 +369,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const Tin *vp = v + ((size_t)b * T * H + h) * D + blockIdx.y * RB;
     const float *gp = g + (size_t)b * T * H + h;
     const float *bp = beta + (size_t)b * T * H + h;
-    float *op = out + ((size_t)b * T * H + h) * D;
+    const size_t ob = ((size_t)b * T * H + h) * D;      // output element of (b, token 0, h)
 
     // stage window w (tokens w*WT .. min(T, (w+1)*WT) - 1) into buffer `buf`
     auto issue = [&](int w, int buf) {
@@ -496,7 +495,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         s[u][jv][e + 1] = sn.y;
                     }
                 const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
-                if (sub == 0) op[o + row0 + u * RU] = ov;
+                if (sub == 0) put_out(out, ob + o + row0 + u * RU, ov, out_bf16);
             }
         }
         __syncthreads();                                     // buffer w & 1 free for window w + 2
@@ -533,10 +532,11 @@ cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
         return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow, NORM>,
                                   static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
                                   static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in,
-                                  p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
+                                  p.state_out, p.out, p.T, p.H, p.Hk, p.scale, p.out_bf16);
     return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin, NORM>, static_cast<const Tin *>(p.q),
                               static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v), p.g,
-                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale);
+                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale,
+                              p.out_bf16);
 }
 
 template <int D, int L, typename Tin, bool NORM>

@@ -220,14 +220,27 @@ def test_flash_attn_empty_is_a_no_op(L):
 
 
 def test_option_bits(L):
-    # GDN_OPT_L2NORM_QK is accepted in the path argument; unknown bits are not
-    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | gdn.OPT_L2NORM_QK) == 32 * 64 * 32768
-    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | 0x200) == 0
-    assert call(L, path=0x200) == gdn.ERR_ARG
-    assert call(L, path=0x101 | 0x400) == gdn.ERR_ARG
+    # GDN_OPT_L2NORM_QK and GDN_OPT_OUT_BF16 are accepted in the path
+    # argument (alone or together); unknown bits are not
+    for opt in (gdn.OPT_L2NORM_QK, gdn.OPT_OUT_BF16, gdn.OPT_L2NORM_QK | gdn.OPT_OUT_BF16):
+        assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | opt) == 32 * 64 * 32768
+        # a valid option still goes through host validation (here: misaligned q)
+        assert call(L, q=BASE + 8, path=opt) == gdn.ERR_ALIGN
+    assert L.gdn_workspace_bytes(1, 4096, 32, 128, 1, 2 | 0x400) == 0
+    assert call(L, path=0x400) == gdn.ERR_ARG
+    assert call(L, path=0x101 | 0x800) == gdn.ERR_ARG
     assert call(L, path=-1) == gdn.ERR_ARG
-    # a valid option still goes through host validation (here: misaligned q)
-    assert call(L, q=BASE + 8, path=gdn.OPT_L2NORM_QK) == gdn.ERR_ALIGN
+
+
+def test_bf16_output_extent_is_two_bytes_per_element(L):
+    """With GDN_OPT_OUT_BF16 the output occupies 2-byte elements: an out
+    buffer ending 1904 bytes before state_out overlaps it as fp32 (8192
+    bytes) but not as bf16 (4096 bytes).  The bf16 call then stops at its
+    too-small workspace instead, still on the host."""
+    s_out = BASE + 768 * MB
+    kw = dict(out=s_out - 6000, d=256, path=2, ws=BASE + 900 * MB, ws_bytes=16)
+    assert call(L, **kw) == gdn.ERR_ALIAS
+    assert call(L, **{**kw, "path": 2 | gdn.OPT_OUT_BF16}) == gdn.ERR_WORKSPACE
 
 
 def test_gdn_entry_points_reject_f16(L):

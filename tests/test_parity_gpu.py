@@ -624,6 +624,67 @@ def test_fused_qk_l2norm_of_unit_inputs_changes_nothing_measurable():
         assert rel(o2, o1) < 2e-2 and rel(s2, s1) < 2e-2, path
 
 
+# ------------------------------------------------------------- bf16 output
+
+def check_bf16_out(inp, path, l2norm=False):
+    """GDN_OPT_OUT_BF16: the output is the fp32 output of the same call
+    rounded to nearest even, element by element (torch converts float32 to
+    bfloat16 the same way), and the state is the same bit for bit."""
+    args = (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"])
+    o32, s32 = gdn.forward(*args, path=path, l2norm_qk=l2norm)
+    o16, s16 = gdn.forward(*args, path=path, l2norm_qk=l2norm, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    assert o16.dtype == torch.bfloat16 and o16.shape == o32.shape
+    assert torch.equal(o16, o32.to(torch.bfloat16)), path
+    assert torch.equal(s16, s32), path
+
+
+@pytest.mark.parametrize("d", [32, 64, 96, 128, 256])
+@pytest.mark.parametrize("T", [1, 5, 70])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_bf16_output_is_the_fp32_output_rounded(d, T, dtype):
+    """Every path and head_dim: one-token and windowed recurrent kernels,
+    and the chunked kernels over a ragged tail."""
+    w = W.Workload(f"o16_d{d}_t{T}", 2, T, 4, d, dtype, 0.0, 0.02, seed=90 + T)
+    inp = W.make_inputs(w, "cuda")
+    for path in paths_for(d, T, dtype):
+        check_bf16_out(inp, path)
+
+
+@pytest.mark.parametrize("name,B,H,d", CHUNKED_KERNELS)
+def test_bf16_output_on_every_chunked_kernel(name, B, H, d):
+    """Each chunked kernel and state-walk width: the one-kernel path stages a
+    bf16 O tile for its TMA store, the state walk stores 4 rounded values at
+    a time; with and without q / k normalisation."""
+    w = W.Workload(f"o16_{name}", B, 200, H, d, "bf16", 0.0, 0.05, seed=92)
+    inp = W.make_inputs(w, "cuda")
+    check_bf16_out(inp, "chunked")
+    check_bf16_out(raw_qk(inp, seed=93), "chunked", l2norm=True)
+
+
+def test_bf16_output_writes_nothing_outside_it():
+    """A caller-provided bf16 output inside NaN guard regions (70 tokens: the
+    last chunk is ragged), on both paths."""
+    w = W.Workload("o16_guard", 2, 70, 3, 64, "bf16", 0.0, 0.02, seed=94)
+    inp = W.make_inputs(w, "cuda")
+    B, T, H, d = 2, 70, 3, 64
+    pad = 4096
+    for path in paths_for(d, T):
+        ob = torch.full((B * T * H * d + 2 * pad,), float("nan"), dtype=torch.bfloat16,
+                        device="cuda")
+        out = ob[pad:pad + B * T * H * d].view(B, T, H, d)
+        o, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                            out=out, path=path)
+        torch.cuda.synchronize()
+        assert o.data_ptr() == out.data_ptr()
+        assert torch.isnan(ob[:pad]).all() and torch.isnan(ob[-pad:]).all(), path
+        ref, _ = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                             path=path)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref.to(torch.bfloat16)), path
+
+
 # ------------------------------------------------ back-to-back state reuse
 
 @pytest.mark.parametrize("T", [1, 5])
