@@ -6,9 +6,6 @@
 #include <cstdint>
 #include <mutex>
 #include <cuda_runtime.h>
-#ifdef __CUDACC__
-#include <cuda_bf16.h>
-#endif
 
 namespace gdn {
 
@@ -71,17 +68,6 @@ struct Problem {
     bool l2norm_qk;                // divide q and k by their norm per token first
     bool out_bf16;                 // out holds bf16: each value rounded to nearest even
 };
-
-#ifdef __CUDACC__
-// Output element i of a call: float32, or bf16 rounded to nearest even when
-// the caller asked for bf16 output (the same value, rounded once).
-__device__ __forceinline__ void put_out(float *out, size_t i, float x, bool bf16) {
-    if (bf16)
-        reinterpret_cast<__nv_bfloat16 *>(out)[i] = __float2bfloat16_rn(x);
-    else
-        out[i] = x;
-}
-#endif
 
 // Recurrent path (gdn_recurrent.cu): any T >= 1, d in {32, 64, 128, 256}.
 cudaError_t launch_recurrent(const Problem &p, cudaStream_t stream);

@@ -102,16 +102,20 @@ struct TokenInputs {
     float g, beta;
 };
 
+// One output value: float32 as computed, or bf16 rounded to nearest even.
+__device__ __forceinline__ void store_out(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_out(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
 // 1 / |x| from the squared norm, 0 for a zero vector.
 __device__ __forceinline__ float inv_norm(float sq) { return sq > 0.f ? rsqrtf(sq) : 0.f; }
 
-template <int D, int L, int R, typename Tin, bool NORM>
+template <int D, int L, int R, typename Tin, bool NORM, typename Tout>
 __global__ void __launch_bounds__(128)
 recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const Tin *__restrict__ v, const float *__restrict__ g,
                  const float *__restrict__ beta, const float *state_in,
-                 float *state_out, float *__restrict__ out, int T, int H, int Hk,
-                 float scale, bool out_bf16)
+                 float *state_out, Tout *__restrict__ out, int T, int H, int Hk,
+                 float scale)
 {
     constexpr int NV = D / (4 * L);   // 128-bit vectors per lane per row
     constexpr int RU = 32 / L;        // rows per warp unit
@@ -168,6 +172,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const Tin *vp = v + in_base;
     const float *gp = g + gb_base;
     const float *bp = beta + gb_base;
+    Tout *op = out + in_base;
 
     using In = TokenInputs<D, L, R, Tin>;
     auto load_token = [&](int t, In &x) {
@@ -247,7 +252,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 for (int e = 0; e < 4; ++e)
                     s[u][j][e] = fmaf(alpha, s[u][j][e], dk * kv[j][e]);
             const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
-            if (sub == 0) put_out(out, in_base + o + row0 + u * RU, ov, out_bf16);
+            if (sub == 0) store_out(op + o + row0 + u * RU, ov);
         }
         if (t + 1 < T) cur = nxt;
     }
@@ -308,13 +313,13 @@ struct alignas(16) TokenWindow {
     float iq[WT];      // 1 / |q| of each token (NORM)
 };
 
-template <int D, int L, int R, typename Tin, int WT, bool NORM>
+template <int D, int L, int R, typename Tin, int WT, bool NORM, typename Tout>
 __global__ void __launch_bounds__(128)
 recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         const Tin *__restrict__ v, const float *__restrict__ g,
                         const float *__restrict__ beta, const float *state_in,
-                        float *state_out, float *__restrict__ out, int T, int H, int Hk,
-                        float scale, bool out_bf16)
+                        float *state_out, Tout *__restrict__ out, int T, int H, int Hk,
+                        float scale)
 {
     constexpr int NV = D / (4 * L);
     constexpr int RU = 32 / L;
@@ -369,7 +374,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const Tin *vp = v + ((size_t)b * T * H + h) * D + blockIdx.y * RB;
     const float *gp = g + (size_t)b * T * H + h;
     const float *bp = beta + (size_t)b * T * H + h;
-    const size_t ob = ((size_t)b * T * H + h) * D;      // output element of (b, token 0, h)
+    Tout *op = out + ((size_t)b * T * H + h) * D;
 
     // stage window w (tokens w*WT .. min(T, (w+1)*WT) - 1) into buffer `buf`
     auto issue = [&](int w, int buf) {
@@ -495,7 +500,7 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                         s[u][jv][e + 1] = sn.y;
                     }
                 const float ov = fmaf(alpha, pq[u], delta * kq) * scale;
-                if (sub == 0) put_out(out, ob + o + row0 + u * RU, ov, out_bf16);
+                if (sub == 0) store_out(op + o + row0 + u * RU, ov);
             }
         }
         __syncthreads();                                     // buffer w & 1 free for window w + 2
@@ -513,8 +518,8 @@ recurrent_window_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 // Tokens staged per window by the multi-token kernel.
 constexpr int kWindow = 8;
 
-template <int D, int L, int R, typename Tin, bool NORM>
-cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
+template <int D, int L, int R, typename Tin, bool NORM, typename Tout>
+cudaError_t launch_one_out(const Problem &p, cudaStream_t stream) {
     constexpr int RB = 4 * R * (32 / L);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.B * (unsigned)p.H, D / RB);
@@ -529,14 +534,23 @@ cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (p.T >= 2)
-        return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow, NORM>,
+        return cudaLaunchKernelEx(&cfg, recurrent_window_kernel<D, L, R, Tin, kWindow, NORM, Tout>,
                                   static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
                                   static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in,
-                                  p.state_out, p.out, p.T, p.H, p.Hk, p.scale, p.out_bf16);
-    return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin, NORM>, static_cast<const Tin *>(p.q),
-                              static_cast<const Tin *>(p.k), static_cast<const Tin *>(p.v), p.g,
-                              p.beta, p.state_in, p.state_out, p.out, p.T, p.H, p.Hk, p.scale,
-                              p.out_bf16);
+                                  p.state_out, reinterpret_cast<Tout *>(p.out), p.T, p.H, p.Hk,
+                                  p.scale);
+    return cudaLaunchKernelEx(&cfg, recurrent_kernel<D, L, R, Tin, NORM, Tout>,
+                              static_cast<const Tin *>(p.q), static_cast<const Tin *>(p.k),
+                              static_cast<const Tin *>(p.v), p.g, p.beta, p.state_in, p.state_out,
+                              reinterpret_cast<Tout *>(p.out), p.T, p.H, p.Hk, p.scale);
+}
+
+// The output type is a template parameter: with a runtime switch the
+// multi-token kernel needed 9 more registers and lost one block per SM.
+template <int D, int L, int R, typename Tin, bool NORM>
+cudaError_t launch_one(const Problem &p, cudaStream_t stream) {
+    return p.out_bf16 ? launch_one_out<D, L, R, Tin, NORM, __nv_bfloat16>(p, stream)
+                      : launch_one_out<D, L, R, Tin, NORM, float>(p, stream);
 }
 
 template <int D, int L, typename Tin, bool NORM>
