@@ -345,6 +345,24 @@ def test_in_place_state_update_chunked(name, B, H, d):
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
+@pytest.mark.parametrize("B,H,d", [(1, 38, 128), (1, 39, 128), (1, 19, 256), (1, 20, 256)])
+def test_state_walk_width_boundary(B, H, d):
+    """The state walk takes 32-row value blocks while (pairs x head_dim / 32)
+    fits one wave of 152 SMs, else 64-row blocks: 38 pairs at head_dim 128
+    and 19 at 256 are the last 32-row cases, 39 and 20 the first 64-row
+    ones.  Each against the oracle, in place, over a ragged tail."""
+    w = W.Workload(f"walkw_h{H}_d{d}", B, 150, H, d, "bf16", 0.0, 0.02, seed=17)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    st = inp["state"].clone()
+    out, _ = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st,
+                         state_out=st, path="chunked")
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    e_out, e_st = errs(out, st, ref_out, ref_st)
+    assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
+
+
 def _named_call(fn, inp, out, st_out):
     p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     B, T, H, d = inp["v"].shape

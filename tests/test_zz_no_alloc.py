@@ -129,3 +129,22 @@ def test_rejects_calls_beyond_the_fixed_scratch(L):
                                8, 16384, 16, 16, 256, gdn.DTYPE_BF16, gdn.PATHS["chunked"], None)
     assert rc == gdn.ERR_SCRATCH
     assert "64 MiB" in gdn.status_string(rc)
+
+
+def test_options_pass_through(L):
+    """Option bits in the path argument reach the kernels through this entry
+    point as through gdn_forward_ex: q/k normalisation and a bf16 output on
+    the scratch-using head_dim-256 path, bit for bit."""
+    w = W.Workload("noalloc_opts", 2, 300, 4, 256, "bf16", 0.0, 0.02, seed=77)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                  inp["state"], path="chunked", l2norm_qk=True,
+                                  out_dtype=torch.bfloat16)
+    out = torch.full_like(ref_out, float("nan"))
+    st = torch.full_like(ref_st, float("nan"))
+    path = gdn.PATHS["chunked"] | gdn.OPT_L2NORM_QK | gdn.OPT_OUT_BF16
+    assert noalloc(L, inp, out, st, path=path) == gdn.OK
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    assert out.dtype == torch.bfloat16
+    assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
