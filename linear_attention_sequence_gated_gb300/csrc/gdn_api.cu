@@ -70,20 +70,21 @@ using gdn::host::range_of;
 using gdn::host::span_bytes;
 
 // Tokens from which AUTO prefers the chunked path, measured on GB300 with
-// bf16 q/k/v (both paths timed over T = 2..128 for 32, 128, 256 and 2048
-// (sequence, head) pairs).  The recurrent path costs a near-constant time
-// per token; the chunked path a near-constant time per 64-token chunk, so
-// the switch sits where one chunk's time equals the tokens' time.  With few
-// (sequence, head) pairs the recurrent kernel has more of the GPU per pair
-// and stays ahead longer.
+// bf16 q/k/v: both paths timed per call over T = 16..128, 20 calls captured
+// in a CUDA graph, for 8 to 2048 (sequence, head) pairs.  The recurrent path
+// costs a near-constant time per token; the chunked path a near-constant time
+// per 64-token chunk (plus, below 80 pairs at head_dim 128 and at head_dim
+// 256, a chunk-transform pass), so the switch sits where one chunk's time
+// equals the tokens' time.  With few pairs the recurrent kernel has more of
+// the GPU per pair and stays ahead longer; with very many, head_dim 64 fills
+// the GPU with the recurrent kernel as well and the switch moves up again.
 int chunked_min_tokens(long long pairs, int head_dim) {
-    const bool many = pairs >= 128;
     switch (head_dim) {
-        case 64: return pairs >= 1024 ? 64 : 48;
-        // fewer than 80 pairs run the two-kernel chunked path (a fixed cost of
-        // two launches and a transform pass), 80 or more the one-kernel path
-        case 128: return pairs >= 80 ? 24 : (pairs >= 48 ? 44 : 72);
-        case 256: return many ? 24 : 32;
+        case 64: return pairs < 64 ? 56 : (pairs < 256 ? 32 : (pairs < 1024 ? 40 : 56));
+        // fewer than 80 pairs run the two-kernel chunked path, 80 or more the
+        // one-kernel path
+        case 128: return pairs < 32 ? 64 : (pairs < 64 ? 48 : (pairs < 80 ? 40 : 24));
+        case 256: return pairs < 12 ? 48 : (pairs < 24 ? 32 : 24);
         default: return INT_MAX;
     }
 }

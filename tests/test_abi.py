@@ -73,10 +73,11 @@ def test_workspace_and_path_queries(L):
     assert gdn.select_path(1, 4096, 32, 32) == "recurrent"            # no chunked d = 32
     assert gdn.select_path(1, 4096, 32, 96) == "recurrent"            # no chunked d = 96
     # measured switch points: (pairs, head_dim) -> first chunked length
-    for pairs, d, t_switch in ((32, 64, 48), (256, 64, 48), (2048, 64, 64), (32, 128, 72),
-                               (64, 128, 44), (96, 128, 24), (128, 128, 24), (2048, 128, 24),
-                               (32, 256, 32), (256, 256, 24)):
-        B, H = pairs // 32, 32
+    for pairs, d, t_switch in ((32, 64, 56), (128, 64, 32), (256, 64, 40), (2048, 64, 56),
+                               (16, 128, 64), (32, 128, 48), (48, 128, 48), (64, 128, 40),
+                               (96, 128, 24), (128, 128, 24), (2048, 128, 24),
+                               (8, 256, 48), (16, 256, 32), (32, 256, 24), (256, 256, 24)):
+        B, H = (pairs // 32, 32) if pairs >= 32 else (1, pairs)
         assert gdn.select_path(B, t_switch - 1, H, d) == "recurrent"
         assert gdn.select_path(B, t_switch, H, d) == "chunked"
         assert gdn.select_path(B, 4096, H, d, "f32") == "recurrent"    # chunked is bf16 only
