@@ -41,7 +41,8 @@
 //   4. MMA  [K;Q] S0^T -> TMEM: both K S0^T (for R) and Q S0^T (for O).
 //   5. R = beta V - beta gamma K S0^T, written as bf16 hi + lo.
 //   6. MMA  Z R -> TMEM: rows 0-63 are U = T R, rows 64-127 are P T R = P U.
-//   7. O = gamma Q S0^T + P U, scaled, to global; U scaled by
+//   7. O = gamma Q S0^T + P U, scaled, to global (fp32, or bf16 rounded to
+//      nearest even when the caller asks for it); U scaled by
 //      exp(G_{C-1} - G_r) and written as bf16 hi + lo.
 //   8. MMA  U~^T K (or K^T U~) -> TMEM: the state increment.
 //   9. S = gamma_{C-1} S + dS in fp32; bf16 hi + lo for step 4.
@@ -93,7 +94,8 @@ struct Cfg {
     // this one is computed.  Not at head_dim 256 with 64-row blocks: its
     // 64-register state block needs the register budget of eight warps (a
     // ninth rounds the budget to twelve), and only one slot of [K;Q] and V
-    // fits.  There thread 0 issues each load as soon as its slot is free.
+    // fits.  There one thread per tile (0: [K;Q], 32: V, 64: Z) issues each
+    // load as soon as its slot is free.
     static constexpr bool PW = !(D == 256 && BV == 64);
     static constexpr int NQK = PW && D == 128 ? 2 : 1;
     static constexpr int NZS = PW ? 2 : 1;
@@ -746,9 +748,9 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (atomicExch(const_cast<int *>(abort_flag), 1) == 0) atomicExch(status, GDN_ERR_TIMEOUT);
     };
 
-    // ---- loads (one thread: lane 0 of warp 8, or thread 0).  Chunk c's
-    // [K;Q], V and Z go to slot c % (slots of that tile); the thread records
-    // the last chunk it loaded into each slot.
+    // ---- loads (lane 0 of warp 8; without it threads 0, 32 and 64, one per
+    // tile).  Chunk c's [K;Q], V and Z go to slot c % (slots of that tile);
+    // the issuing thread records the last chunk it loaded into each slot.
     int last_qk[2] = {-1, -1}, last_v[2] = {-1, -1}, last_z[2] = {-1, -1};
     auto issue_v = [&](int c) {
         const int sv = c % CF::NVS;
