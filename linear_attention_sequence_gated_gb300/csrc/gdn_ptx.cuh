@@ -278,25 +278,6 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// Each thread of the warp reads 32 consecutive fp32 columns of its lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
-        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
-        " [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Barrier among `nthreads` threads (a multiple of 32) using hardware barrier
 // `id` (1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
@@ -304,22 +285,6 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
 }
 
 // ------------------------------------------------------------- bf16 helpers
-
-// Round-to-nearest-even fp32 -> bf16 bits, and the exact residual.
-__device__ __forceinline__ uint32_t bf16_bits_rn(float x) {
-    uint32_t u = __float_as_uint(x);
-    // NaN stays NaN; everything else rounds to nearest even
-    if ((u & 0x7fffffffu) > 0x7f800000u) return (u >> 16) | 0x40u;
-    u += 0x7fffu + ((u >> 16) & 1u);
-    return u >> 16;
-}
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
-
-// Split x into hi + lo, both bf16, hi = bf16(x), lo = bf16(x - hi).
-__device__ __forceinline__ void split_bf16(float x, uint32_t &hi, uint32_t &lo) {
-    hi = bf16_bits_rn(x);
-    lo = bf16_bits_rn(x - bf16_bits_to_float(hi));
-}
 
 // Split a pair (a, b) into bf16 hi / lo words: hi truncates (keeps the top 16
 // bits of each fp32), lo = bf16_rn(x - hi).  x - hi is exact in fp32, so
