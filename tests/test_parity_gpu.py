@@ -363,6 +363,32 @@ def test_state_walk_width_boundary(B, H, d):
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
+def test_concurrent_calls_on_two_streams():
+    """Two head_dim-256 chunked calls (each needs a workspace, taken
+    stream-ordered from the library's pool) in flight at once on two
+    streams, with different inputs: each equals the same call made alone."""
+    ws = [W.Workload(f"conc_{i}", 2, 300, 4, 256, "bf16", 0.0, 0.02, seed=40 + i) for i in range(2)]
+    inps = [W.make_inputs(w, "cuda") for w in ws]
+    alone = []
+    for inp in inps:
+        o, s_ = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                            path="chunked")
+        alone.append((o, s_))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    together = [None, None]
+    for rep in range(3):
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                together[i] = gdn.forward(inps[i]["q"], inps[i]["k"], inps[i]["v"], inps[i]["g"],
+                                          inps[i]["beta"], inps[i]["state"], path="chunked",
+                                          stream=streams[i])
+        torch.cuda.synchronize()
+        assert gdn.device_status() == gdn.OK
+        for i in range(2):
+            assert torch.equal(together[i][0], alone[i][0]) and torch.equal(together[i][1], alone[i][1])
+
+
 def _named_call(fn, inp, out, st_out):
     p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
     B, T, H, d = inp["v"].shape
