@@ -110,8 +110,8 @@ enum gdn_path { GDN_PATH_AUTO = 0, GDN_PATH_RECURRENT = 1, GDN_PATH_CHUNKED = 2 
  *   the float32 value the call writes without this option, rounded to
  *   nearest even; the recurrence and the state stay float32.  The call then
  *   needs half the output bytes (its size, alignment and overlap checks count
- *   2-byte elements).  The extra error is that one rounding: at most 2^-9 of
- *   each element's magnitude.
+ *   2-byte elements).  The extra error is that one rounding: at most 2^-8 of
+ *   each element's magnitude (bf16 keeps an 8-bit significand).
  */
 #define GDN_OPT_OUT_BF16 0x200
 

@@ -729,6 +729,54 @@ def test_bf16_output_writes_nothing_outside_it():
         assert torch.equal(out, ref.to(torch.bfloat16)), path
 
 
+# ------------------------------------------------ random configuration sweep
+
+def test_random_configurations_against_the_oracle():
+    """A seeded sweep over the configuration space the other tests cover one
+    axis at a time: sequences, tokens (chunk boundaries and ragged tails),
+    heads and key heads, head_dim, dtype, gate regime, path, q/k
+    normalisation and bf16 output together.  Each result is held to its
+    path's bound against the oracle; a bf16 output additionally to its one
+    rounding (2^-8 of each element's magnitude: bf16 keeps an 8-bit
+    significand)."""
+    rng = np.random.default_rng(2024)
+    for case in range(40):
+        d = int(rng.choice([32, 64, 96, 128, 256]))
+        dtype = str(rng.choice(["bf16", "f32"]))
+        B = int(rng.integers(1, 4))
+        H = int(rng.choice([1, 2, 4, 6, 8]))
+        Hk = int(rng.choice([x for x in range(1, H + 1) if H % x == 0]))
+        T = int(rng.choice([1, 2, 7, 63, 64, 65, 130, 200]))
+        g_shift = float(rng.choice([0.0, 2.0]))
+        l2norm = bool(rng.integers(0, 2))
+        out16 = bool(rng.integers(0, 2))
+        paths = ["auto"] + paths_for(d, T, dtype)
+        path = paths[int(rng.integers(0, len(paths)))]
+        w = W.Workload(f"rand_{case}", B, T, H, d, dtype, g_shift, 0.02, seed=300 + case)
+        inp = W.make_inputs(w, "cuda")
+        inp["q"] = inp["q"][:, :, :Hk].contiguous()
+        inp["k"] = inp["k"][:, :, :Hk].contiguous()
+        if l2norm:
+            inp = raw_qk(inp, seed=400 + case)
+        out, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                              path=path, l2norm_qk=l2norm,
+                              out_dtype=torch.bfloat16 if out16 else torch.float32)
+        torch.cuda.synchronize()
+        assert gdn.device_status() == gdn.OK
+        n = W.to_numpy_f32(inp)
+        ref_out, ref_st = oracle.recurrent_c(n["q"], n["k"], n["v"], n["g"], n["beta"],
+                                             n["state"], l2norm_qk=l2norm)
+        e_out, e_st = errs(out.float(), st, ref_out, ref_st)
+        chunked = path == "chunked" or (path == "auto" and
+                                        gdn.select_path(B, T, H, d, dtype) == "chunked")
+        tol = TOL["bf16"] if chunked else (TOL_RECURRENT if dtype == "bf16" else TOL[dtype])
+        tol_out = tol
+        if out16 and ref_out.size:
+            tol_out += 2.0 ** -8 * float(np.abs(ref_out).max() / np.sqrt((ref_out ** 2).mean()))
+        what = (case, B, T, H, Hk, d, dtype, path, l2norm, out16)
+        assert e_out <= tol_out and e_st <= tol, (what, e_out, e_st)
+
+
 # ------------------------------------------------ back-to-back state reuse
 
 @pytest.mark.parametrize("T", [1, 5])
