@@ -77,6 +77,22 @@ constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrice
 // whose columns are value indices (V, S hi / lo, R / U~ hi / lo) have rows
 // of BV bf16: 128 B with the 128-byte swizzle (BV 64), 64 B with the 64-byte
 // swizzle (BV 32).
+// x[j] = TMEM column (col + j) + column (col + off + j), j < N (a multiple of
+// 16), of this warp's lane quarter: the hi- and lo-operand halves of a
+// product, summed.  16 columns of each half per wait.
+template <int N>
+__device__ __forceinline__ void tmem_ld_pair(uint32_t col, int off, float (&x)[N]) {
+#pragma unroll
+    for (int j = 0; j < N; j += 16) {
+        float lo[16];
+        ptx::tmem_ld16(col + j, *reinterpret_cast<float(*)[16]>(x + j));
+        ptx::tmem_ld16(col + off + j, lo);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[j + e] += lo[e];
+    }
+}
+
 template <int D, int BV_>
 struct Cfg {
     static constexpr int BV = BV_;                         // value rows per CTA
@@ -110,12 +126,18 @@ struct Cfg {
     static constexpr int OFF_MISC = OFF_RU + 2 * 64 * ROWB; // 2 gate sets: G, beta, gamma, end-decay
     static constexpr int OFF_NRM = OFF_MISC + 2 * 4 * 64 * 4;  // 1/|k|, 1/|q| of the chunk
     static constexpr int SMEM = OFF_NRM + 2 * 64 * 4 + 1024;   // + alignment slack
-    // TMEM columns
+    // A split operand's hi and lo tiles lie one tile apart, so that a single
+    // MMA takes both as one B operand of N = 2 BV (its second 64- or 128-byte
+    // atom column is the lo tile: LBO = the tile size).  The products then
+    // land in two column halves, summed by the epilogue that reads them.
+    static constexpr int LBO_S = D * ROWB;                 // S hi -> S lo
+    static constexpr int LBO_RU = 64 * ROWB;               // R (U~) hi -> lo
+    // TMEM columns: X, Y and each 128-key tile of dS take 2 BV (hi | lo half)
     static constexpr int COL_X = 0;
-    static constexpr int COL_Y = BV;
-    static constexpr int COL_DS = 2 * BV;
-    static constexpr int TMEM_COLS = 256;
-    static_assert(COL_DS + KT * BV <= TMEM_COLS, "TMEM columns");
+    static constexpr int COL_Y = 2 * BV;
+    static constexpr int COL_DS = 4 * BV;
+    static constexpr int TMEM_COLS = COL_DS + 2 * KT * BV <= 256 ? 256 : 512;
+    static_assert(COL_DS + 2 * KT * BV <= TMEM_COLS, "TMEM columns");
     static_assert(SMEM + 256 <= 232448, "shared memory (dynamic + static)");
     static_assert(OFF_V % 1024 == 0 && V_BYTES % 1024 == 0 && OFF_Z % 1024 == 0 && OFF_S % 1024 == 0 && OFF_RU % 1024 == 0 &&
                   (D * ROWB) % 1024 == 0 && (64 * ROWB) % 1024 == 0,
@@ -924,21 +946,18 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             }
             ptx::named_sync(1, NT);
 
-            // ---------------- 4. MMA: [K;Q] S^T  (M=128, N=BV, K=D; S as hi + lo)
+            // ---------------- 4. MMA: [K;Q] [S hi | S lo]^T  (M=128, N=2 BV, K=D)
             if (tid == 0) {
                 ptx::tc_fence_after();
-                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
-                const uint32_t bS[2] = {ptx::smem_u32(sShi), ptx::smem_u32(sSlo)};
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 2 * BV, false, true);
+                const uint32_t bS = ptx::smem_u32(sShi);
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint64_t da =
-                            ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t db =
-                            ptx::smem_desc(bS[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
-                        ptx::mma_bf16(tmem + CF::COL_X, da, db, idesc, part > 0 || kk > 0);
-                    }
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t da =
+                        ptx::smem_desc(aQK + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t db =
+                        ptx::smem_desc(bS + kk * 16 * ROWB, CF::LBO_S, 8 * ROWB, CF::SWZ);
+                    ptx::mma_bf16(tmem + CF::COL_X, da, db, idesc, kk > 0);
                 }
                 ptx::mma_commit(&bars.mma);
             }
@@ -957,11 +976,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             float xq[HALF];   // Q S^T for this thread's output row (lanes 64-127)
             {
                 float x[HALF];
-#pragma unroll
-                for (int j = 0; j < HALF; j += 16)
-                    ptx::tmem_ld16(tmem + lane_off + CF::COL_X + wg * HALF + j,
-                                   *reinterpret_cast<float(*)[16]>(x + j));
-                ptx::tmem_ld_wait();
+                tmem_ld_pair<HALF>(tmem + lane_off + CF::COL_X + wg * HALF, BV, x);
                 if (row < 64) {
                     const int r = row;
                     const float br = sBeta[r], bg = br * (NORM ? sGam[r] * sNk[r] : sGam[r]);
@@ -1000,24 +1015,28 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 else if (more) issue_v(c + 1);
             }
 
-            // ---------------- 6. MMA: Z R  (M=128, N=BV, K=64; hi*hi + hi*lo + lo*hi)
+            // ---------------- 6. MMA: Z R  (M=128, K=64): Z hi [R hi | R lo] (N = 2 BV),
+            //                    then Z lo R hi into the hi half
             if (tid == 0) {
                 {
                     ptx::tc_fence_after();
-                    constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, false, true);
-                    const uint32_t aZ[3] = {ptx::smem_u32(sZhi), ptx::smem_u32(sZhi),
-                                            ptx::smem_u32(sZlo)};
-                    const uint32_t bR[3] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo),
-                                            ptx::smem_u32(sRhi)};
+                    constexpr uint32_t idesc2 = ptx::idesc_bf16_f32(128, 2 * BV, false, true);
+                    constexpr uint32_t idesc1 = ptx::idesc_bf16_f32(128, BV, false, true);
+                    const uint32_t aZhi = ptx::smem_u32(sZhi), aZlo = ptx::smem_u32(sZlo);
+                    const uint32_t bR = ptx::smem_u32(sRhi);
 #pragma unroll
-                    for (int part = 0; part < 3; ++part) {
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t db =
+                            ptx::smem_desc(bR + kk * 16 * ROWB, CF::LBO_RU, 8 * ROWB, CF::SWZ);
+                        ptx::mma_bf16(tmem + CF::COL_Y, ptx::smem_desc(aZhi + kk * 32, 16, 1024),
+                                      db, idesc2, kk > 0);
+                    }
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t da = ptx::smem_desc(aZ[part] + kk * 32, 16, 1024);
-                            const uint64_t db =
-                                ptx::smem_desc(bR[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
-                            ptx::mma_bf16(tmem + CF::COL_Y, da, db, idesc, part > 0 || kk > 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t db =
+                            ptx::smem_desc(bR + kk * 16 * ROWB, CF::LBO_RU, 8 * ROWB, CF::SWZ);
+                        ptx::mma_bf16(tmem + CF::COL_Y, ptx::smem_desc(aZlo + kk * 32, 16, 1024),
+                                      db, idesc1, true);
                     }
                     ptx::mma_commit(&bars.mma);
                     if constexpr (PW) ptx::mma_commit(&bars.empty_z[sz]);   // Z free once it is done
@@ -1029,11 +1048,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // ---------------- 7. O (lanes 64-127) and U~ hi / lo (lanes 0-63)
             {
                 float y[HALF];
-#pragma unroll
-                for (int j = 0; j < HALF; j += 16)
-                    ptx::tmem_ld16(tmem + lane_off + CF::COL_Y + wg * HALF + j,
-                                   *reinterpret_cast<float(*)[16]>(y + j));
-                ptx::tmem_ld_wait();
+                tmem_ld_pair<HALF>(tmem + lane_off + CF::COL_Y + wg * HALF, BV, y);
                 if (row >= 64) {
                     const int r = row - 64;
                     if (r < n) {
@@ -1077,24 +1092,21 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::tc_fence_before();
             ptx::named_sync(1, NT);
 
-            // ---------------- 8. MMA: K^T U~  (per 128-key tile: M=128, N=BV, K=64)
+            // ---------------- 8. MMA: K^T [U~ hi | U~ lo]  (per 128-key tile: M=128,
+            //                    N=2 BV, K=64)
             if (tid == 0) {
                 ptx::tc_fence_after();
-                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, BV, true, true);
-                const uint32_t bU[2] = {ptx::smem_u32(sRhi), ptx::smem_u32(sRlo)};
+                constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 2 * BV, true, true);
+                const uint32_t bU = ptx::smem_u32(sRhi);
 #pragma unroll
                 for (int kt = 0; kt < KT; ++kt) {
 #pragma unroll
-                    for (int part = 0; part < 2; ++part) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t da =
-                                ptx::smem_desc(aQK + kt * 2 * 16384 + kk * 2048, 16384, 1024);
-                            const uint64_t db =
-                                ptx::smem_desc(bU[part] + kk * 16 * ROWB, 8192, 8 * ROWB, CF::SWZ);
-                            ptx::mma_bf16(tmem + CF::COL_DS + kt * BV, da, db, idesc,
-                                          part > 0 || kk > 0);
-                        }
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t da =
+                            ptx::smem_desc(aQK + kt * 2 * 16384 + kk * 2048, 16384, 1024);
+                        const uint64_t db =
+                            ptx::smem_desc(bU + kk * 16 * ROWB, CF::LBO_RU, 8 * ROWB, CF::SWZ);
+                        ptx::mma_bf16(tmem + CF::COL_DS + kt * 2 * BV, da, db, idesc, kk > 0);
                     }
                 }
                 ptx::mma_commit(&bars.mma);
@@ -1109,11 +1121,8 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                 for (int kt = 0; kt < KT; ++kt) {
                     float ds[HALF];
-#pragma unroll
-                    for (int j = 0; j < HALF; j += 16)
-                        ptx::tmem_ld16(tmem + lane_off + CF::COL_DS + kt * BV + wg * HALF + j,
-                                       *reinterpret_cast<float(*)[16]>(ds + j));
-                    ptx::tmem_ld_wait();
+                    tmem_ld_pair<HALF>(tmem + lane_off + CF::COL_DS + kt * 2 * BV + wg * HALF, BV,
+                                       ds);
                     const int key = kt * 128 + row;
 #pragma unroll
                     for (int j = 0; j < HALF; ++j) S[kt][j] = fmaf(gC, S[kt][j], ds[j]);
