@@ -387,7 +387,8 @@ def run_single_call(torch, gdn, W, w, dev, timer, args, dist, peaks, kind, in_pl
     ms = dist.max(sum(times) / len(times))
     in_b = 2 if w.dtype == "bf16" else 4
     res = {"workload": w.name, "path": path, "ms_per_step": ms, "spread": spread(times),
-           "launches_per_step": launches_per_call(path, nws)}
+           "launches_per_step": launches_per_call(
+               path, nws, B * H, d, torch.cuda.get_device_properties(dev).multi_processor_count)}
     if kind == "decode":
         bytes_launch = run_bytes(B, T, H, w.n_k, d, in_b)
         achieved = bytes_launch / (ms / 1e3) / 1e9
@@ -476,11 +477,30 @@ def run_decode_steady(torch, gdn, W, w, dev, args, dist, peaks, n_bufs=4):
                                  "equal them (state read + written back once)"}}
 
 
-def launches_per_call(path, workspace_bytes):
+def walk_launches(pairs, d, sms):
+    """State-walk launches of a two-kernel chunked call: the library's value
+    block split (64-row blocks for the full waves, the rest at 32 rows after
+    them when 64-row blocks leave a partial last wave that fits one wave at
+    32 rows), restated here to count kernels."""
+    if pairs * (d // 32) <= sms:
+        return 1
+    ctas64 = pairs * (d // 64)
+    full = ctas64 // sms
+    if full >= 1 and ctas64 % sms and (full * sms) % (d // 64) == 0:
+        p64 = full * sms // (d // 64)
+        if (pairs - p64) * (d // 32) <= sms:
+            return 2
+    return 1
+
+
+def launches_per_call(path, workspace_bytes, pairs=0, d=0, sms=0):
     """Kernels one call launches.  A chunked call that needs a workspace
     (head_dim 256, and head_dim 128 with few (sequence, head) pairs) runs the
-    chunk-transform kernel and then the state kernel; every other call one."""
-    return 2 if (path == "chunked" and workspace_bytes > 0) else 1
+    chunk-transform kernel and then the state walk (one or two launches);
+    every other call one."""
+    if path == "chunked" and workspace_bytes > 0:
+        return 1 + walk_launches(pairs, d, sms)
+    return 1
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -675,7 +675,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ g,
                const float *__restrict__ beta, const float *state_in, float *state_out,
                float *__restrict__ out, const uint8_t *__restrict__ zws, int T, int H, int Hk,
-               float scale, int *status, bool out_bf16)
+               float scale, int *status, bool out_bf16, int pair0)
 {
     using CF = Cfg<D, BV_>;
     constexpr int BV = CF::BV;
@@ -704,7 +704,7 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const bool producer = PW && warp == NT / 32;   // warp 8: the loads; warps 0-7: the chain
     // the value blocks of one head are neighbours in the grid, so they share
     // their [K;Q] and Z reads through L2
-    const int bh = blockIdx.x / CF::NVB;
+    const int bh = pair0 + (int)(blockIdx.x / CF::NVB);   // (sequence, head) pair
     const int b = bh / H, h = bh - b * H;
     const int v0 = (blockIdx.x % CF::NVB) * BV;
     const int n_chunks = (T + C - 1) / C;
@@ -1900,42 +1900,90 @@ bool make_map_out(CUtensorMap *map, void *base, int B, int T, int H, int d, bool
            CUDA_SUCCESS;
 }
 
-// head_dim 256, and head_dim 128 with few pairs: the chunk transform for
-// every chunk into the workspace, then the state walk (D / BV CTAs per head,
-// BV value rows each) reading it.
+}  // namespace
+
+// Value blocks of the two-kernel state walk for P (sequence, head) pairs on
+// `sms` SMs (one walk CTA per SM):
+//   - 32 rows for every pair where D / 32 CTAs per pair fit one wave: a small
+//     problem then runs twice the CTAs, each with a shorter chain per chunk;
+//   - otherwise 64 rows; when that leaves a partial last wave whose pairs fit
+//     one wave at 32 rows, the pairs of the full waves keep 64-row blocks and
+//     the rest run after them at 32 rows (a shorter last wave: at 8 x 16384
+//     tokens x 16 heads x 256, 3 full waves of 64-row blocks and 112 CTAs of
+//     32-row blocks instead of a fourth wave of 56 CTAs).
+// The walk's kernel launches are then one (pairs64 == 0 or == P) or two.
+WalkSplit walk_split(long long P, int D, int sms) {
+    WalkSplit w{0};
+    if (P <= 0 || sms <= 0) return w;
+    const long long per32 = D / 32, per64 = D / 64;
+    if (P * per32 <= sms) return w;                          // all 32-row blocks
+    w.pairs64 = (int)P;
+    const long long ctas64 = P * per64;
+    const long long full = ctas64 / sms;
+    if (full >= 1 && ctas64 % sms != 0 && (full * sms) % per64 == 0) {
+        const long long p64 = full * sms / per64;
+        if ((P - p64) * per32 <= sms) w.pairs64 = (int)p64;
+    }
+    return w;
+}
+
+namespace {
+
+// State walk over pairs pair0 .. pair0 + n_pairs - 1 with value blocks of BV
+// rows (D / BV CTAs per pair), reading the transforms in the workspace.
 template <int D, int BV, bool NORM>
-cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
+cudaError_t launch_walk_part(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
+                             const uint8_t *zws, int pair0, int n_pairs, cudaStream_t stream) {
     using CF = Cfg<D, BV>;
+    CUtensorMap mv;
+    if (!make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV)) return cudaErrorInvalidValue;
+    static PerDeviceOnce attrs;
+    const cudaError_t attr_err = attrs.run([] {
+        return cudaFuncSetAttribute(chunked_kernel<D, BV, NORM>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    chunked_kernel<D, BV, NORM><<<(unsigned)(n_pairs * CF::NVB), CF::NTH, CF::SMEM, stream>>>(
+        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
+        p.status, p.out_bf16, pair0);
+    return cudaGetLastError();
+}
+
+// head_dim 256, and head_dim 128 with few pairs: the chunk transform for
+// every chunk into the workspace, then the state walk reading it, in value
+// blocks chosen by walk_split.
+template <int D, bool NORM>
+cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
     using ZC = ZCfg<D>;
     const int n_chunks = (p.T + C - 1) / C;
     const long long n_tasks = (long long)p.B * p.H * n_chunks;
     if (!workspace || ws_bytes < (size_t)n_tasks * Z_BYTES || n_tasks > INT_MAX)
         return cudaErrorInvalidValue;
-    CUtensorMap mq, mk, mv;
-    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64) ||
-        !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64) ||
-        !make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV))
+    CUtensorMap mq, mk;
+    if (!make_map(&mq, p.q, p.B, p.T, p.Hk, D, 64) || !make_map(&mk, p.k, p.B, p.T, p.Hk, D, 64))
         return cudaErrorInvalidValue;
     static PerDeviceOnce attrs;
     const cudaError_t attr_err = attrs.run([] {
-        cudaError_t e = cudaFuncSetAttribute(chunk_z_kernel<D, NORM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chunked_kernel<D, BV, NORM>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        return e;
+        return cudaFuncSetAttribute(chunk_z_kernel<D, NORM>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, ZC::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
     uint8_t *zws = static_cast<uint8_t *>(workspace);
-    const long long z_grid = std::min<long long>(n_tasks, 3LL * current_sm_count());
+    const int sms = current_sm_count();
+    const long long z_grid = std::min<long long>(n_tasks, 3LL * sms);
     chunk_z_kernel<D, NORM><<<(unsigned)z_grid, NT, ZC::SMEM, stream>>>(
         mq, mk, p.g, p.beta, zws, p.T, p.H, p.Hk, n_chunks, (int)n_tasks, p.status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    chunked_kernel<D, BV, NORM><<<(unsigned)(p.B * p.H * CF::NVB), CF::NTH, CF::SMEM, stream>>>(
-        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
-        p.status, p.out_bf16);
-    return cudaGetLastError();
+    const WalkSplit ws = walk_split(p.B * p.H, D, sms);
+    if (ws.pairs64 > 0) {
+        e = launch_walk_part<D, 64, NORM>(p, mq, mk, zws, 0, ws.pairs64, stream);
+        if (e != cudaSuccess) return e;
+    }
+    if (ws.pairs64 < p.B * p.H)
+        e = launch_walk_part<D, 32, NORM>(p, mq, mk, zws, ws.pairs64, p.B * p.H - ws.pairs64,
+                                          stream);
+    return e;
 }
 
 template <int D, bool NORM>
@@ -2005,15 +2053,9 @@ size_t chunked_workspace_bytes(int B, int T, int H, int d, int) {
     return (size_t)B * (size_t)H * n_chunks * (size_t)Z_BYTES;
 }
 
-// The two-kernel state walk takes value blocks of 32 rows where D / 32 CTAs
-// per (sequence, head) still fit every pair into one wave on this device's
-// SMs: a small problem then runs twice the CTAs, each with half the work per
-// chunk on the chain of dependent steps.  Otherwise blocks of 64 rows.
 template <int D, bool NORM>
 cudaError_t launch_walk(const Problem &p, void *workspace, size_t ws_bytes, cudaStream_t stream) {
-    if ((long long)p.B * p.H * (D / 32) <= current_sm_count())
-        return launch_d<D, 32, NORM>(p, workspace, ws_bytes, stream);
-    return launch_d<D, 64, NORM>(p, workspace, ws_bytes, stream);
+    return launch_d<D, NORM>(p, workspace, ws_bytes, stream);
 }
 
 template <bool NORM>

@@ -77,6 +77,14 @@ size_t chunked_workspace_bytes(int B, int T, int H, int d, int dtype);
 cudaError_t launch_chunked(const Problem &p, void *workspace, size_t ws_bytes,
                            cudaStream_t stream);
 bool chunked_supports(int d);
+
+// Value blocks of the two-kernel state walk (head_dim 256, and 128 with few
+// pairs): pairs [0, pairs64) take 64-row blocks and the rest 32-row blocks,
+// launched after them.
+struct WalkSplit {
+    int pairs64;
+};
+WalkSplit walk_split(long long P, int D, int sms);
 // One CTA whose bounded wait gives up and records GDN_ERR_TIMEOUT (self-test).
 cudaError_t launch_wait_selftest(int *status, cudaStream_t stream);
 

@@ -48,6 +48,16 @@ def test_launch_counts():
     assert bench.launches_per_call("recurrent", 0) == 1
     assert bench.launches_per_call("chunked", 0) == 1          # one-kernel chunked path
     assert bench.launches_per_call("chunked", 1 << 20) == 2    # transform pass + state walk
+    # the state walk's value-block split on 152 SMs: one launch of 32-row
+    # blocks (32 pairs x 128), one of 64-row blocks filling whole waves (76
+    # pairs x 128), or full waves of 64-row blocks then the rest at 32 rows
+    # (8 x 16 pairs x 256: 114 + 14; 77 x 128: 76 + 1)
+    assert bench.launches_per_call("chunked", 1, 32, 128, 152) == 2
+    assert bench.launches_per_call("chunked", 1, 76, 128, 152) == 2
+    assert bench.launches_per_call("chunked", 1, 128, 256, 152) == 3
+    assert bench.launches_per_call("chunked", 1, 77, 128, 152) == 3
+    assert bench.launches_per_call("chunked", 1, 40, 256, 152) == 3
+    assert bench.launches_per_call("chunked", 1, 60, 256, 152) == 2    # rest of 22 > one 32-row wave
 
 
 def test_one_thread_oracle_call_keeps_the_default_thread_count():

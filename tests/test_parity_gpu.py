@@ -363,6 +363,29 @@ def test_state_walk_width_boundary(B, H, d):
     assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (e_out, e_st)
 
 
+@pytest.mark.parametrize("B,H,d", [(1, 40, 256), (2, 23, 256), (1, 77, 128)])
+def test_state_walk_mixed_value_blocks(B, H, d):
+    """When 64-row value blocks leave a partial last wave whose pairs fit one
+    wave at 32 rows, the pairs of the full waves take 64-row blocks and the
+    rest a second launch of 32-row blocks (on 152 SMs: 40 pairs at head_dim
+    256 -> 38 + 2, 46 -> 38 + 8, 77 at 128 -> 76 + 1).  Every pair, both
+    launches, against the oracle, in place, over a ragged tail."""
+    w = W.Workload(f"walkmix_b{B}_h{H}_d{d}", B, 150, H, d, "bf16", 0.0, 0.02, seed=23)
+    inp = W.make_inputs(w, "cuda")
+    ref_out, ref_st = run_oracle(inp)
+    st = inp["state"].clone()
+    out, _ = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], st,
+                         state_out=st, path="chunked")
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    o, s_ = out.double().cpu().numpy(), st.double().cpu().numpy()
+    for b in range(B):                    # each pair on its own: a wrong block is not diluted
+        for h in range(H):
+            e_out = oracle.parity_error(o[b, :, h], ref_out[b, :, h])
+            e_st = oracle.parity_error(s_[b, h], ref_st[b, h])
+            assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (b, h, e_out, e_st)
+
+
 def test_concurrent_calls_on_two_streams():
     """Two head_dim-256 chunked calls (each needs a workspace, taken
     stream-ordered from the library's pool) in flight at once on two
