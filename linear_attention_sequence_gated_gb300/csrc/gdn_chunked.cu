@@ -161,7 +161,7 @@ struct ZCfg {
     static constexpr int OFF_A = 0;                        // A, then T in place
     static constexpr int OFF_PHI = 18432;                  // P hi: 64 rows x 128 B (swizzled)
     static constexpr int OFF_PLO = OFF_PHI + 8192;         // P lo
-    static constexpr int OFF_Z = OFF_PLO + 8192;           // Z hi | Z lo (W lives here during the solve)
+    static constexpr int OFF_Z = OFF_PLO + 8192;           // Z hi | Z lo
     static constexpr int REGION = (D / 64) * 16384 > OFF_Z + Z_BYTES ? (D / 64) * 16384
                                                                      : OFF_Z + Z_BYTES;
     static constexpr int OFF_MISC = REGION;                // G, beta, 1/|k|, 1/|q|
@@ -367,6 +367,100 @@ __device__ __forceinline__ void ut_transform32(float *sAT, float *sW, int t, int
     ptx::named_sync(bar, 256);
 }
 
+// The same T = (I + A)^-1 with the off-diagonal block in one round of
+// register-resident MMAs.  Threads t = 0..255 of one stream share hardware
+// barrier `bar`; threads 0-127 also share `bar4`:
+//   1. T_00 and T_11 by column substitution (as in ut_transform32) on warps 1
+//      and 3 of the stream, which sit on the SMSPs of no issuing thread (a
+//      warp blocked issuing a product or a copy holds back the other warps
+//      of its SMSP)
+//   2. T_10 = -(T_11 A_10) T_00 by warps 0-3: warp w forms the 16-row band
+//      16 (w >> 1) of X = T_11 A_10 (all 32 columns; the two warps of a band
+//      compute it twice) and feeds its accumulators straight back as the A
+//      operand of the product with T_00, for 16 output columns 16 (w & 1).
+//      k blocks that meet only the zero triangle of T_11 or T_00 are skipped.
+// One round and two barriers instead of X through shared memory.  Same
+// operands and result as ut_transform32.  Used by chunk_z_kernel, where
+// three CTAs share an SM (8 x 16384 x 16 x 256: 4.65 -> 4.59 ms); in
+// chunked_d128_kernel, whose state stream shares the SMSPs, ut_transform32
+// measured faster.
+__device__ __forceinline__ void ut_transform32r(float *sAT, int t, int bar, int bar4) {
+    const int warp = t >> 5, lane = t & 31;
+    if ((warp == 1 || warp == 3)) {
+        const int blk = warp >> 1, j = lane;
+        float *Ab = sAT + (blk * 32) * FST + blk * 32;
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i4 = 0; i4 < 32; i4 += 4) {
+                if (i4 < r) {
+                    const float4 a = *reinterpret_cast<const float4 *>(Ab + r * FST + i4);
+                    acc[0] = fmaf(a.x, x[i4], acc[0]);
+                    if (i4 + 1 < r) acc[1] = fmaf(a.y, x[i4 + 1], acc[1]);
+                    if (i4 + 2 < r) acc[2] = fmaf(a.z, x[i4 + 2], acc[2]);
+                    if (i4 + 3 < r) acc[3] = fmaf(a.w, x[i4 + 3], acc[3]);
+                }
+            }
+            const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            x[r] = (r == j) ? 1.f : ((r > j) ? -sum : 0.f);
+        }
+        __syncwarp();                                 // every lane has read A_bb
+#pragma unroll
+        for (int r = 0; r < 32; ++r) Ab[r * FST + j] = x[r];
+    }
+    ptx::named_sync(bar, 256);
+    if (t < 128) {
+        const int g = lane >> 2, c = lane & 3;
+        const int mb = warp >> 1, nh = warp & 1;
+        // X band: rows 16 mb .. +15 of T_11 A_10 (row m of T_11 is zero past column m)
+        float d[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 32; ks += 16) {
+            if (mb == 0 && ks == 16) continue;
+            uint32_t ah[4], al[4];
+            frag_a(sAT + (32 + 16 * mb) * FST + 32 + ks, FST, lane, ah, al);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                uint32_t bh[2], bl[2];
+                frag_b(sAT + (32 + ks) * FST + 8 * nt, FST, lane, bh, bl);
+                mma3(d[nt], ah, al, bh, bl);
+            }
+        }
+        // columns 16 nh .. +15 of -X T_00 (rows 0-15 of T_00 are zero past column 15)
+        float e[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) e[nt][0] = e[nt][1] = e[nt][2] = e[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 32; ks += 16) {
+            if (nh == 1 && ks == 0) continue;
+            const int t0 = ks / 8, t1 = t0 + 1;
+            uint32_t ah[4], al[4];
+            ptx::split_pair(d[t0][0], d[t0][1], ah[0], al[0]);
+            ptx::split_pair(d[t0][2], d[t0][3], ah[1], al[1]);
+            ptx::split_pair(d[t1][0], d[t1][1], ah[2], al[2]);
+            ptx::split_pair(d[t1][2], d[t1][3], ah[3], al[3]);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t bh[2], bl[2];
+                frag_b(sAT + ks * FST + 16 * nh + 8 * nt, FST, lane, bh, bl);
+                mma3(e[nt], ah, al, bh, bl);
+            }
+        }
+        ptx::named_sync(bar4, 128);                   // every band has read A_10
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            float *o = sAT + (32 + 16 * mb) * FST + 16 * nh + 8 * nt + 2 * c;
+            *reinterpret_cast<float2 *>(o + g * FST) = make_float2(-e[nt][0], -e[nt][1]);
+            *reinterpret_cast<float2 *>(o + (g + 8) * FST) = make_float2(-e[nt][2], -e[nt][3]);
+        }
+    }
+    ptx::named_sync(bar, 256);
+}
+
 // The same T = (I + A)^-1 with four 16x16 diagonal blocks: shorter
 // column substitutions, two more rounds of MMAs.  Same operands, threads and
 // result as ut_transform32:
@@ -473,7 +567,6 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     uint8_t *sQK = sm + ZC::OFF_QK;
     float *sA = reinterpret_cast<float *>(sm + ZC::OFF_A);
     uint8_t *sPhi = sm + ZC::OFF_PHI, *sPlo = sm + ZC::OFF_PLO;
-    float *sW = reinterpret_cast<float *>(sm + ZC::OFF_Z);
     uint8_t *sZhi = sm + ZC::OFF_Z, *sZlo = sm + ZC::OFF_Z + 16384;
 
     const int tid = threadIdx.x;
@@ -606,7 +699,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         ptx::tc_fence_before();
         __syncthreads();
-        ut_transform32(sA, sW, tid, 0);               // T in place over A; W dead afterwards
+        ut_transform32r(sA, tid, 0, 1);               // T in place over A
         {                                             // T as hi / lo into Z rows 0-63
             const int r = tid >> 2, c0 = (tid & 3) * 16;
             float t[16];
