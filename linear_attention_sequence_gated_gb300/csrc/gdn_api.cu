@@ -83,8 +83,9 @@ int chunked_min_tokens(long long pairs, int head_dim) {
         case 64: return pairs < 64 ? 56 : (pairs < 256 ? 32 : (pairs < 1024 ? 40 : 56));
         // fewer than 80 pairs run the two-kernel chunked path, 80 or more the
         // one-kernel path
-        case 128: return pairs < 32 ? 64 : (pairs < 64 ? 48 : (pairs < 80 ? 40 : 24));
-        case 256: return pairs < 12 ? 48 : (pairs < 24 ? 32 : 24);
+        case 128:
+            return pairs < 32 ? 56 : (pairs < 48 ? 48 : (pairs < 64 ? 40 : (pairs < 80 ? 32 : 24)));
+        case 256: return pairs < 16 ? 40 : (pairs < 24 ? 32 : 16);
         default: return INT_MAX;
     }
 }

@@ -5,6 +5,7 @@ queries, and rejects bad arguments on the host before touching CUDA.
 Every call here that passes (made-up) device addresses is one the library
 must reject during host validation; no call in this file can reach a launch.
 """
+import math
 import ctypes
 import os
 import re
@@ -74,10 +75,12 @@ def test_workspace_and_path_queries(L):
     assert gdn.select_path(1, 4096, 32, 96) == "recurrent"            # no chunked d = 96
     # measured switch points: (pairs, head_dim) -> first chunked length
     for pairs, d, t_switch in ((32, 64, 56), (128, 64, 32), (256, 64, 40), (2048, 64, 56),
-                               (16, 128, 64), (32, 128, 48), (48, 128, 48), (64, 128, 40),
-                               (96, 128, 24), (128, 128, 24), (2048, 128, 24),
-                               (8, 256, 48), (16, 256, 32), (32, 256, 24), (256, 256, 24)):
-        B, H = (pairs // 32, 32) if pairs >= 32 else (1, pairs)
+                               (16, 128, 56), (32, 128, 48), (48, 128, 40), (64, 128, 32),
+                               (72, 128, 32), (96, 128, 24), (128, 128, 24), (2048, 128, 24),
+                               (8, 256, 40), (12, 256, 40), (16, 256, 32), (24, 256, 16),
+                               (32, 256, 16), (256, 256, 16)):
+        H = math.gcd(pairs, 32)                                       # B x H == pairs
+        B = pairs // H
         assert gdn.select_path(B, t_switch - 1, H, d) == "recurrent"
         assert gdn.select_path(B, t_switch, H, d) == "chunked"
         assert gdn.select_path(B, 4096, H, d, "f32") == "recurrent"    # chunked is bf16 only
