@@ -386,6 +386,31 @@ def test_state_walk_mixed_value_blocks(B, H, d):
             assert e_out <= TOL["bf16"] and e_st <= TOL["bf16"], (b, h, e_out, e_st)
 
 
+def test_state_walk_mixed_value_blocks_with_options():
+    """The two launches of a mixed value-block walk (on 152 SMs: 38 pairs at
+    64 rows, 2 at 32) with 8 key heads for 40 value heads, q / k normalised
+    inside the op and a bf16 output: every pair against the normalising
+    oracle, its output rounded to bf16 (a rounding of at most 2^-8 of each
+    element on top of the bf16-input bound)."""
+    w = W.Workload("walkmix_opts", 1, 150, 40, 256, "bf16", 0.0, 0.02, seed=29, Hk=8)
+    inp = raw_qk(W.make_inputs(w, "cuda"), seed=30)
+    out, st = gdn.forward(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["state"],
+                          path="chunked", l2norm_qk=True, out_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert gdn.device_status() == gdn.OK
+    assert out.dtype == torch.bfloat16
+    n = W.to_numpy_f32(inp)
+    ref_out, ref_st = oracle.recurrent_c(n["q"], n["k"], n["v"], n["g"], n["beta"], n["state"],
+                                         l2norm_qk=True)
+    o, s_ = out.double().cpu().numpy(), st.double().cpu().numpy()
+    for h in range(w.H):
+        ro = ref_out[0, :, h]
+        tol_o = TOL["bf16"] + 2.0 ** -8 * np.abs(ro).max() / max(np.sqrt((ro ** 2).mean()), 1e-30)
+        e_out = oracle.parity_error(o[0, :, h], ro)
+        e_st = oracle.parity_error(s_[0, h], ref_st[0, h])
+        assert e_out <= tol_o and e_st <= TOL["bf16"], (h, e_out, e_st)
+
+
 def test_concurrent_calls_on_two_streams():
     """Two head_dim-256 chunked calls (each needs a workspace, taken
     stream-ordered from the library's pool) in flight at once on two
