@@ -575,6 +575,10 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const int wg = tid >> 7;
     const int row = tid & 127;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    // The state walk that follows may be scheduled as soon as every CTA of
+    // this grid has started: it reads the workspace only after its grid
+    // dependency wait, which returns once this grid has completed.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (tid == 0) {
         bars.abort = 0;
@@ -931,6 +935,17 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             int c = 0;
             for (; c < n_chunks; ++c) {
                 const int sq = c % CF::NQK, sv = c % CF::NVS, sz = c % CF::NZS;
+                if (c == 0) {
+                    // chunk 0: its V and [K;Q] come from the caller's inputs;
+                    // Z is the transform kernel's output, read only once that
+                    // grid has completed (this grid may start before, as a
+                    // programmatic dependent launch)
+                    issue_v(0);
+                    issue_qk(0);
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
+                    issue_z(0);
+                    continue;
+                }
                 if (c >= CF::NVS && !ptx::mbar_wait(&bars.empty_v[sv],
                                                     (uint32_t)((c / CF::NVS - 1) & 1), abort_flag))
                     break;
@@ -1000,7 +1015,10 @@ chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!PW && n_chunks > 0) {                   // chunk 0's tiles
             if (tid == 0) issue_qk(0);
             else if (tid == 32) issue_v(0);
-            else if (tid == 64) issue_z(0);
+            else if (tid == 64) {                    // Z: once the transform grid is done
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                issue_z(0);
+            }
         }
         if (gate_thread && n_chunks > 0) {
             load_gates(0);
@@ -2024,9 +2042,13 @@ namespace {
 
 // State walk over pairs pair0 .. pair0 + n_pairs - 1 with value blocks of BV
 // rows (D / BV CTAs per pair), reading the transforms in the workspace.
+// With `pdl` the launch is a programmatic dependent launch behind the
+// transform kernel: its CTAs load their state and first tiles while the
+// transform grid finishes, and its workspace reads wait for that grid.
 template <int D, int BV, bool NORM>
 cudaError_t launch_walk_part(const Problem &p, const CUtensorMap &mq, const CUtensorMap &mk,
-                             const uint8_t *zws, int pair0, int n_pairs, cudaStream_t stream) {
+                             const uint8_t *zws, int pair0, int n_pairs, bool pdl,
+                             cudaStream_t stream) {
     using CF = Cfg<D, BV>;
     CUtensorMap mv;
     if (!make_map(&mv, p.v, p.B, p.T, p.H, D, CF::BV)) return cudaErrorInvalidValue;
@@ -2036,10 +2058,19 @@ cudaError_t launch_walk_part(const Problem &p, const CUtensorMap &mq, const CUte
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    chunked_kernel<D, BV, NORM><<<(unsigned)(n_pairs * CF::NVB), CF::NTH, CF::SMEM, stream>>>(
-        mq, mk, mv, p.g, p.beta, p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
-        p.status, p.out_bf16, pair0);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(n_pairs * CF::NVB));
+    cfg.blockDim = dim3(CF::NTH);
+    cfg.dynamicSmemBytes = CF::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunked_kernel<D, BV, NORM>, mq, mk, mv, p.g, p.beta,
+                              p.state_in, p.state_out, p.out, zws, p.T, p.H, p.Hk, p.scale,
+                              p.status, p.out_bf16, pair0);
 }
 
 // head_dim 256, and head_dim 128 with few pairs: the chunk transform for
@@ -2070,12 +2101,12 @@ cudaError_t launch_d(const Problem &p, void *workspace, size_t ws_bytes, cudaStr
     if (e != cudaSuccess) return e;
     const WalkSplit ws = walk_split(p.B * p.H, D, sms);
     if (ws.pairs64 > 0) {
-        e = launch_walk_part<D, 64, NORM>(p, mq, mk, zws, 0, ws.pairs64, stream);
+        e = launch_walk_part<D, 64, NORM>(p, mq, mk, zws, 0, ws.pairs64, true, stream);
         if (e != cudaSuccess) return e;
     }
     if (ws.pairs64 < p.B * p.H)
         e = launch_walk_part<D, 32, NORM>(p, mq, mk, zws, ws.pairs64, p.B * p.H - ws.pairs64,
-                                          stream);
+                                          ws.pairs64 == 0, stream);
     return e;
 }
 
