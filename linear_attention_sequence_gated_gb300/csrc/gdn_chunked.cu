@@ -28,9 +28,11 @@
 //     walk the state.
 //   - chunk_z_kernel + chunked_kernel (head_dim 256, and head_dim 128 with
 //     few (sequence, head) pairs): persistent CTAs write every chunk's Z to
-//     a workspace; the state walk then runs one CTA per block of 64 value
-//     rows (32 where that still fits the pairs into one wave of CTAs), keys
-//     on lanes, the fp32 state in registers.
+//     a workspace; the state walk (a dependent launch that starts while the
+//     transform finishes) then runs one CTA per block of 64 value rows (32
+//     where that still fits the pairs into one wave of CTAs, or for the
+//     pairs past the last full wave of 64-row blocks), keys on lanes, the
+//     fp32 state in registers.
 // Per chunk:
 //   1. TMA (128-byte swizzle) brings K, Q (stacked as one 128-row tile) and
 //      V; plain loads bring g, beta.
@@ -70,13 +72,6 @@ constexpr int C = 64;            // chunk length (tokens)
 constexpr int NT = 256;          // threads per CTA (two warpgroups)
 constexpr int FST = 68;          // fp32 row stride of the 64x64 scratch matrices (16-B rows)
 
-// Shared-memory and TMEM map of the state kernel (head_dim 256, and 128 with
-// few pairs).  The chunk transform Z = [T; P T] arrives ready-made from the
-// workspace (written by chunk_z_kernel), so a CTA only carries BV value rows
-// of the state: 64, or 32 to double the CTAs of a small problem.  The tiles
-// whose columns are value indices (V, S hi / lo, R / U~ hi / lo) have rows
-// of BV bf16: 128 B with the 128-byte swizzle (BV 64), 64 B with the 64-byte
-// swizzle (BV 32).
 // x[j] = TMEM column (col + j) + column (col + off + j), j < N (a multiple of
 // 16), of this warp's lane quarter: the hi- and lo-operand halves of a
 // product, summed.  16 columns of each half per wait.
@@ -93,6 +88,13 @@ __device__ __forceinline__ void tmem_ld_pair(uint32_t col, int off, float (&x)[N
     }
 }
 
+// Shared-memory and TMEM map of the state kernel (head_dim 256, and 128 with
+// few pairs).  The chunk transform Z = [T; P T] arrives ready-made from the
+// workspace (written by chunk_z_kernel), so a CTA only carries BV value rows
+// of the state: 64, or 32 to double the CTAs of a small problem.  The tiles
+// whose columns are value indices (V, S hi / lo, R / U~ hi / lo) have rows
+// of BV bf16: 128 B with the 128-byte swizzle (BV 64), 64 B with the 64-byte
+// swizzle (BV 32).
 template <int D, int BV_>
 struct Cfg {
     static constexpr int BV = BV_;                         // value rows per CTA
