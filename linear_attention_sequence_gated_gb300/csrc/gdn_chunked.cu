@@ -292,8 +292,10 @@ __device__ __forceinline__ void mma3(float (&d)[4], const uint32_t (&ah)[4], con
 // threads t = 0..255 (8 warps) sharing hardware barrier `bar`, with two
 // 32x32 diagonal blocks:
 //   1. T_00 = (I + A_00)^-1 and T_11 = (I + A_11)^-1 by column substitution
-//      on CUDA cores, one column per thread (warp 0: block 0, warp 1:
-//      block 1; every lane of a warp reads the same row of A, a broadcast)
+//      on CUDA cores, one column per thread (warp 1: block 0, warp 3:
+//      block 1, on SMSPs 1 and 3 of the stream's warps 8-15, away from the
+//      threads that issue products and copies; every lane of a warp reads
+//      the same row of A, a broadcast)
 //   2. X = T_11 A_10 (32x32, into W): eight 16 x 8 tiles, warp-level MMAs
 //   3. T_10 = -X T_00: eight tiles, warp-level MMAs
 // which is block forward substitution: A_10 T_00 + (I + A_11) T_10 = 0.
@@ -309,8 +311,9 @@ __device__ __forceinline__ void ut_transform32(float *sAT, float *sW, int t, int
     // 1. diagonal blocks: x = column j of T_bb, x[r] = -sum_{i<r} A[r][i] x[i]
     //    below the diagonal (four partial sums per row)
     float x[32];
-    const int blk = t >> 5, j = t & 31;
-    if (t < 64) {
+    const bool subst = (warp == 1 || warp == 3);
+    const int blk = (warp == 3) ? 1 : 0, j = lane;
+    if (subst) {
         const float *Ab = sAT + (blk * 32) * FST + blk * 32;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
@@ -330,7 +333,7 @@ __device__ __forceinline__ void ut_transform32(float *sAT, float *sW, int t, int
         }
     }
     ptx::named_sync(bar, 256);
-    if (t < 64) {
+    if (subst) {
         float *Tb = sAT + (blk * 32) * FST + blk * 32;
 #pragma unroll
         for (int r = 0; r < 32; ++r) Tb[r * FST + j] = x[r];
@@ -1305,6 +1308,12 @@ namespace d128 {
 constexpr int NS = 256;                 // threads per stream
 constexpr int NTH = 2 * NS;             // state stream (warps 0-7) + transform stream (8-15)
 constexpr int BAR_S = 1, BAR_Z = 2;     // hardware barrier of each stream
+// Thread of the transform stream that issues its products and mbarrier
+// arrivals: warp 10, SMSP 2.  The state stream's issuing thread (0) sits on
+// SMSP 0, and a warp blocked issuing holds back the other warps of its SMSP
+// (measured, 8 x 16384 x 64 x 64: 5.05 -> 4.98 ms against thread 0 of the
+// stream, no change on SMSP 1).
+constexpr int ZI = 64;
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int OFF_QK = 0;               // 2 stages x [K;Q] (2 slabs x 128 rows x 128 B)
 constexpr int OFF_V = 65536;            // V of one chunk (2 boxes x 64 rows x 128 B)
@@ -1573,7 +1582,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             if (t < 64) set_norms<NSLAB, NORM>(gs, sm + OFF_QK + st * 32768, t, end);
             ptx::named_sync(BAR_Z, NS);
             const bool ok = !*abort_flag;
-            if (t == 0) {
+            if (t == ZI) {
                 ptx::mbar_arrive(&sh.g_ready[c & 3]);
                 // [K;Q] K^T  (M = 128, N = 64, K = 128)
                 if (ok) {
@@ -1666,7 +1675,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::named_sync(BAR_Z, NS);
 
             // P T  (A = [P hi; P lo] 128 rows, B = T rows (MN-major), N = 64, K = 64)
-            if (t == 0 && !*abort_flag) {
+            if (t == ZI && !*abort_flag) {
                 ptx::tc_fence_after();
                 constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 64, false, true);
                 const uint32_t aP[3] = {ptx::smem_u32(sPhi), ptx::smem_u32(sPhi), ptx::smem_u32(sPlo)};
@@ -1698,7 +1707,7 @@ chunked_d128_kernel(const __grid_constant__ CUtensorMap tm_q,
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             ptx::named_sync(BAR_Z, NS);
-            if (t == 0) ptx::mbar_arrive(&sh.z_ready[st]);
+            if (t == ZI) ptx::mbar_arrive(&sh.z_ready[st]);
         }
     } else {
         // ================= state stream
