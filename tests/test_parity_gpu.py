@@ -109,7 +109,9 @@ N_SMS = 152
 def ctas_per_pair(w, path):
     """CTAs one (sequence, head) pair takes on the chunked path: the state walk
     of the two-kernel path (which needs a workspace) runs head_dim / 64
-    value-row blocks per pair, the one-kernel path one CTA per pair."""
+    value-row blocks per pair, the one-kernel path one CTA per pair.  (When
+    the walk's last pairs run as a second launch of 32-row blocks, those
+    pairs are the last range of pairs, which sampled_pairs also samples.)"""
     if path == "auto":
         path = gdn.select_path(w.B, w.T, w.H, w.d, w.dtype)
     if path == "chunked" and gdn.workspace_bytes(w.B, w.T, w.H, w.d, "bf16", "chunked"):
