@@ -609,32 +609,49 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 
     uint32_t phase = 0, mma_phase = 0;                // TMA and MMA barrier phases
     bool tma_pending = false;                         // thread 0: a load not yet waited for
-    for (int task = blockIdx.x; task < n_tasks && !*abort_flag; task += gridDim.x) {
-        const int c = task % n_chunks;
-        const int bh = task / n_chunks;
-        const int b = bh / H, h = bh - b * H;
-        const int t0 = c * C;
-        const int n = min(C, T - t0);
-
-        // 1. loads
-        if (tid == 0) {
-            constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192;
-            ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
-            tma_pending = true;
+    // A task's [K;Q] tile and gates are fetched during the task before it:
+    // the gates (threads 0-63, into registers) once that task's P T product
+    // has completed, and the tile at the same point where its bytes no longer
+    // overlap anything live (head_dim 64 and 128: the tile ends below the Z
+    // tile; at 256 it covers Z and is fetched once Z has been stored).
+    constexpr bool kTileEarly = (D / 64) * 16384 <= ZC::OFF_Z;
+    auto issue_tile = [&](int tsk) {                  // thread 0
+        const int cc = tsk % n_chunks, bbh = tsk / n_chunks;
+        const int bb = bbh / H, hh = bbh - bb * H;
+        constexpr uint32_t bytes = (uint32_t)(D / 64) * 2 * 8192;
+        ptx::mbar_arrive_expect_tx(&bars.tma, bytes);
+        tma_pending = true;
 #pragma unroll
-            for (int sl = 0; sl < D / 64; ++sl) {
-                ptx::tma_load_4d(sQK + sl * 16384, &tm_k, &bars.tma, sl * 64, h % Hk, t0, b);
-                ptx::tma_load_4d(sQK + sl * 16384 + 8192, &tm_q, &bars.tma, sl * 64, h % Hk, t0, b);
-            }
+        for (int sl = 0; sl < D / 64; ++sl) {
+            ptx::tma_load_4d(sQK + sl * 16384, &tm_k, &bars.tma, sl * 64, hh % Hk, cc * C, bb);
+            ptx::tma_load_4d(sQK + sl * 16384 + 8192, &tm_q, &bars.tma, sl * 64, hh % Hk, cc * C,
+                             bb);
         }
+    };
+    float gnext = 0.f, bnext = 0.f;                   // threads 0-63: the next task's gates
+    auto load_gates = [&](int tsk) {
+        const int cc = tsk % n_chunks, bbh = tsk / n_chunks;
+        const int bb = bbh / H, hh = bbh - bb * H;
+        gnext = 0.f;
+        bnext = 0.f;
+        if (tid < min(C, T - cc * C)) {
+            const size_t gi = ((size_t)bb * T + cc * C + tid) * H + hh;
+            gnext = g[gi];
+            bnext = beta[gi];
+        }
+    };
+    if (blockIdx.x < n_tasks) {
+        if (tid == 0) issue_tile(blockIdx.x);
+        if (tid < 64) load_gates(blockIdx.x);
+    }
+    for (int task = blockIdx.x; task < n_tasks && !*abort_flag; task += gridDim.x) {
+        const int next = task + (int)gridDim.x;
+
+        // 1. this task's gates (fetched during the task before) -> cumsum
         if (tid < 64) {
+            const float gr = fmaxf(gnext, -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
+            const float br = bnext;
             const int r = tid;
-            float gr = 0.f, br = 0.f;
-            if (r < n) {
-                const size_t gi = ((size_t)b * T + t0 + r) * H + h;
-                gr = fmaxf(g[gi], -30.f);     // exp(-30) ~ 1e-13: a reset stays a reset
-                br = beta[gi];
-            }
             float sacc = gr;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -738,6 +755,10 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (!ptx::mbar_wait(&bars.mma, mma_phase, abort_flag)) fail();
         ptx::tc_fence_after();
         mma_phase ^= 1;
+        if (next < n_tasks) {                         // the next task's inputs, in flight meanwhile
+            if (kTileEarly && tid == 0) issue_tile(next);
+            if (tid < 64) load_gates(next);
+        }
         if ((warp & 3) < 2) {                         // P T rows -> Z rows 64-127
             float pt[32];
             ptx::tmem_ld16(tmem + lane_off + wg * 32, *reinterpret_cast<float(*)[16]>(pt));
@@ -754,6 +775,7 @@ chunk_z_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             ptx::bulk_store(zws + (size_t)task * Z_BYTES, sZhi, Z_BYTES);
             ptx::bulk_commit_group();
             ptx::bulk_wait_read_all();
+            if (!kTileEarly && next < n_tasks) issue_tile(next);   // Z has left the tile's bytes
         }
         ptx::tc_fence_before();
         __syncthreads();
