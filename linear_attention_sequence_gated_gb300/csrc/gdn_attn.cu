@@ -143,6 +143,17 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// Scores are kept in log2 units (q pre-scaled by scale * log2 e, the mask by
+// log2 e), so every exponential of the softmax is a hardware 2^x; the
+// softmax is unchanged by the base.  Results below the fp32 normal range
+// flush to zero.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float exp2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // 8 consecutive elements of a row in shared memory, as fp32
 __device__ __forceinline__ void lds8(const float *p, float (&x)[8]) {
     const float4 a = *reinterpret_cast<const float4 *>(p);
@@ -292,7 +303,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int i = 0; i < ST - 1; ++i) issue(i, i);
 
-    // the CTA's rows of q, scaled, fp32 (rows past R: zeros); rows rbase + lr
+    // the CTA's rows of q, scaled by scale * log2 e, fp32 (rows past R: zeros); rows rbase + lr
     // are consecutive in q: head hk*rep + row / n_q, query row % n_q
     for (int i = tid; i < rows_cta * (DK / 8); i += NTHR) {
         const int lr = i / (DK / 8), c = i - lr * (DK / 8);
@@ -305,8 +316,9 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
         float4 *dst = reinterpret_cast<float4 *>(sQ + lr * DK + c * 8);
-        dst[0] = make_float4(scale * x[0], scale * x[1], scale * x[2], scale * x[3]);
-        dst[1] = make_float4(scale * x[4], scale * x[5], scale * x[6], scale * x[7]);
+        const float sl = scale * kLog2e;
+        dst[0] = make_float4(sl * x[0], sl * x[1], sl * x[2], sl * x[3]);
+        dst[1] = make_float4(sl * x[4], sl * x[5], sl * x[6], sl * x[7]);
     }
     __syncthreads();
 
@@ -367,7 +379,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             if (r < nr && key < nk) {
                 if (mask) {
                     const int i = (r0 + r) % n_q;
-                    sc[r] += to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]);
+                    sc[r] = fmaf(to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]), kLog2e,
+                                 sc[r]);
                 }
             } else {
                 sc[r] = -INFINITY;
@@ -385,8 +398,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         for (int r = 0; r < RG; ++r) {
             const float m_new = fmaxf(m[r], gm[r]);
             const bool none = (m_new == -INFINITY);
-            pv[r] = none ? 0.f : expf(sc[r] - m_new);
-            cf[r] = none ? 1.f : expf(m[r] - m_new);
+            pv[r] = none ? 0.f : exp2_approx(sc[r] - m_new);
+            cf[r] = none ? 1.f : exp2_approx(m[r] - m_new);
             m[r] = m_new;
             ps[r] = pv[r];
         }
@@ -447,7 +460,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         float L = 0.f;
         for (int w = g; w < NW; w += n_rgc) {
             const float mw = sm.wm[w][r];
-            const float wt = (M == -INFINITY || mw == -INFINITY) ? 0.f : expf(mw - M);
+            const float wt = (M == -INFINITY || mw == -INFINITY) ? 0.f : exp2_approx(mw - M);
             L = fmaf(wt, sm.wl[w][r], L);
             sm.wm[w][r] = wt;                         // each warp belongs to one row group
         }
@@ -479,7 +492,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
         for (int pr = 0; pr < MAX_CLUSTER; ++pr) {
             float wt = 0.f;
             if (pr < CL && M != -INFINITY && mk[pr] != -INFINITY) {
-                wt = expf(mk[pr] - M);
+                wt = exp2_approx(mk[pr] - M);
                 L = fmaf(wt, ld_peer(peer_addr(&sm.cl[tid], pr)), L);
             }
             sm.pw[tid][pr] = wt;
