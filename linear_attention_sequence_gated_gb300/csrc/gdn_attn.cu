@@ -217,6 +217,8 @@ template <int DK, int DV, typename Tin> struct Geo {
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST % 16 == 0 && STEP % 16 == 0 && QOFF % 16 == 0, "alignment");
     static_assert(DQ % 8 == 0 && KPL * NKS == 32, "score split");
+    static_assert((NKS * (DK * ELT / 16)) % 32 == 0 && (NKS * (DV * ELT / 16)) % 32 == 0,
+                  "whole copies per lane");
 };
 
 // Small per-CTA state outside the ring.
@@ -241,6 +243,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     constexpr int NKS = G::NKS, DQ = G::DQ;
     extern __shared__ __align__(16) uint8_t ring[];
     __shared__ __align__(16) SmallSmem<NW, RG, NKS> sm;
+    static_assert(G::SMEM + sizeof(sm) <= 227 * 1024, "shared memory (dynamic + static)");
     float (*wo)[RG][DV] = reinterpret_cast<float (*)[RG][DV]>(ring + G::WO);
     float (*co)[DV] = reinterpret_cast<float (*)[DV]>(ring + G::CO);
     float *sQ = reinterpret_cast<float *>(ring + G::QOFF);
@@ -285,17 +288,22 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             constexpr int CPV = DV * G::ELT / 16;     // ... per v row
             uint8_t *dk = wring + st * G::STEP;
             uint8_t *dv = dk + NKS * G::KST;
-            for (int c = lane; c < NKS * CPK; c += 32) {
-                const int g = c / CPK, x = c - g * CPK;
-                if (g < nk)
-                    cp_async16(dk + g * G::KST + x * 16,
-                               reinterpret_cast<const uint8_t *>(kg + (size_t)(j0 + g) * DK) + x * 16);
+            const uint8_t *sk = reinterpret_cast<const uint8_t *>(kg + (size_t)j0 * DK);
+            const uint8_t *sv = reinterpret_cast<const uint8_t *>(vg + (size_t)j0 * DV);
+            // copy i of this lane: piece c = lane + 32 i of the stage, row c / CP,
+            // 16-byte column c % CP; unrolled, so only the lane's first row and
+            // column are computed at run time
+#pragma unroll
+            for (int i = 0; i < NKS * CPK / 32; ++i) {
+                const int g = CPK <= 32 ? lane / CPK + i * (32 / CPK) : i / (CPK / 32);
+                const int x = CPK <= 32 ? lane % CPK : lane + 32 * (i % (CPK / 32));
+                if (g < nk) cp_async16(dk + g * G::KST + x * 16, sk + (size_t)g * (DK * G::ELT) + x * 16);
             }
-            for (int c = lane; c < NKS * CPV; c += 32) {
-                const int g = c / CPV, x = c - g * CPV;
-                if (g < nk)
-                    cp_async16(dv + g * G::VST + x * 16,
-                               reinterpret_cast<const uint8_t *>(vg + (size_t)(j0 + g) * DV) + x * 16);
+#pragma unroll
+            for (int i = 0; i < NKS * CPV / 32; ++i) {
+                const int g = CPV <= 32 ? lane / CPV + i * (32 / CPV) : i / (CPV / 32);
+                const int x = CPV <= 32 ? lane % CPV : lane + 32 * (i % (CPV / 32));
+                if (g < nk) cp_async16(dv + g * G::VST + x * 16, sv + (size_t)g * (DV * G::ELT) + x * 16);
             }
         }
         cp_async_commit();
