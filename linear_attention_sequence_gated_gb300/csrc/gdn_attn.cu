@@ -19,7 +19,12 @@
 //     memory filled by asynchronous copies (the next step's k and v land while
 //     this one is computed; no block barrier), and keeps its own online
 //     softmax (running max, sum of exp, output slice) per row;
-//   * scores: each lane (head_dim/64 lanes per key) reads its key's k row
+//   * 16-bit inputs (bf16, f16): per step of 16 keys a warp forms
+//     S^T = K Q^T and O^T += V^T P^T with warp-level tensor-core MMAs
+//     (m16n8k16, fp32 accumulators; 8 rows per warp as the N dimension):
+//     k and v feed the MMAs straight from the stage, q waits in registers,
+//     and the probabilities enter as hi + lo 16-bit pairs;
+//   * fp32 inputs: each lane (head_dim/64 lanes per key) reads its key's k row
 //     across the padded stage (one bank group per lane) against the CTA's
 //     q rows, which are broadcast from shared memory; P V: each lane owns
 //     head_dim/32 value columns and reads the step's probabilities as one
@@ -36,6 +41,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
@@ -143,6 +149,66 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// 16-byte copy that writes zeros and reads nothing (source size 0); `src` is
+// still a valid address of the range.
+__device__ __forceinline__ void cp_async16_zero(void *dst, const void *src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(0)
+                 : "memory");
+}
+
+// Warp-level tensor-core pieces of the 16-bit path.  ldmatrix hands every
+// lane its part of four 8 x 8 tiles of 16-bit elements, lanes 8i .. 8i + 7
+// naming the 16-byte rows of tile i (.trans: the tiles transposed);
+// mma.sync m16n8k16 (A row-major 16 x 16, B column-major 16 x 8) accumulates
+// in fp32.  Fragment of lane (g = lane / 4, t = lane % 4): A rows g, g + 8 and
+// columns 2t, 2t + 1, 2t + 8, 2t + 9; B columns (n) g and rows (k) 2t, 2t + 1,
+// 2t + 8, 2t + 9; C rows g, g + 8 and columns 2t, 2t + 1.
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t (&r)[4], const void *p) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(a) : "memory");
+}
+template <typename Tin>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value)
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// x0, x1 (fp32) as two 16-bit pairs, hi = (x0, x1) rounded and lo = the
+// rounded remainders, so hi + lo carries about 16 significant bits (the
+// first element in the low half, as the MMA fragments order them)
+template <typename Tin>
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+        const float2 f = __bfloat1622float2(h);
+        const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - f.x, x1 - f.y);
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    } else {
+        const __half2 h = __floats2half2_rn(x0, x1);
+        const float2 f = __half22float2(h);
+        const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+        hi = *reinterpret_cast<const uint32_t *>(&h);
+        lo = *reinterpret_cast<const uint32_t *>(&l);
+    }
+}
+constexpr int kPTS = 20;          // row stride (floats) of a warp's probabilities, [row][key]
+
 // Scores are kept in log2 units (q pre-scaled by scale * log2 e, the mask by
 // log2 e), so every exponential of the softmax is a hardware 2^x; the
 // softmax is unchanged by the base.  Results below the fp32 normal range
@@ -161,16 +227,6 @@ __device__ __forceinline__ void lds8(const float *p, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
-__device__ __forceinline__ void lds8(const __nv_bfloat16 *p, float (&x)[8]) {
-    Slice<__nv_bfloat16, 8> s;
-    ld_slice<false>(s, p);
-    unpack(s, x);
-}
-__device__ __forceinline__ void lds8(const __half *p, float (&x)[8]) {
-    Slice<__half, 8> s;
-    ld_slice<false>(s, p);
-    unpack(s, x);
-}
 // 8 consecutive elements of q in global memory, as fp32
 template <typename Tin>
 __device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
@@ -187,6 +243,11 @@ __device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
 }
 
 // Geometry for key / query width DK, value width DV and input type Tin.
+// 16-bit inputs (MMA): a step is NKS = 16 keys (the M of S^T = K Q^T and the
+//   K of O^T += V^T P^T) and a warp carries RG = 8 rows (their N); k and v
+//   rows are both padded by 16 bytes, so the 8 rows of an ldmatrix tile fall
+//   on distinct banks.
+// fp32 inputs:
 //   scores: KPL = max(DK, DV)/64 lanes share a key (each a DQ = DK/KPL-element
 //           part of its row), so a step holds NKS = 32/KPL keys, one per lane
 //           group (wide value rows keep the step, and the ring, small);
@@ -196,15 +257,17 @@ __device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
 // that lanes reading different rows hit different banks) and v.
 template <int DK, int DV, typename Tin> struct Geo {
     static constexpr int ELT = (int)sizeof(Tin);
-    static constexpr int KPL = (DK > DV ? DK : DV) / 64;
-    static constexpr int NKS = 32 / KPL;
+    static constexpr bool MMA = ELT == 2;
+    static constexpr int KPL = MMA ? 1 : (DK > DV ? DK : DV) / 64;
+    static constexpr int NKS = MMA ? 16 : 32 / KPL;
     static constexpr int DQ = DK / KPL;
     static constexpr int SL = DV / 32;
-    static constexpr int RG = 4;
+    static constexpr int RG = MMA ? 8 : 4;
     static constexpr int KST = DK * ELT + 16;
-    static constexpr int VST = DV * ELT;
+    static constexpr int VST = DV * ELT + (MMA ? 16 : 0);
     static constexpr int STEP = NKS * (KST + VST);
-    static constexpr int NW = ELT == 4 ? 4 : 8;       // warps per CTA
+    // warps per CTA: 8 while their rings take at most 200 KB
+    static constexpr int NW = ELT == 4 ? 4 : (8 * 2 * STEP <= 200 * 1024 ? 8 : 4);
     static constexpr int ST = 2;                      // ring stages per warp
     static constexpr int NTHR = NW * 32;
     static constexpr int RING = NW * ST * STEP;
@@ -213,22 +276,24 @@ template <int DK, int DV, typename Tin> struct Geo {
     static constexpr int CO = WO + NW * RG * DV * 4;              // [NW*RG][DV] fp32
     static constexpr int MERGE = CO + NW * RG * DV * 4;
     static constexpr int QOFF = RING > MERGE ? RING : MERGE;      // the CTA's q rows, fp32
-    static constexpr int SMEM = QOFF + NW * RG * DK * 4;
+    static constexpr int SMEM = QOFF + (MMA ? 0 : NW * RG * DK * 4);
     static_assert(SMEM <= 227 * 1024, "shared memory");
     static_assert(KST % 16 == 0 && STEP % 16 == 0 && QOFF % 16 == 0, "alignment");
-    static_assert(DQ % 8 == 0 && KPL * NKS == 32, "score split");
+    static_assert(MMA || (DQ % 8 == 0 && KPL * NKS == 32), "score split");
+    static_assert(!MMA || (DK % 16 == 0 && DV % 16 == 0), "MMA tiles");
     static_assert((NKS * (DK * ELT / 16)) % 32 == 0 && (NKS * (DV * ELT / 16)) % 32 == 0,
                   "whole copies per lane");
 };
 
 // Small per-CTA state outside the ring.
-template <int NW, int RG, int NKS>
+template <int NW, int RG, int NKS, bool MMA>
 struct SmallSmem {
     float wm[NW][RG], wl[NW][RG];                     // each warp's partial max (then weight), sum
     float cm[NW * RG], cl[NW * RG];                   // the CTA's partial per local row
     float pw[NW * RG][MAX_CLUSTER];                   // cluster merge: weight of each CTA per row
     float pl[NW * RG];                                // cluster merge: total sum of exp per row
-    float p[NW][NKS][RG];                             // a step's probabilities, [key][row]
+    float p[NW][MMA ? 1 : NKS][RG];                   // a step's probabilities, [key][row]
+    float pt[NW][MMA ? RG * kPTS : 1];                // ... on the MMA path, [row][key]
 };
 
 template <int DK, int DV, typename Tin>
@@ -242,7 +307,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     constexpr int SL = G::SL, RG = G::RG, NW = G::NW, ST = G::ST, NTHR = G::NTHR;
     constexpr int NKS = G::NKS, DQ = G::DQ;
     extern __shared__ __align__(16) uint8_t ring[];
-    __shared__ __align__(16) SmallSmem<NW, RG, NKS> sm;
+    __shared__ __align__(16) SmallSmem<NW, RG, NKS, G::MMA> sm;
     static_assert(G::SMEM + sizeof(sm) <= 227 * 1024, "shared memory (dynamic + static)");
     float (*wo)[RG][DV] = reinterpret_cast<float (*)[RG][DV]>(ring + G::WO);
     float (*co)[DV] = reinterpret_cast<float (*)[DV]>(ring + G::CO);
@@ -279,7 +344,8 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     const Tin *vg = v + (size_t)(b * Hkv + hk) * n_kv * DV;
     uint8_t *wring = ring + warp * ST * G::STEP;
     // stage `st` <- keys kb + NKS*step ..: k rows (padded), then v rows; rows
-    // past the range are not copied (their scores are masked, their v rows skipped)
+    // past the range are not copied (their scores are masked, their v rows
+    // skipped) or, on the MMA path, zero-filled (an MMA cannot skip a key)
     auto issue = [&](int step, int st) {
         if (step < n_steps) {
             const int j0 = kb + step * NKS;
@@ -298,12 +364,14 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                 const int g = CPK <= 32 ? lane / CPK + i * (32 / CPK) : i / (CPK / 32);
                 const int x = CPK <= 32 ? lane % CPK : lane + 32 * (i % (CPK / 32));
                 if (g < nk) cp_async16(dk + g * G::KST + x * 16, sk + (size_t)g * (DK * G::ELT) + x * 16);
+                else if constexpr (G::MMA) cp_async16_zero(dk + g * G::KST + x * 16, sk + x * 16);
             }
 #pragma unroll
             for (int i = 0; i < NKS * CPV / 32; ++i) {
                 const int g = CPV <= 32 ? lane / CPV + i * (32 / CPV) : i / (CPV / 32);
                 const int x = CPV <= 32 ? lane % CPV : lane + 32 * (i % (CPV / 32));
                 if (g < nk) cp_async16(dv + g * G::VST + x * 16, sv + (size_t)g * (DV * G::ELT) + x * 16);
+                else if constexpr (G::MMA) cp_async16_zero(dv + g * G::VST + x * 16, sv + x * 16);
             }
         }
         cp_async_commit();
@@ -311,153 +379,294 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int i = 0; i < ST - 1; ++i) issue(i, i);
 
-    // the CTA's rows of q, scaled by scale * log2 e, fp32 (rows past R: zeros); rows rbase + lr
-    // are consecutive in q: head hk*rep + row / n_q, query row % n_q
-    for (int i = tid; i < rows_cta * (DK / 8); i += NTHR) {
-        const int lr = i / (DK / 8), c = i - lr * (DK / 8);
-        const int rg = rbase + lr;
-        float x[8];
-        if (rg < R) {
-            ldg8(q + ((size_t)(b * H + hk * rep) * n_q + rg) * DK + c * 8, x);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-        float4 *dst = reinterpret_cast<float4 *>(sQ + lr * DK + c * 8);
+    if constexpr (G::MMA) {
+        // Tensor-core path.  Per step of NKS = 16 keys a warp forms
+        //   S^T  = K Q^T     (M = 16 keys, N = 8 rows, K = DK; A = the k rows
+        //                     of the stage, B = q in registers)
+        //   O^T += V^T P^T   (per 16 value columns: M = 16, N = 8 rows,
+        //                     K = 16 keys; A = the v rows transposed by
+        //                     ldmatrix, B = the probabilities as hi + lo)
+        // Lane (gi, ti) holds the S^T and O^T entries of rows 2ti and 2ti + 1
+        // of the warp, and keeps the online softmax of those two rows.
+        const int gi = lane >> 2, ti = lane & 3;
+        const int rho0 = 2 * ti;
         const float sl = scale * kLog2e;
-        dst[0] = make_float4(sl * x[0], sl * x[1], sl * x[2], sl * x[3]);
-        dst[1] = make_float4(sl * x[4], sl * x[5], sl * x[6], sl * x[7]);
-    }
-    __syncthreads();
-
-    float m[RG], l[RG];
-    float2 acc[RG][SL / 2];
+        // q as B fragments: row gi of the warp, columns 16s + 2ti (+1) and
+        // 16s + 8 + 2ti (+1); rows past the valid ones are zeros
+        uint32_t qf[DK / 16][2];
+        {
+            const bool ok = gi < nr;
+            const uint32_t *qr = reinterpret_cast<const uint32_t *>(
+                q + ((size_t)(b * H + hk * rep) * n_q + (ok ? r0 + gi : 0)) * DK);
 #pragma unroll
-    for (int r = 0; r < RG; ++r) {
-        m[r] = -INFINITY;
-        l[r] = 0.f;
+            for (int s2 = 0; s2 < DK / 16; ++s2) {
+                qf[s2][0] = ok ? __ldg(qr + s2 * 8 + ti) : 0u;
+                qf[s2][1] = ok ? __ldg(qr + s2 * 8 + 4 + ti) : 0u;
+            }
+        }
+        float oacc[DV / 16][4];
 #pragma unroll
-        for (int e = 0; e < SL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
-    }
-    const int key = lane % NKS, part = lane / NKS;    // score pass: this lane's key and row part
-    const float *qw = sQ + (rgc * RG) * DK + part * DQ;
-
-    for (int step = 0; step < n_steps; ++step) {
-        cp_async_wait<ST - 2>();                      // this step's copies (own lane) landed
-        __syncwarp();                                 // ... and every lane's
-        // refill the stage the previous step used (every lane passed the
-        // __syncwarp after reading it) while this step is computed
-        issue(step + ST - 1, (step + ST - 1) % ST);
-        const int j0 = kb + step * NKS;
-        const int nk = min(NKS, ke - j0);
-        const uint8_t *sk = wring + (step % ST) * G::STEP;
-        const Tin *sv = reinterpret_cast<const Tin *>(sk + NKS * G::KST);
-
-        // ---- scores: q . k over this lane's part of its key's row
-        float2 a2[RG];
+        for (int mt = 0; mt < DV / 16; ++mt)
 #pragma unroll
-        for (int r = 0; r < RG; ++r) a2[r] = make_float2(0.f, 0.f);
-        const Tin *krow = reinterpret_cast<const Tin *>(sk + key * G::KST) + part * DQ;
+            for (int e = 0; e < 4; ++e) oacc[mt][e] = 0.f;
+        float mr[2] = {-INFINITY, -INFINITY}, lr[2] = {0.f, 0.f};
+        float *pt = sm.pt[warp];
+        // ldmatrix row addresses: k tiles (keys lane & 15, 16-byte half lane >> 4),
+        // v tiles transposed (keys (lane & 7) + 8 (lane >> 4), half (lane >> 3) & 1)
+        const int koff = (lane & 15) * G::KST + (lane >> 4) * 16;
+        const int voff = ((lane & 7) + ((lane >> 4) << 3)) * G::VST + ((lane >> 3) & 1) * 16;
+        for (int step = 0; step < n_steps; ++step) {
+            cp_async_wait<ST - 2>();                  // this step's copies (own lane) landed
+            __syncwarp();                             // ... and every lane's
+            issue(step + ST - 1, (step + ST - 1) % ST);
+            const int j0 = kb + step * NKS;
+            const int nk = min(NKS, ke - j0);
+            const uint8_t *sk = wring + (step % ST) * G::STEP;
+            const uint8_t *sv = sk + NKS * G::KST;
+
+            // ---- S^T = K Q^T, two accumulators (even / odd column blocks)
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s2 = 0; s2 < DK / 16; ++s2) {
+                uint32_t a[4];
+                ldsm4(a, sk + koff + s2 * 32);
+                if (s2 & 1) mma16816<Tin>(sb, a, qf[s2][0], qf[s2][1]);
+                else        mma16816<Tin>(sa, a, qf[s2][0], qf[s2][1]);
+            }
+            // entry e: key gi + 8 (e >> 1), row rho0 + (e & 1); scores in log2 units
+            float sc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = gi + (e >> 1) * 8, row = rho0 + (e & 1);
+                float x = (sa[e] + sb[e]) * sl;
+                if (key < nk && row < nr) {
+                    if (mask) {
+                        const int i = (r0 + row) % n_q;
+                        x = fmaf(to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]), kLog2e, x);
+                    }
+                } else {
+                    x = -INFINITY;
+                }
+                sc[e] = x;
+            }
+            // ---- online softmax of rows rho0, rho0 + 1 (the step's 16 keys
+            //      sit on the 8 lanes of equal ti, two per lane)
+            float mx[2] = {fmaxf(sc[0], sc[2]), fmaxf(sc[1], sc[3])};
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], off));
+            float cf[2], pv[4];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float m_new = fmaxf(mr[r], mx[r]);
+                const bool none = (m_new == -INFINITY);
+                cf[r] = none ? 1.f : exp2_approx(mr[r] - m_new);
+                pv[r] = none ? 0.f : exp2_approx(sc[r] - m_new);
+                pv[r + 2] = none ? 0.f : exp2_approx(sc[r + 2] - m_new);
+                lr[r] = fmaf(lr[r], cf[r], pv[r] + pv[r + 2]);   // this lane's keys only
+                mr[r] = m_new;
+            }
+            if (__any_sync(0xffffffffu, cf[0] != 1.f || cf[1] != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < DV / 16; ++mt) {
+                    oacc[mt][0] *= cf[0]; oacc[mt][1] *= cf[1];
+                    oacc[mt][2] *= cf[0]; oacc[mt][3] *= cf[1];
+                }
+            }
+            // ---- probabilities to [row][key], read back as B fragments:
+            //      keys 2ti, 2ti + 1 and 2ti + 8, 2ti + 9 of row gi
+            pt[rho0 * kPTS + gi] = pv[0];
+            pt[(rho0 + 1) * kPTS + gi] = pv[1];
+            pt[rho0 * kPTS + gi + 8] = pv[2];
+            pt[(rho0 + 1) * kPTS + gi + 8] = pv[3];
+            __syncwarp();
+            const float2 u = *reinterpret_cast<const float2 *>(pt + gi * kPTS + 2 * ti);
+            const float2 w = *reinterpret_cast<const float2 *>(pt + gi * kPTS + 2 * ti + 8);
+            uint32_t bh0, bl0, bh1, bl1;
+            split2<Tin>(u.x, u.y, bh0, bl0);
+            split2<Tin>(w.x, w.y, bh1, bl1);
+            // ---- O^T += V^T P^T (keys past the range: zero rows, zero weights)
+#pragma unroll
+            for (int mt = 0; mt < DV / 16; ++mt) {
+                uint32_t a[4];
+                ldsm4_t(a, sv + voff + mt * 32);
+                mma16816<Tin>(oacc[mt], a, bh0, bh1);
+                mma16816<Tin>(oacc[mt], a, bl0, bl1);
+            }
+            __syncwarp();                             // stage and probabilities consumed
+        }
+        // each row's sum over the 8 lanes that hold its keys
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) lr[r] += __shfl_xor_sync(0xffffffffu, lr[r], off);
+        cp_async_wait<0>();
+        __syncthreads();                              // every warp is done with the ring
+
+        // ---- this warp's partials for the merge below
+        if (gi == 0) {
+            sm.wm[warp][rho0] = mr[0];
+            sm.wm[warp][rho0 + 1] = mr[1];
+            sm.wl[warp][rho0] = lr[0];
+            sm.wl[warp][rho0 + 1] = lr[1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < DV / 16; ++mt) {
+            wo[warp][rho0][mt * 16 + gi] = oacc[mt][0];
+            wo[warp][rho0 + 1][mt * 16 + gi] = oacc[mt][1];
+            wo[warp][rho0][mt * 16 + gi + 8] = oacc[mt][2];
+            wo[warp][rho0 + 1][mt * 16 + gi + 8] = oacc[mt][3];
+        }
+    } else {
+        // the CTA's rows of q, scaled by scale * log2 e, fp32 (rows past R: zeros); rows rbase + lr
+        // are consecutive in q: head hk*rep + row / n_q, query row % n_q
+        for (int i = tid; i < rows_cta * (DK / 8); i += NTHR) {
+            const int lr = i / (DK / 8), c = i - lr * (DK / 8);
+            const int rg = rbase + lr;
+            float x[8];
+            if (rg < R) {
+                ldg8(q + ((size_t)(b * H + hk * rep) * n_q + rg) * DK + c * 8, x);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = 0.f;
+            }
+            float4 *dst = reinterpret_cast<float4 *>(sQ + lr * DK + c * 8);
+            const float sl = scale * kLog2e;
+            dst[0] = make_float4(sl * x[0], sl * x[1], sl * x[2], sl * x[3]);
+            dst[1] = make_float4(sl * x[4], sl * x[5], sl * x[6], sl * x[7]);
+        }
+        __syncthreads();
+
+        float m[RG], l[RG];
+        float2 acc[RG][SL / 2];
+#pragma unroll
+        for (int r = 0; r < RG; ++r) {
+            m[r] = -INFINITY;
+            l[r] = 0.f;
+#pragma unroll
+            for (int e = 0; e < SL / 2; ++e) acc[r][e] = make_float2(0.f, 0.f);
+        }
+        const int key = lane % NKS, part = lane / NKS;    // score pass: this lane's key and row part
+        const float *qw = sQ + (rgc * RG) * DK + part * DQ;
+
+        for (int step = 0; step < n_steps; ++step) {
+            cp_async_wait<ST - 2>();                      // this step's copies (own lane) landed
+            __syncwarp();                                 // ... and every lane's
+            // refill the stage the previous step used (every lane passed the
+            // __syncwarp after reading it) while this step is computed
+            issue(step + ST - 1, (step + ST - 1) % ST);
+            const int j0 = kb + step * NKS;
+            const int nk = min(NKS, ke - j0);
+            const uint8_t *sk = wring + (step % ST) * G::STEP;
+            const Tin *sv = reinterpret_cast<const Tin *>(sk + NKS * G::KST);
+
+            // ---- scores: q . k over this lane's part of its key's row
+            float2 a2[RG];
+#pragma unroll
+            for (int r = 0; r < RG; ++r) a2[r] = make_float2(0.f, 0.f);
+            const Tin *krow = reinterpret_cast<const Tin *>(sk + key * G::KST) + part * DQ;
 #pragma unroll 4
-        for (int c = 0; c < DQ / 8; ++c) {
-            float kx[8];
-            lds8(krow + c * 8, kx);
+            for (int c = 0; c < DQ / 8; ++c) {
+                float kx[8];
+                lds8(krow + c * 8, kx);
+#pragma unroll
+                for (int r = 0; r < RG; ++r) {
+                    float qx[8];
+                    lds8(qw + r * DK + c * 8, qx);
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        a2[r] = ffma2(make_float2(qx[e], qx[e + 1]), make_float2(kx[e], kx[e + 1]),
+                                      a2[r]);
+                }
+            }
+            // ---- online softmax over the step's keys, all RG rows side by side
+            //      (rows past the warp's valid rows are masked out, not branched
+            //      around, so each reduction level issues RG independent shuffles)
+            float sc[RG];
+#pragma unroll
+            for (int r = 0; r < RG; ++r) sc[r] = a2[r].x + a2[r].y;
+#pragma unroll
+            for (int off = NKS; off < 32; off <<= 1)
+#pragma unroll
+                for (int r = 0; r < RG; ++r) sc[r] += __shfl_xor_sync(0xffffffffu, sc[r], off);
 #pragma unroll
             for (int r = 0; r < RG; ++r) {
-                float qx[8];
-                lds8(qw + r * DK + c * 8, qx);
-#pragma unroll
-                for (int e = 0; e < 8; e += 2)
-                    a2[r] = ffma2(make_float2(qx[e], qx[e + 1]), make_float2(kx[e], kx[e + 1]),
-                                  a2[r]);
-            }
-        }
-        // ---- online softmax over the step's keys, all RG rows side by side
-        //      (rows past the warp's valid rows are masked out, not branched
-        //      around, so each reduction level issues RG independent shuffles)
-        float sc[RG];
-#pragma unroll
-        for (int r = 0; r < RG; ++r) sc[r] = a2[r].x + a2[r].y;
-#pragma unroll
-        for (int off = NKS; off < 32; off <<= 1)
-#pragma unroll
-            for (int r = 0; r < RG; ++r) sc[r] += __shfl_xor_sync(0xffffffffu, sc[r], off);
-#pragma unroll
-        for (int r = 0; r < RG; ++r) {
-            if (r < nr && key < nk) {
-                if (mask) {
-                    const int i = (r0 + r) % n_q;
-                    sc[r] = fmaf(to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]), kLog2e,
-                                 sc[r]);
+                if (r < nr && key < nk) {
+                    if (mask) {
+                        const int i = (r0 + r) % n_q;
+                        sc[r] = fmaf(to_f32(mask[((size_t)b * n_q + i) * n_kv + j0 + key]), kLog2e,
+                                     sc[r]);
+                    }
+                } else {
+                    sc[r] = -INFINITY;
                 }
-            } else {
-                sc[r] = -INFINITY;
             }
-        }
-        float gm[RG];
+            float gm[RG];
 #pragma unroll
-        for (int r = 0; r < RG; ++r) gm[r] = sc[r];
+            for (int r = 0; r < RG; ++r) gm[r] = sc[r];
 #pragma unroll
-        for (int off = 1; off < NKS; off <<= 1)
+            for (int off = 1; off < NKS; off <<= 1)
 #pragma unroll
-            for (int r = 0; r < RG; ++r) gm[r] = fmaxf(gm[r], __shfl_xor_sync(0xffffffffu, gm[r], off));
-        float pv[RG], ps[RG], cf[RG];
+                for (int r = 0; r < RG; ++r) gm[r] = fmaxf(gm[r], __shfl_xor_sync(0xffffffffu, gm[r], off));
+            float pv[RG], ps[RG], cf[RG];
 #pragma unroll
-        for (int r = 0; r < RG; ++r) {
-            const float m_new = fmaxf(m[r], gm[r]);
-            const bool none = (m_new == -INFINITY);
-            pv[r] = none ? 0.f : exp2_approx(sc[r] - m_new);
-            cf[r] = none ? 1.f : exp2_approx(m[r] - m_new);
-            m[r] = m_new;
-            ps[r] = pv[r];
-        }
+            for (int r = 0; r < RG; ++r) {
+                const float m_new = fmaxf(m[r], gm[r]);
+                const bool none = (m_new == -INFINITY);
+                pv[r] = none ? 0.f : exp2_approx(sc[r] - m_new);
+                cf[r] = none ? 1.f : exp2_approx(m[r] - m_new);
+                m[r] = m_new;
+                ps[r] = pv[r];
+            }
 #pragma unroll
-        for (int off = 1; off < NKS; off <<= 1)
+            for (int off = 1; off < NKS; off <<= 1)
 #pragma unroll
-            for (int r = 0; r < RG; ++r) ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], off);
+                for (int r = 0; r < RG; ++r) ps[r] += __shfl_xor_sync(0xffffffffu, ps[r], off);
 #pragma unroll
-        for (int r = 0; r < RG; ++r) {
-            l[r] = fmaf(l[r], cf[r], ps[r]);
-#pragma unroll
-            for (int e = 0; e < SL / 2; ++e)
-                acc[r][e] = make_float2(acc[r][e].x * cf[r], acc[r][e].y * cf[r]);
-        }
-        static_assert(RG == 4, "one 128-bit store of the probabilities per key");
-        if (part == 0)
-            *reinterpret_cast<float4 *>(&sm.p[warp][key][0]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
-        __syncwarp();
-        // ---- P V on this lane's value columns (keys past the range skipped:
-        //      their stage rows hold stale data)
-#pragma unroll 2
-        for (int g = 0; g < nk; ++g) {
-            Slice<Tin, SL> vr;
-            ld_slice<false>(vr, sv + g * DV + lane * SL);
-            float vx[SL];
-            unpack(vr, vx);
-            const float4 p4 = *reinterpret_cast<const float4 *>(&sm.p[warp][g][0]);
-            const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int r = 0; r < RG; ++r)
+            for (int r = 0; r < RG; ++r) {
+                l[r] = fmaf(l[r], cf[r], ps[r]);
 #pragma unroll
                 for (int e = 0; e < SL / 2; ++e)
-                    acc[r][e] = ffma2(make_float2(pr[r], pr[r]), make_float2(vx[2 * e], vx[2 * e + 1]),
-                                      acc[r][e]);
+                    acc[r][e] = make_float2(acc[r][e].x * cf[r], acc[r][e].y * cf[r]);
+            }
+            static_assert(RG == 4, "one 128-bit store of the probabilities per key");
+            if (part == 0)
+                *reinterpret_cast<float4 *>(&sm.p[warp][key][0]) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+            __syncwarp();
+            // ---- P V on this lane's value columns (keys past the range skipped:
+            //      their stage rows hold stale data)
+#pragma unroll 2
+            for (int g = 0; g < nk; ++g) {
+                Slice<Tin, SL> vr;
+                ld_slice<false>(vr, sv + g * DV + lane * SL);
+                float vx[SL];
+                unpack(vr, vx);
+                const float4 p4 = *reinterpret_cast<const float4 *>(&sm.p[warp][g][0]);
+                const float pr[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+                for (int r = 0; r < RG; ++r)
+#pragma unroll
+                    for (int e = 0; e < SL / 2; ++e)
+                        acc[r][e] = ffma2(make_float2(pr[r], pr[r]), make_float2(vx[2 * e], vx[2 * e + 1]),
+                                          acc[r][e]);
+            }
+            __syncwarp();                                 // stage and probabilities consumed
         }
-        __syncwarp();                                 // stage and probabilities consumed
-    }
-    cp_async_wait<0>();
-    __syncthreads();                                  // every warp is done with the ring
+        cp_async_wait<0>();
+        __syncthreads();                                  // every warp is done with the ring
 
-    // ---- merge the warps of this CTA (same row group, different keys).  The
-    //      weights exp(m_w - M) depend only on the row: one thread per row
-    //      computes them (in place of the maxima) and the row's M and L.
+        // ---- merge the warps of this CTA (same row group, different keys).  The
+        //      weights exp(m_w - M) depend only on the row: one thread per row
+        //      computes them (in place of the maxima) and the row's M and L.
 #pragma unroll
-    for (int r = 0; r < RG; ++r) {
-        if (lane == 0) { sm.wm[warp][r] = m[r]; sm.wl[warp][r] = l[r]; }
+        for (int r = 0; r < RG; ++r) {
+            if (lane == 0) { sm.wm[warp][r] = m[r]; sm.wl[warp][r] = l[r]; }
 #pragma unroll
-        for (int e = 0; e < SL / 2; ++e) {
-            wo[warp][r][lane * SL + 2 * e] = acc[r][e].x;
-            wo[warp][r][lane * SL + 2 * e + 1] = acc[r][e].y;
+            for (int e = 0; e < SL / 2; ++e) {
+                wo[warp][r][lane * SL + 2 * e] = acc[r][e].x;
+                wo[warp][r][lane * SL + 2 * e + 1] = acc[r][e].y;
+            }
         }
     }
     __syncthreads();
