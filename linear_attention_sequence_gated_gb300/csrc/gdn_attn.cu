@@ -268,7 +268,9 @@ template <int DK, int DV, typename Tin> struct Geo {
     static constexpr int STEP = NKS * (KST + VST);
     // warps per CTA: 8 while their rings take at most 200 KB
     static constexpr int NW = ELT == 4 ? 4 : (8 * 2 * STEP <= 200 * 1024 ? 8 : 4);
-    static constexpr int ST = 2;                      // ring stages per warp
+    // ring stages per warp: three on the MMA path where they fit (its steps
+    // are short, so more copies must be in flight), else two
+    static constexpr int ST = MMA && NW * 3 * STEP <= 212 * 1024 ? 3 : 2;
     static constexpr int NTHR = NW * 32;
     static constexpr int RING = NW * ST * STEP;
     // after the key loop the ring is reused for the merge buffers
