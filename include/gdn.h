@@ -245,7 +245,9 @@ int gdn_get_device_status(gdn_stream_t stream);
  * mask: (n_seqs, 1, n_q, n_kv) dtype, additive (-inf masks a key), or NULL
  * out:  (n_seqs, n_q, n_heads, head_dim_v) float32, written by the call
  * dtype: GDN_DTYPE_F32, GDN_DTYPE_BF16 or GDN_DTYPE_F16 for q, k, v and the
- *   mask together; arithmetic is float32 with exact upcast.
+ *   mask together; accumulation is float32 and q, k, v enter exactly (for
+ *   16-bit inputs through tensor-core MMAs, the softmax weights as hi + lo
+ *   16-bit pairs, about 16 significant bits).
  * scale: finite float multiplying q . k (callers usually pass
  *   1 / sqrt(head_dim_k)).
  * Supported: 1 <= n_q <= 19 (else GDN_ERR_SHAPE), head_dim_k and head_dim_v

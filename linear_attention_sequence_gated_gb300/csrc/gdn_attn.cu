@@ -8,17 +8,18 @@
 //
 // Decode is a stream over the cache: per key, a few rows (query heads of the
 // group x queries) each take one dot product and one axpy over head_dim, so
-// the kernel is bound by HBM and by latency, not by arithmetic.  Mapping on
+// the kernel is bound by HBM once the per-key work is cheap.  Mapping on
 // sm_103a:
 //   * the R = (n_heads / n_heads_kv) * n_q rows of one kv head are cut into
 //     row groups of RG rows; one thread-block cluster of CL <= 16 CTAs serves
 //     (sequence, kv head, row block), and the cluster's CL x (warps per row
 //     group) warps split the keys into contiguous ranges; CL grows when there
 //     are few (sequence, kv head) pairs to fill the GPU with;
-//   * a warp streams its keys through its own two-stage ring of shared
-//     memory filled by asynchronous copies (the next step's k and v land while
-//     this one is computed; no block barrier), and keeps its own online
-//     softmax (running max, sum of exp, output slice) per row;
+//   * a warp streams its keys through its own ring of shared memory (three
+//     stages on the MMA path where they fit, else two) filled by asynchronous
+//     copies (the next steps' k and v land while this one is computed; no
+//     block barrier), and keeps its own online softmax (running max, sum of
+//     exp, output slice) per row;
 //   * 16-bit inputs (bf16, f16): per step of 16 keys a warp forms
 //     S^T = K Q^T and O^T += V^T P^T with warp-level tensor-core MMAs
 //     (m16n8k16, fp32 accumulators; 8 rows per warp as the N dimension):
@@ -32,8 +33,9 @@
 //   * at the end the warps of a CTA merge through shared memory and the CTAs
 //     of the cluster through distributed shared memory, so no partial result
 //     goes through global scratch.
-// Accumulation is fp32 from exactly upcast inputs (upstream accumulates in
-// f16; that is its kernel's choice, not part of the operation).
+// Accumulation is fp32; q, k and v enter exactly (upcast, or as 16-bit MMA
+// operands) and the MMA path's probabilities as hi + lo pairs (upstream
+// accumulates in f16; that is its kernel's choice, not part of the operation).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
