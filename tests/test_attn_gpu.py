@@ -98,8 +98,11 @@ def test_causal_tail_and_fully_masked_rows():
     assert np.all(got[:, 0] == 0.0) and np.all(ref[:, 0] == 0.0)
 
 
-def test_scale_argument_and_large_scores():
-    w = W.AttnWorkload("scale", 1, 4, 4, 2, 100, 256, "f32", seed=8)
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_scale_argument_and_large_scores(dtype):
+    """Peaked and uniform softmax on both kernel paths (packed FMAs for fp32,
+    tensor-core MMAs with hi + lo probabilities for 16-bit inputs)."""
+    w = W.AttnWorkload(f"scale_{dtype}", 1, 4, 4, 2, 100, 256, dtype, seed=8)
     run_and_check(w, scale=1.0)        # scores of magnitude ~ 16: a peaked softmax
     run_and_check(w, scale=0.0)        # uniform weights: the mean of v
 
