@@ -86,29 +86,26 @@ __device__ __forceinline__ float ld_peer(uint32_t addr) {
     return x;
 }
 
-// A lane's SL consecutive elements of one row (SL = head_dim / 32), raw.
+// A lane's SL consecutive fp32 elements of one row (SL = head_dim / 32), raw
+// (packed-FMA path).
 template <typename Tin, int SL>
 struct Slice {
     static constexpr int BYTES = SL * (int)sizeof(Tin);
     static constexpr int WORDS = BYTES / 4;
     uint32_t w[WORDS];
 };
-// from global memory (kGlobal) or shared memory
-template <bool kGlobal, typename Tin, int SL>
+// from shared memory
+template <typename Tin, int SL>
 __device__ __forceinline__ void ld_slice(Slice<Tin, SL> &s, const Tin *p) {
     constexpr int B = Slice<Tin, SL>::BYTES;
-    if constexpr (B == 4) {
-        s.w[0] = kGlobal ? __ldg(reinterpret_cast<const uint32_t *>(p))
-                         : *reinterpret_cast<const uint32_t *>(p);
-    } else if constexpr (B == 8) {
-        const uint2 a = kGlobal ? __ldg(reinterpret_cast<const uint2 *>(p))
-                                : *reinterpret_cast<const uint2 *>(p);
+    if constexpr (B == 8) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(p);
         s.w[0] = a.x; s.w[1] = a.y;
     } else {
+        static_assert(B % 16 == 0, "slice of 2, 4 or 8 floats");
 #pragma unroll
         for (int i = 0; i < B / 16; ++i) {
-            const uint4 a = kGlobal ? __ldg(reinterpret_cast<const uint4 *>(p) + i)
-                                    : *(reinterpret_cast<const uint4 *>(p) + i);
+            const uint4 a = *(reinterpret_cast<const uint4 *>(p) + i);
             s.w[4 * i] = a.x; s.w[4 * i + 1] = a.y; s.w[4 * i + 2] = a.z; s.w[4 * i + 3] = a.w;
         }
     }
@@ -117,23 +114,6 @@ template <int SL>
 __device__ __forceinline__ void unpack(const Slice<float, SL> &s, float (&x)[SL]) {
 #pragma unroll
     for (int i = 0; i < SL; ++i) x[i] = __uint_as_float(s.w[i]);
-}
-template <int SL>
-__device__ __forceinline__ void unpack(const Slice<__nv_bfloat16, SL> &s, float (&x)[SL]) {
-#pragma unroll
-    for (int i = 0; i < SL / 2; ++i) {
-        x[2 * i] = __uint_as_float(s.w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(s.w[i] & 0xffff0000u);
-    }
-}
-template <int SL>
-__device__ __forceinline__ void unpack(const Slice<__half, SL> &s, float (&x)[SL]) {
-#pragma unroll
-    for (int i = 0; i < SL / 2; ++i) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&s.w[i]));
-        x[2 * i] = f.x;
-        x[2 * i + 1] = f.y;
-    }
 }
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -229,19 +209,12 @@ __device__ __forceinline__ void lds8(const float *p, float (&x)[8]) {
     x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
-// 8 consecutive elements of q in global memory, as fp32
-template <typename Tin>
-__device__ __forceinline__ void ldg8(const Tin *p, float (&x)[8]) {
-    if constexpr (sizeof(Tin) == 4) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-        Slice<Tin, 8> s;
-        ld_slice<true>(s, p);
-        unpack(s, x);
-    }
+// 8 consecutive fp32 elements of q in global memory (packed-FMA path)
+__device__ __forceinline__ void ldg8(const float *p, float (&x)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // Geometry for key / query width DK, value width DV and input type Tin.
@@ -643,7 +616,7 @@ attn_decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll 2
             for (int g = 0; g < nk; ++g) {
                 Slice<Tin, SL> vr;
-                ld_slice<false>(vr, sv + g * DV + lane * SL);
+                ld_slice(vr, sv + g * DV + lane * SL);
                 float vx[SL];
                 unpack(vr, vx);
                 const float4 p4 = *reinterpret_cast<const float4 *>(&sm.p[warp][g][0]);
