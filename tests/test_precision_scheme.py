@@ -15,7 +15,9 @@ What it pins:
   * the scheme meets the bf16 parity bound (3e-3) with a tenfold margin in
     every gate regime below;
   * no term can go: dropping any one split term breaks the bound in at least
-    one regime, and so does carrying Z as a single fp16 term.
+    one regime, and so does carrying Z as a single fp16 term;
+  * for decode attention (bound 1e-4), the probabilities need their hi + lo
+    pair in the P V product: one bf16 term misses the bound.
 
 Chunk algebra (chunk of C = 64 tokens from state S0, G the in-chunk running
 sum of max(g, -30), gamma = exp(G)): A[r,i] = beta_r exp(G_r - G_i) k_r.k_i
@@ -167,3 +169,59 @@ def test_every_split_term_is_needed(name):
 def test_single_fp16_z_term_breaks_the_bound():
     errs = regime_errors(FP16_Z, FP16_Z_REGIME)
     assert max(errs) > BOUND, errs
+
+
+# ---------------------------------------------------------------- decode attention
+#
+# The attention kernel's path for 16-bit inputs forms the scores from exact
+# products (fp32 accumulation), keeps the online softmax in log2 units over
+# steps of 16 keys, and feeds the probabilities to the P V product as a
+# 16-bit hi + lo pair.  The op's bound is max-abs / RMS <= 1e-4 against the
+# float64 oracle (softmax attention as written).
+
+ATTN_BOUND = 1e-4
+LOG2E = 1.4426950408889634
+
+
+def attention_mma(q, k, v, scale, p_terms):
+    """Decode attention with the probabilities entering P V as `p_terms`
+    ('hl': bf16 hi + lo, 'h': one bf16 term); q (B, H, n_q, d), k and v
+    (B, Hkv, n_kv, d) as fp32 values of bf16 data."""
+    B, H, n_q, d = q.shape
+    Hkv, n_kv = k.shape[1], k.shape[2]
+    rep = H // Hkv
+    out = np.zeros((B, n_q, H, v.shape[3]))
+    sl = np.float32(scale * LOG2E)
+    for b, h, i in itertools.product(range(B), range(H), range(n_q)):
+        kv = h // rep
+        s = (mm(k[b, kv], q[b, h, i][:, None])[:, 0] * sl).astype(np.float32)
+        m, l = -np.inf, np.float32(0.0)
+        o = np.zeros(v.shape[3], np.float32)
+        for j0 in range(0, n_kv, 16):
+            sc = s[j0:j0 + 16]
+            m_new = max(m, float(sc.max()))
+            cf = np.float32(np.exp2(m - m_new))
+            p = np.exp2(sc - np.float32(m_new)).astype(np.float32)
+            l = np.float32(l * cf + p.sum(dtype=np.float32))
+            ph, plo = split(p)
+            pe = ph + plo if p_terms == "hl" else ph
+            o = (o * cf + mm(pe[None, :], v[b, kv, j0:j0 + 16])[0]).astype(np.float32)
+            m = m_new
+        out[b, i, h] = o / l
+    return out
+
+
+@pytest.mark.parametrize("scale", [None, 1.0])
+def test_attention_probabilities_need_hi_and_lo(scale):
+    """The hi + lo pair meets the attention bound tenfold; one bf16 term for
+    the probabilities does not meet it (scale None: 1/sqrt(d); 1.0: a peaked
+    softmax)."""
+    from oracle.attn import attention
+    w = W.AttnWorkload("prec_attn", 2, 8, 2, 1, 1000, 128, "bf16", seed=21)
+    inp = {n: x.float().numpy() for n, x in W.make_attn_inputs(w, "cpu").items() if x is not None}
+    s = float(np.float32(1.0 / np.sqrt(w.d) if scale is None else scale))
+    ref = attention(inp["q"], inp["k"], inp["v"], None, s)
+    hl = oracle.parity_error(attention_mma(inp["q"], inp["k"], inp["v"], s, "hl"), ref)
+    one = oracle.parity_error(attention_mma(inp["q"], inp["k"], inp["v"], s, "h"), ref)
+    assert hl <= ATTN_BOUND / 10, hl
+    assert one > ATTN_BOUND, one
